@@ -1,0 +1,196 @@
+"""CPU oracle for the W4A4 + LoRA quantized linear layer (ctypes wrapper).
+
+TEST INFRASTRUCTURE ONLY: imported by ``tests/``, ``__graft_entry__.smoke()``
+and the CPU-baseline leg of ``bench.py``.  The product path
+(``w4a4_quantized_gemm_gb300``) never imports it, and this package imports
+nothing from the product.
+
+The arithmetic lives in ``w4a4_oracle.c`` (plain single-threaded C, fp64 /
+int64 accumulation); this file only compiles it with gcc and marshals numpy
+arrays.  See the C file's header for the passages each function follows.
+
+Status of the pins (tests/test_oracle_pins.py):
+  * fp16 conversions          -- pinned (exhaustive + numpy's float16 cast)
+  * quantize_act/_weights     -- pinned (invariants, crafted ties, closed forms)
+  * group_partials            -- pinned (brute force, all -8 = 4096, cancellation)
+  * lora_down / linear        -- pinned (numpy fp64 matmul special cases:
+                                 rank 0, zero weights, dequantised reference)
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "w4a4_oracle.c")
+_LIB_PATH = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+GROUP = 64
+CFLAGS = ["-O2", "-std=c11", "-fPIC", "-shared", "-ffp-contract=off", "-fno-fast-math",
+          "-fno-unsafe-math-optimizations", "-frounding-math"]
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle into oracle/liboracle.so (gcc, portable flags)."""
+    if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
+        tmp = _LIB_PATH + f".tmp{os.getpid()}"
+        subprocess.run(["gcc", *CFLAGS, "-o", tmp, _SRC, "-lm"], check=True)
+        os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        lib = ctypes.CDLL(build())
+        P = ctypes.c_void_p
+        I = ctypes.c_int64
+        lib.oracle_f16_to_f32.argtypes = [ctypes.c_uint16]
+        lib.oracle_f16_to_f32.restype = ctypes.c_float
+        lib.oracle_f32_to_f16.argtypes = [ctypes.c_float]
+        lib.oracle_f32_to_f16.restype = ctypes.c_uint16
+        lib.oracle_quantize_act.argtypes = [P, I, I, P, P]
+        lib.oracle_quantize_weights.argtypes = [P, I, I, P, P]
+        lib.oracle_group_partials.argtypes = [P, P, I, I, I, P]
+        lib.oracle_group_partials.restype = I
+        lib.oracle_lora_down.argtypes = [P, P, I, I, I, P]
+        lib.oracle_linear_from_codes.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, P]
+        lib.oracle_linear_sampled.argtypes = [P, P, P, P, P, P, I, I, I, I, P, P, I, P, P, P, P, P, P]
+        _lib = lib
+        return lib
+
+
+def _ptr(a: np.ndarray):
+    assert a.flags["C_CONTIGUOUS"]
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _c(a, dtype):
+    return np.ascontiguousarray(np.asarray(a, dtype=dtype))
+
+
+def f16_to_f32(h: int) -> float:
+    return float(_load().oracle_f16_to_f32(int(h)))
+
+
+def f32_to_f16(x: float) -> int:
+    return int(_load().oracle_f32_to_f16(float(np.float32(x))))
+
+
+def f16_to_f32_array(h: np.ndarray) -> np.ndarray:
+    lib = _load()
+    flat = np.asarray(h, dtype=np.uint16).ravel()
+    out = np.fromiter((lib.oracle_f16_to_f32(int(v)) for v in flat), dtype=np.float32, count=flat.size)
+    return out.reshape(np.shape(h))
+
+
+def quantize_act(X: np.ndarray):
+    """X: fp16 bits [M, K] -> (codes int8 [M, K], scales fp32 [M, K/64])."""
+    X = _c(X, np.uint16)
+    M, K = X.shape
+    assert K % GROUP == 0
+    q = np.empty((M, K), np.int8)
+    s = np.empty((M, K // GROUP), np.float32)
+    _load().oracle_quantize_act(_ptr(X), M, K, _ptr(q), _ptr(s))
+    return q, s
+
+
+def quantize_weights(W: np.ndarray):
+    """W: fp32 [N, K] -> (codes int8 [N, K], scales fp16 bits [N, K/64])."""
+    W = _c(W, np.float32)
+    N, K = W.shape
+    assert K % GROUP == 0
+    q = np.empty((N, K), np.int8)
+    s = np.empty((N, K // GROUP), np.uint16)
+    _load().oracle_quantize_weights(_ptr(W), N, K, _ptr(q), _ptr(s))
+    return q, s
+
+
+def group_partials(qA: np.ndarray, qW: np.ndarray) -> np.ndarray:
+    """int32 [M, N, K/64] exact per-group integer dot products."""
+    qA = _c(qA, np.int8)
+    qW = _c(qW, np.int8)
+    M, K = qA.shape
+    N, K2 = qW.shape
+    assert K == K2 and K % GROUP == 0
+    P = np.empty((M, N, K // GROUP), np.int32)
+    bad = _load().oracle_group_partials(_ptr(qA), _ptr(qW), M, N, K, _ptr(P))
+    assert bad == 0, f"{bad} partial sums overflow int32"
+    return P
+
+
+def lora_down(X: np.ndarray, L_down: np.ndarray) -> np.ndarray:
+    """fp64 [M, r] = X (fp16) @ L_down (fp16 [K, r])."""
+    X = _c(X, np.uint16)
+    Ld = _c(L_down, np.uint16)
+    M, K = X.shape
+    K2, r = Ld.shape if Ld.ndim == 2 else (K, 0)
+    assert K2 == K
+    D = np.zeros((M, r), np.float64)
+    if r:
+        _load().oracle_lora_down(_ptr(X), _ptr(Ld), M, K, r, _ptr(D))
+    return D
+
+
+def linear_from_codes(qA, sA, qW, sW, D, L_up, colscale, bias) -> np.ndarray:
+    qA = _c(qA, np.int8); sA = _c(sA, np.float32)
+    qW = _c(qW, np.int8); sW = _c(sW, np.uint16)
+    M, K = qA.shape
+    N = qW.shape[0]
+    D = _c(D, np.float64).reshape(M, -1)
+    r = D.shape[1]
+    Lup = _c(L_up, np.uint16).reshape(r, N) if r else np.zeros((0, N), np.uint16)
+    cs = _c(colscale, np.uint16); b = _c(bias, np.uint16)
+    Y = np.empty((M, N), np.float64)
+    _load().oracle_linear_from_codes(_ptr(qA), _ptr(sA), _ptr(qW), _ptr(sW), _ptr(D), _ptr(Lup),
+                                     _ptr(cs), _ptr(b), M, N, K, r, _ptr(Y))
+    return Y
+
+
+class Reference:
+    """Every intermediate of the oracle for one layer (small and medium sizes)."""
+
+    def __init__(self, X, W, L_down, L_up, colscale, bias):
+        self.qA, self.sA = quantize_act(X)
+        self.qW, self.sW = quantize_weights(W)
+        self.D = lora_down(X, L_down)
+        self.Y = linear_from_codes(self.qA, self.sA, self.qW, self.sW, self.D, L_up, colscale, bias)
+
+    def partials(self):
+        return group_partials(self.qA, self.qW)
+
+
+def linear(X, W, L_down, L_up, colscale, bias) -> np.ndarray:
+    """fp64 Y [M, N] of the whole layer from raw inputs."""
+    return Reference(X, W, L_down, L_up, colscale, bias).Y
+
+
+def linear_sampled(X, W, L_down, L_up, colscale, bias, rows, cols) -> np.ndarray:
+    """fp64 Y[rows[i], cols[i]] from raw inputs (sorted by row for reuse)."""
+    X = _c(X, np.uint16); W = _c(W, np.float32)
+    M, K = X.shape
+    N = W.shape[0]
+    r = 0 if L_down is None else np.asarray(L_down).reshape(K, -1).shape[1]
+    Ld = _c(L_down, np.uint16).reshape(K, r) if r else np.zeros((K, 0), np.uint16)
+    Lup = _c(L_up, np.uint16).reshape(r, N) if r else np.zeros((0, N), np.uint16)
+    rows = _c(rows, np.int64); cols = _c(cols, np.int64)
+    order = np.lexsort((cols, rows))
+    rs, cs_ = np.ascontiguousarray(rows[order]), np.ascontiguousarray(cols[order])
+    out = np.empty(rows.size, np.float64)
+    qa = np.empty(K, np.int8); sa = np.empty(K // GROUP, np.float32)
+    qw = np.empty(K, np.int8); sw = np.empty(K // GROUP, np.uint16)
+    d = np.zeros(max(r, 1), np.float64)
+    _load().oracle_linear_sampled(_ptr(X), _ptr(W), _ptr(Ld), _ptr(Lup), _ptr(_c(colscale, np.uint16)),
+                                  _ptr(_c(bias, np.uint16)), M, N, K, r, _ptr(rs), _ptr(cs_), rows.size,
+                                  _ptr(qa), _ptr(sa), _ptr(qw), _ptr(sw), _ptr(d), _ptr(out))
+    res = np.empty_like(out)
+    res[order] = out
+    return res

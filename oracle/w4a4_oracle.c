@@ -1,0 +1,209 @@
+/*
+ * CPU oracle for the W4A4 + LoRA quantized linear layer.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Tests, the smoke check and the CPU-baseline leg
+ * of the benchmark call this file; the product path never does.  It shares no
+ * code, header, table or constant with the CUDA library.
+ *
+ * Plain, single-threaded, loop-by-loop code: every function is the definition
+ * of one step written out, accumulating in int64 (integer products) or fp64
+ * (everything scaled).  Build with -ffp-contract=off and without fast-math so
+ * that every float operation is one IEEE binary32 operation with
+ * round-to-nearest-even.
+ *
+ * What it computes (page citations by page title and section):
+ *   Y[m,n] = colscale[n] * ( sum_g sA[m,g] sW[n,g] P[m,n,g]
+ *                            + sum_j D[m,j] L_up[j,n] ) + bias[n]
+ *   P[m,n,g] = sum_{k in group g} qA[m,k] qW[n,k]          (exact integers)
+ *   D[m,j]   = sum_k X[m,k] L_down[k,j]                    (unquantised X)
+ * - activation quantiser: "W4A4 CUDA Kernel for Voice Clone", 3.6
+ *   (fused_quantize_repack_act_kernel): absmax per 64-column group,
+ *   scale = max(absmax/7, 1e-10), q = clamp(round-half-even(x/scale), -8, 7);
+ * - weight quantiser: same post, 2.1 and 2.3 (round(W/scale), fp16
+ *   per-group-64 scales);
+ * - per-group integer products, scaled per group and summed: same post, 3.7;
+ * - LoRA down from the unquantised X, LoRA up added to the same output
+ *   accumulator: same post, 3.6 and 3.7;
+ * - column-wise affine after the low-rank residual: "High-Performance Kernel
+ *   Design for W4A4 ... on Blackwell Architecture", section 1.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+
+#define OR_GROUP 64
+
+/* ---- fp16 <-> fp32, written from the IEEE 754 binary16 definition ------ */
+
+/* binary16 bits -> value (exact). */
+float oracle_f16_to_f32(uint16_t h) {
+    int s = h >> 15, e = (h >> 10) & 31, m = h & 1023;
+    double v;
+    if (e == 0) v = ldexp((double)m, -24);                 /* subnormal / zero */
+    else if (e == 31) v = m ? NAN : INFINITY;
+    else v = ldexp((double)(m + 1024), e - 25);             /* (1.m) 2^(e-15) */
+    return (float)(s ? -v : v);
+}
+
+/* value -> nearest binary16, ties to even (overflow to infinity). */
+uint16_t oracle_f32_to_f16(float f) {
+    uint32_t x;
+    memcpy(&x, &f, 4);
+    uint16_t sign = (uint16_t)((x >> 16) & 0x8000u);
+    uint32_t ax = x & 0x7fffffffu;
+    if (ax > 0x7f800000u) return (uint16_t)(sign | 0x7e00u);   /* NaN */
+    if (ax == 0x7f800000u) return (uint16_t)(sign | 0x7c00u);  /* inf */
+    double v = fabs((double)f);
+    if (v >= 65520.0) return (uint16_t)(sign | 0x7c00u);      /* past 65504 + half a step */
+    int e2;
+    frexp(v, &e2);                        /* v in [2^(e2-1), 2^e2) */
+    int be = e2 - 1;
+    if (v == 0.0 || be < -14) be = -14;   /* subnormals share the smallest binade's step */
+    double quantum = ldexp(1.0, be - 10); /* spacing of binary16 numbers there */
+    double n = rint(v / quantum);         /* exact scaling; rint ties to even */
+    uint32_t bits;
+    if (be == -14 && n < 1024.0) {
+        bits = (uint32_t)n;               /* subnormal or zero */
+    } else {
+        if (n == 2048.0) { be += 1; n = 1024.0; }
+        bits = ((uint32_t)(be + 15) << 10) | ((uint32_t)n - 1024u);
+    }
+    return (uint16_t)(sign | bits);
+}
+
+static int8_t clamp_code(float q) {
+    if (q < -8.0f) q = -8.0f;
+    if (q > 7.0f) q = 7.0f;
+    return (int8_t)q;
+}
+
+/* ---- activation quantiser (Voice Clone post, 3.6) ------------------------
+ * X: fp16 bits [M, K]; qA: int8 codes [M, K]; sA: fp32 [M, K/64].          */
+void oracle_quantize_act(const uint16_t* X, int64_t M, int64_t K, int8_t* qA, float* sA) {
+    int64_t G = K / OR_GROUP;
+    for (int64_t m = 0; m < M; ++m) {
+        for (int64_t g = 0; g < G; ++g) {
+            const uint16_t* x = X + m * K + g * OR_GROUP;
+            float amax = 0.0f;
+            for (int k = 0; k < OR_GROUP; ++k) {
+                float v = fabsf(oracle_f16_to_f32(x[k]));
+                if (v > amax) amax = v;
+            }
+            float s = amax / 7.0f;
+            if (s < 1e-10f) s = 1e-10f;
+            sA[m * G + g] = s;
+            for (int k = 0; k < OR_GROUP; ++k)
+                qA[m * K + g * OR_GROUP + k] = clamp_code(rintf(oracle_f16_to_f32(x[k]) / s));
+        }
+    }
+}
+
+/* ---- weight quantiser (Voice Clone post, 2.1 / 2.3) ----------------------
+ * W: fp32 [N, K]; qW: int8 codes [N, K]; sW: fp16 bits [N, K/64].
+ * The scale is absmax/7 rounded to fp16 and floored at 2^-14 (the smallest
+ * normal fp16); codes are taken against the stored fp16 scale.             */
+void oracle_quantize_weights(const float* W, int64_t N, int64_t K, int8_t* qW, uint16_t* sW) {
+    int64_t G = K / OR_GROUP;
+    for (int64_t n = 0; n < N; ++n) {
+        for (int64_t g = 0; g < G; ++g) {
+            const float* w = W + n * K + g * OR_GROUP;
+            float amax = 0.0f;
+            for (int k = 0; k < OR_GROUP; ++k) {
+                float v = fabsf(w[k]);
+                if (v > amax) amax = v;
+            }
+            float s32 = amax / 7.0f;
+            if (s32 < 0x1p-14f) s32 = 0x1p-14f;
+            uint16_t h = oracle_f32_to_f16(s32);
+            sW[n * G + g] = h;
+            float s = oracle_f16_to_f32(h);
+            for (int k = 0; k < OR_GROUP; ++k)
+                qW[n * K + g * OR_GROUP + k] = clamp_code(rintf(w[k] / s));
+        }
+    }
+}
+
+/* ---- per-group integer dot products (Voice Clone post, 3.7 phase 1) -----
+ * P[m, n, g] = sum over the 64 k of group g of qA[m,k] qW[n,k].  Returns the
+ * number of partials that do not fit int32 (always 0 for 4-bit codes).     */
+int64_t oracle_group_partials(const int8_t* qA, const int8_t* qW, int64_t M, int64_t N, int64_t K,
+                              int32_t* P) {
+    int64_t G = K / OR_GROUP, bad = 0;
+    for (int64_t m = 0; m < M; ++m)
+        for (int64_t n = 0; n < N; ++n)
+            for (int64_t g = 0; g < G; ++g) {
+                int64_t acc = 0;
+                for (int k = 0; k < OR_GROUP; ++k)
+                    acc += (int64_t)qA[m * K + g * OR_GROUP + k] * (int64_t)qW[n * K + g * OR_GROUP + k];
+                if (acc > INT32_MAX || acc < INT32_MIN) ++bad;
+                P[(m * N + n) * G + g] = (int32_t)acc;
+            }
+    return bad;
+}
+
+/* ---- LoRA down-projection from the unquantised X (3.6, LoRA branch) -----
+ * D[m, j] = sum_k X[m,k] L_down[k,j] in fp64.                              */
+void oracle_lora_down(const uint16_t* X, const uint16_t* Ld, int64_t M, int64_t K, int64_t r, double* D) {
+    for (int64_t m = 0; m < M; ++m)
+        for (int64_t j = 0; j < r; ++j) {
+            double acc = 0.0;
+            for (int64_t k = 0; k < K; ++k)
+                acc += (double)oracle_f16_to_f32(X[m * K + k]) * (double)oracle_f16_to_f32(Ld[k * r + j]);
+            D[m * r + j] = acc;
+        }
+}
+
+/* ---- output of one element from quantised operands ----------------------
+ * main = sum_g sA sW P ; lora = sum_j D L_up ; y = cs (main + lora) + bias. */
+static double output_element(const int8_t* qa_row, const float* sa_row, const int8_t* qw_row,
+                             const uint16_t* sw_row, const double* d_row, const uint16_t* Lup,
+                             int64_t n, int64_t N, int64_t K, int64_t r, uint16_t cs, uint16_t bias) {
+    int64_t G = K / OR_GROUP;
+    double main_sum = 0.0;
+    for (int64_t g = 0; g < G; ++g) {
+        int64_t p = 0;
+        for (int k = 0; k < OR_GROUP; ++k)
+            p += (int64_t)qa_row[g * OR_GROUP + k] * (int64_t)qw_row[g * OR_GROUP + k];
+        main_sum += (double)sa_row[g] * (double)oracle_f16_to_f32(sw_row[g]) * (double)p;
+    }
+    double lora = 0.0;
+    for (int64_t j = 0; j < r; ++j) lora += d_row[j] * (double)oracle_f16_to_f32(Lup[j * N + n]);
+    return (double)oracle_f16_to_f32(cs) * (main_sum + lora) + (double)oracle_f16_to_f32(bias);
+}
+
+/* Y (fp64) from already-quantised operands and D (all [row-major]). */
+void oracle_linear_from_codes(const int8_t* qA, const float* sA, const int8_t* qW, const uint16_t* sW,
+                              const double* D, const uint16_t* Lup, const uint16_t* cs,
+                              const uint16_t* bias, int64_t M, int64_t N, int64_t K, int64_t r,
+                              double* Y) {
+    int64_t G = K / OR_GROUP;
+    for (int64_t m = 0; m < M; ++m)
+        for (int64_t n = 0; n < N; ++n)
+            Y[m * N + n] = output_element(qA + m * K, sA + m * G, qW + n * K, sW + n * G, D + m * r, Lup,
+                                          n, N, K, r, cs[n], bias[n]);
+}
+
+/* Selected outputs (rows[i], cols[i]) of the full layer, from the raw inputs.
+ * Quantises only the rows and columns it needs: used at sizes where the whole
+ * product is too slow for a single CPU thread.                              */
+void oracle_linear_sampled(const uint16_t* X, const float* W, const uint16_t* Ld, const uint16_t* Lup,
+                           const uint16_t* cs, const uint16_t* bias, int64_t M, int64_t N, int64_t K,
+                           int64_t r, const int64_t* rows, const int64_t* cols, int64_t ns,
+                           int8_t* qa_buf /*K*/, float* sa_buf /*K/64*/, int8_t* qw_buf /*K*/,
+                           uint16_t* sw_buf /*K/64*/, double* d_buf /*r*/, double* out) {
+    (void)M;
+    int64_t last_row = -1, last_col = -1;
+    for (int64_t i = 0; i < ns; ++i) {
+        int64_t m = rows[i], n = cols[i];
+        if (m != last_row) {
+            oracle_quantize_act(X + m * K, 1, K, qa_buf, sa_buf);
+            if (r > 0) oracle_lora_down(X + m * K, Ld, 1, K, r, d_buf);
+            last_row = m;
+        }
+        if (n != last_col) {
+            oracle_quantize_weights(W + n * K, 1, K, qw_buf, sw_buf);
+            last_col = n;
+        }
+        out[i] = output_element(qa_buf, sa_buf, qw_buf, sw_buf, d_buf, Lup, n, N, K, r, cs[n], bias[n]);
+    }
+}

@@ -1,0 +1,251 @@
+"""Pins of the CPU oracle against facts that do not come from the oracle itself.
+
+Each test checks one oracle function against a closed form, an invariant, a
+brute-force computation, a library routine on a special case, or a value fixed
+by hand from the rules on the pages (fixtures under tests/golden/, each with its
+citation).  A plausible mistake in the oracle (truncation instead of
+ties-to-even, a /8 instead of /7, a transposed operand, a dropped LoRA term, a
+wrong bias sign, fp16 scale rounding in the wrong direction) fails at least one.
+"""
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+from synthetic import make_linear_case, random_codes
+
+GOLD = os.path.join(os.path.dirname(__file__), "golden")
+G = 64
+
+
+def _f16(vals):
+    return np.asarray(vals, np.float32).astype(np.float16).view(np.uint16)
+
+
+# ---------------------------------------------------------------- fp16 routines
+def test_f16_decode_matches_numpy_all_patterns():
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    ref = bits.view(np.float16).astype(np.float32)
+    ours = oracle.f16_to_f32_array(bits)
+    finite = np.isfinite(ref)
+    assert np.array_equal(ours[finite], ref[finite])
+    assert np.array_equal(np.isnan(ours), np.isnan(ref))
+    assert np.array_equal(np.isinf(ours), np.isinf(ref))
+
+
+def test_f16_roundtrip_exhaustive():
+    for h in range(65536):
+        e = (h >> 10) & 31
+        if e == 31 and (h & 1023):
+            continue  # NaN payloads are not preserved (canonical quiet NaN)
+        assert oracle.f32_to_f16(oracle.f16_to_f32(h)) == h, hex(h)
+
+
+def test_f16_encode_matches_numpy_rne():
+    rng = np.random.default_rng(1)
+    vals = np.concatenate([
+        rng.standard_normal(20000).astype(np.float32) * np.float32(3.0),
+        (rng.standard_normal(5000) * 1e-5).astype(np.float32),       # subnormal range
+        (rng.standard_normal(2000) * 3e4).astype(np.float32),        # near overflow
+    ])
+    # exact midpoints between neighbouring fp16 values: ties must go to even
+    h = np.arange(1, 0x7BFF, 97, dtype=np.uint16)
+    lo = h.view(np.float16).astype(np.float64)
+    hi = (h + 1).view(np.float16).astype(np.float64)
+    mids = ((lo + hi) / 2).astype(np.float32)
+    vals = np.concatenate([vals, mids, -mids, np.float32([65504, 65519.9, 65520, 6.1e-5, 0.0, -0.0])])
+    ref = vals.astype(np.float16).view(np.uint16)
+    ours = np.array([oracle.f32_to_f16(v) for v in vals], np.uint16)
+    assert np.array_equal(ours, ref)
+
+
+# ---------------------------------------------------------- activation quantiser
+def _read_ties():
+    cases = []
+    with open(os.path.join(GOLD, "act_quant_ties.txt")) as f:
+        for line in f:
+            if line.startswith("#") or not line.strip():
+                continue
+            gid, scale, xs, qs = [p.strip() for p in line.split("|")]
+            cases.append((int(gid), np.float32(float(scale)),
+                          [float(v) for v in xs.split()], [int(v) for v in qs.split()]))
+    return cases
+
+
+def test_act_quant_crafted_ties_golden():
+    cases = _read_ties()
+    X = np.zeros((1, G * len(cases)), np.float32)
+    for gid, _, xs, _ in cases:
+        X[0, gid * G: gid * G + len(xs)] = xs
+    q, s = oracle.quantize_act(_f16(X))
+    for gid, scale, xs, qs in cases:
+        assert s[0, gid] == scale, (gid, s[0, gid], scale)
+        exp = np.zeros(G, np.int8)
+        exp[: len(qs)] = qs
+        assert np.array_equal(q[0, gid * G:(gid + 1) * G], exp), gid
+
+
+def test_act_quant_invariants():
+    c = make_linear_case(96, 1024, 64, 32, seed=3)
+    q, s = oracle.quantize_act(c.X)
+    x = c.X.view(np.float16).astype(np.float64).reshape(96, 16, G)
+    qq = q.astype(np.float64).reshape(96, 16, G)
+    ss = s.astype(np.float64)[..., None]
+    # reconstruction error within half a step (plus the rounding of x/s)
+    assert np.all(np.abs(x - qq * ss) <= ss * (0.5 + 1e-6))
+    # codes in [-7, 7]; the group's absmax element maps to +-7 with its sign
+    assert q.min() >= -7 and q.max() <= 7
+    am = np.abs(x).argmax(axis=2)
+    top = np.take_along_axis(qq, am[..., None], axis=2)[..., 0]
+    sign = np.sign(np.take_along_axis(x, am[..., None], axis=2)[..., 0])
+    assert np.array_equal(top, 7 * sign)
+    # scale is absmax/7 in fp32
+    amax = np.abs(x).max(axis=2).astype(np.float32)
+    assert np.array_equal(s, np.maximum(amax / np.float32(7), np.float32(1e-10)))
+
+
+# -------------------------------------------------------------- weight quantiser
+def test_weight_quant_closed_forms_golden():
+    rows = []
+    with open(os.path.join(GOLD, "weight_quant_closed_forms.txt")) as f:
+        for line in f:
+            if line.startswith("#") or not line.strip():
+                continue
+            name, amax, bits, val, code = [p.strip() for p in line.split("|")]
+            rows.append((name, np.float32(float(amax)), int(bits, 16), float(val), int(code)))
+    W = np.zeros((len(rows), G), np.float32)
+    for i, (_, amax, _, _, _) in enumerate(rows):
+        W[i, 5] = amax
+        W[i, 9] = -amax * np.float32(0.5)
+    q, s = oracle.quantize_weights(W)
+    for i, (name, amax, bits, val, code) in enumerate(rows):
+        assert int(s[i, 0]) == bits, name
+        assert oracle.f16_to_f32(bits) == val, name
+        assert q[i, 5] == code, name
+
+
+def test_weight_quant_identity_closed_form():
+    K = 256
+    W = np.eye(K, dtype=np.float32)
+    q, s = oracle.quantize_weights(W)
+    for n in range(K):
+        for g in range(K // G):
+            if g == n // G:
+                assert s[n, g] == 0x3092  # fp16(1/7) = 0.142822265625
+            else:
+                assert s[n, g] == 0x0400  # floor 2^-14
+    assert np.array_equal(q, 7 * np.eye(K, dtype=np.int8))
+
+
+def test_weight_quant_invariants():
+    rng = np.random.default_rng(5)
+    W = (rng.standard_normal((64, 512)) * 0.02).astype(np.float32)
+    q, s = oracle.quantize_weights(W)
+    sv = s.view(np.float16).astype(np.float64)[..., None]
+    w = W.astype(np.float64).reshape(64, 8, G)
+    qq = q.astype(np.float64).reshape(64, 8, G)
+    assert np.all(np.abs(w - qq * sv) <= sv * (0.5 + 1e-6))
+    assert q.min() >= -8 and q.max() <= 7
+    # fp16 scale = round-to-nearest of absmax/7 (numpy's RNE cast is the check)
+    amax = np.abs(w).max(axis=2).astype(np.float32)
+    exp = np.maximum(amax / np.float32(7), np.float32(2 ** -14)).astype(np.float16).view(np.uint16)
+    assert np.array_equal(s, exp)
+
+
+# ------------------------------------------------------------ integer partials
+def test_group_partials_bruteforce_8x8x128():
+    rng = np.random.default_rng(7)
+    qA = random_codes(rng, (8, 128))
+    qW = random_codes(rng, (8, 128))
+    P = oracle.group_partials(qA, qW)
+    for m in range(8):
+        for n in range(8):
+            for g in range(2):
+                acc = 0
+                for k in range(g * G, (g + 1) * G):
+                    acc += int(qA[m, k]) * int(qW[n, k])
+                assert P[m, n, g] == acc
+
+
+def test_group_partials_extremes():
+    qA = np.full((2, 128), -8, np.int8)
+    qW = np.full((3, 128), -8, np.int8)
+    assert np.all(oracle.group_partials(qA, qW) == 4096)
+    alt = np.tile(np.array([7, -7], np.int8), 64)[None, :]
+    assert np.all(oracle.group_partials(alt, np.full((1, 128), 5, np.int8)) == 0)
+    # distinct rows/cols give distinct partials: a transposed operand would fail
+    qA = np.zeros((2, 64), np.int8); qA[0, 0] = 1; qA[1, 1] = 1
+    qW = np.zeros((3, 64), np.int8); qW[0, 0] = 2; qW[1, 1] = 3; qW[2, 0] = 5
+    assert oracle.group_partials(qA, qW)[:, :, 0].tolist() == [[2, 0, 5], [0, 3, 0]]
+
+
+# --------------------------------------------------------------- whole layer
+def _dequant_reference(c, qA, sA, qW, sW, r=True):
+    """Y from a dense fp64 matmul of the dequantised operands (the validation
+    recipe of "INT4 Kernel Architecture, in depth", Failure modes)."""
+    M, K = qA.shape
+    xh = (qA.astype(np.float64).reshape(M, -1, G) * sA.astype(np.float64)[..., None]).reshape(M, K)
+    N = qW.shape[0]
+    wh = (qW.astype(np.float64).reshape(N, -1, G) * sW.view(np.float16).astype(np.float64)[..., None]).reshape(N, K)
+    main = xh @ wh.T
+    lora = 0.0
+    if r and c.r:
+        X = c.X.view(np.float16).astype(np.float64)
+        lora = (X @ c.L_down.view(np.float16).astype(np.float64)) @ c.L_up.view(np.float16).astype(np.float64)
+    cs = c.colscale.view(np.float16).astype(np.float64)
+    b = c.bias.view(np.float16).astype(np.float64)
+    return cs * (main + lora) + b
+
+
+def test_linear_matches_dequantised_dense_reference():
+    c = make_linear_case(40, 256, 48, 32, seed=11)
+    ref = oracle.Reference(c.X, c.W, c.L_down, c.L_up, c.colscale, c.bias)
+    y = _dequant_reference(c, ref.qA, ref.sA, ref.qW, ref.sW)
+    np.testing.assert_allclose(ref.Y, y, rtol=1e-12, atol=1e-12)
+
+
+def test_linear_zero_input_gives_bias_exactly():
+    c = make_linear_case(8, 128, 32, 32, seed=2)
+    X0 = np.zeros_like(c.X)
+    y = oracle.linear(X0, c.W, c.L_down, c.L_up, c.colscale, c.bias)
+    assert np.array_equal(y, np.broadcast_to(c.bias.view(np.float16).astype(np.float64), y.shape))
+
+
+def test_linear_rank0_is_plain_grouped_gemm():
+    c = make_linear_case(16, 192, 24, 0, seed=4)
+    ref = oracle.Reference(c.X, c.W, c.L_down, c.L_up, c.colscale, c.bias)
+    y = _dequant_reference(c, ref.qA, ref.sA, ref.qW, ref.sW, r=False)
+    np.testing.assert_allclose(ref.Y, y, rtol=1e-12, atol=1e-12)
+
+
+def test_linear_zero_weights_is_textbook_lora():
+    c = make_linear_case(12, 128, 40, 32, seed=6)
+    W0 = np.zeros_like(c.W)
+    y = oracle.linear(c.X, W0, c.L_down, c.L_up, c.colscale, c.bias)
+    X = c.X.view(np.float16).astype(np.float64)
+    lora = X @ c.L_down.view(np.float16).astype(np.float64) @ c.L_up.view(np.float16).astype(np.float64)
+    exp = c.colscale.view(np.float16).astype(np.float64) * lora + c.bias.view(np.float16).astype(np.float64)
+    np.testing.assert_allclose(y, exp, rtol=1e-12, atol=1e-13)
+
+
+def test_linear_identity_weight_closed_form():
+    K = N = 128
+    c = make_linear_case(6, K, N, 0, seed=9)
+    W = np.eye(N, K, dtype=np.float32)
+    ref = oracle.Reference(c.X, W, c.L_down, c.L_up, c.colscale, c.bias)
+    sw = 0.142822265625
+    g = np.arange(N) // G
+    main = 7 * sw * ref.sA.astype(np.float64)[:, g] * ref.qA.astype(np.float64)[:, np.arange(N)]
+    exp = c.colscale.view(np.float16).astype(np.float64) * main + c.bias.view(np.float16).astype(np.float64)
+    np.testing.assert_allclose(ref.Y, exp, rtol=1e-13, atol=1e-15)
+
+
+def test_linear_sampled_matches_full():
+    c = make_linear_case(20, 256, 36, 32, seed=12)
+    full = oracle.linear(c.X, c.W, c.L_down, c.L_up, c.colscale, c.bias)
+    rng = np.random.default_rng(0)
+    rows = rng.integers(0, 20, 50)
+    cols = rng.integers(0, 36, 50)
+    s = oracle.linear_sampled(c.X, c.W, c.L_down, c.L_up, c.colscale, c.bias, rows, cols)
+    assert np.array_equal(s, full[rows, cols])
