@@ -1,0 +1,374 @@
+#!/usr/bin/env python
+"""Throughput of the W4A4 + LoRA linear layer on GB300.
+
+One step = the four linears of a Qwen3-style 1024-hidden decoder layer at
+M = 700 tokens (qkv 1024->4096, o 2048->1024, gate_up 1024->6144,
+down 3072->1024; group 64, LoRA rank 32), each as the path's two kernels:
+w4a4_quantize_act (quantise + LoRA down) and w4a4_linear (GEMM + LoRA up +
+column affine).  Weight packing is offline (done once, untimed).
+
+Inputs are seeded synthetic data (synthetic.make_linear_case).  To keep the
+timed inputs out of L2, the step cycles through R replicas of the layer
+(distinct buffers, > 2x the 129 MB L2 in total).
+
+Prints one JSON line (metric: effective TOPS = (2MNK + 2Mr(K+N)) / time).
+  --impl reference : the CPU oracle timed on the host cores (bounded sample).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from synthetic import DECODER_LAYER_M700, make_linear_case  # noqa: E402
+from w4a4_quantized_gemm_gb300 import metrics  # noqa: E402
+
+METRIC = "W4A4+LoRA linear effective TOPS (decoder-layer linears, M=700)"
+UNIT = "TOPS"
+WORKLOAD = "qwen3_1024_decoder_layer_linears_M700"
+L2_BYTES = 129 * 2 ** 20
+
+
+def _env_int(k, d):
+    try:
+        return int(os.environ.get(k, d))
+    except ValueError:
+        return d
+
+
+def layer_ops() -> int:
+    return sum(metrics.linear_ops(s["M"], s["N"], s["K"], s["r"]) for s in DECODER_LAYER_M700.values())
+
+
+def base_config(extra=None):
+    cfg = {"workload": WORKLOAD, "M": 700, "group": 64, "rank": 32,
+           "linears": {k: [v["K"], v["N"]] for k, v in DECODER_LAYER_M700.items()}}
+    if extra:
+        cfg.update(extra)
+    return cfg
+
+
+# ----------------------------------------------------------------- CPU oracle
+def time_oracle(budget_s: float, max_rows: int = 700, chunk: int = 16):
+    """Run the oracle on row chunks of every linear until `budget_s` elapses.
+    Returns (ops done, seconds, rows per linear)."""
+    import oracle
+    oracle.build()
+    cases = {k: make_linear_case(seed=i, **v) for i, (k, v) in enumerate(DECODER_LAYER_M700.items())}
+    ops, rows, t0 = 0, 0, time.perf_counter()
+    while rows < max_rows:
+        n = min(chunk, max_rows - rows)
+        for c in cases.values():
+            oracle.linear(c.X[rows:rows + n], c.W, c.L_down, c.L_up, c.colscale, c.bias)
+            ops += metrics.linear_ops(n, c.N, c.K, c.r)
+        rows += n
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    return ops, time.perf_counter() - t0, rows
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return 0
+    # each step: the oracle on a bounded row sample of every linear
+    rows_per_step = args.ref_rows
+    steps = []
+    import oracle
+    oracle.build()
+    cases = {k: make_linear_case(seed=i, **v) for i, (k, v) in enumerate(DECODER_LAYER_M700.items())}
+    for i in range(args.warmup + args.steps):
+        t0 = time.perf_counter()
+        ops = 0
+        r0 = (i * rows_per_step) % (700 - rows_per_step)
+        for c in cases.values():
+            oracle.linear(c.X[r0:r0 + rows_per_step], c.W, c.L_down, c.L_up, c.colscale, c.bias)
+            ops += metrics.linear_ops(rows_per_step, c.N, c.K, c.r)
+        dt = time.perf_counter() - t0
+        if i >= args.warmup:
+            steps.append((ops, dt))
+    ops = sum(o for o, _ in steps)
+    sec = sum(t for _, t in steps)
+    value = ops / sec / 1e12
+    sample = f"{rows_per_step} of 700 rows of each of the 4 linears per step"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * sec / len(steps),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int64/f64",
+        "data": "synthetic", "config": base_config({"sample": sample}),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            p = [x.strip() for x in ln.split(",")]
+            if len(p) < 9:
+                continue
+            try:
+                sm.append(float(p[1]))
+                mx = float(p[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, p[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": ["unavailable"], "samples": 0}
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ GPU arm
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import torch.distributed as dist
+
+    torch.cuda.set_device(local_rank)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    from w4a4_quantized_gemm_gb300 import build as wbuild
+    wbuild.build()
+    import w4a4_quantized_gemm_gb300 as w4
+
+    dev = torch.device("cuda", local_rank)
+    stream = torch.cuda.current_stream()
+    names = list(DECODER_LAYER_M700)
+    R = args.replicas
+    L = {}
+    for i, name in enumerate(names):
+        s = DECODER_LAYER_M700[name]
+        c = make_linear_case(seed=i, **s)
+        X = torch.from_numpy(c.X.view(np.float16).copy()).to(dev)
+        W = torch.from_numpy(c.W).to(dev)
+        Ld = torch.from_numpy(c.L_down.view(np.float16).copy()).to(dev)
+        Lu = torch.from_numpy(c.L_up.view(np.float16).copy()).to(dev)
+        cs = torch.from_numpy(c.colscale.view(np.float16).copy()).to(dev)
+        b = torch.from_numpy(c.bias.view(np.float16).copy()).to(dev)
+        packed = torch.empty(w4.packed_weights_bytes(c.N, c.K, c.r), dtype=torch.uint8, device=dev)
+        w4.w4a4_pack_weights(W, Ld, Lu, packed, c.r)
+        del W
+        wsb = w4.act_workspace_bytes(c.M, c.K, c.r)
+        L[name] = dict(
+            c=c, X=[X.clone() for _ in range(R)], packed=[packed.clone() for _ in range(R)],
+            cs=[cs.clone() for _ in range(R)], b=[b.clone() for _ in range(R)],
+            ws=[torch.empty(wsb, dtype=torch.uint8, device=dev) for _ in range(R)],
+            Y=[torch.empty((c.M, c.N), dtype=torch.float16, device=dev) for _ in range(R)])
+    torch.cuda.synchronize()
+    footprint = sum(sum(t.numel() * t.element_size() for k in ("X", "packed", "ws", "Y") for t in d[k])
+                    for d in L.values())
+
+    def step(i, timers=None):
+        rep = i % R
+        for name in names:
+            d = L[name]
+            c = d["c"]
+            if timers is not None:
+                timers[name][0].record(stream)
+            w4.w4a4_quantize_act(d["X"][rep], d["packed"][rep], d["ws"][rep], c.r, stream)
+            if timers is not None:
+                timers[name][1].record(stream)
+            w4.w4a4_linear(d["ws"][rep], d["packed"][rep], d["cs"][rep], d["b"][rep], d["Y"][rep], c.K, c.r,
+                           w4.KERNEL_AUTO, stream)
+            if timers is not None:
+                timers[name][2].record(stream)
+
+    dispatch = {}
+    for i in range(args.warmup):
+        step(i)
+    for name in names:  # record the kernel each linear uses
+        d = L[name]
+        w4.w4a4_linear(d["ws"][0], d["packed"][0], d["cs"][0], d["b"][0], d["Y"][0], d["c"].K, d["c"].r)
+        dispatch[name] = w4.w4a4_last_dispatch()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(local_rank) if rank == 0 else None
+    if sampler:
+        sampler.__enter__()
+        time.sleep(0.3)
+    torch.cuda.synchronize()
+    ev0.record(stream)
+    for i in range(args.steps):
+        step(i)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    if sampler:
+        sampler.__exit__()
+    ms = ev0.elapsed_time(ev1)
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+        dist.barrier()
+    ms_per_step = ms / args.steps
+    value = world * layer_ops() / (ms_per_step * 1e-3) / 1e12
+
+    # per-kernel breakdown pass (same work, events around each launch)
+    timers = {n: [torch.cuda.Event(enable_timing=True) for _ in range(3)] for n in names}
+    q_ms = {n: 0.0 for n in names}
+    g_ms = {n: 0.0 for n in names}
+    for i in range(args.steps):
+        step(i, timers)
+        torch.cuda.synchronize()
+        for n in names:
+            q_ms[n] += timers[n][0].elapsed_time(timers[n][1])
+            g_ms[n] += timers[n][1].elapsed_time(timers[n][2])
+    gemm_ops = layer_ops()
+    gemm_s = sum(g_ms.values()) / args.steps * 1e-3
+    q_s = sum(q_ms.values()) / args.steps * 1e-3
+    peaks = {}
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            peaks = json.load(f)
+    except (OSError, ValueError):
+        pass
+    if "bf16_tflops" in peaks:
+        bf16, peak_src = float(peaks["bf16_tflops"]), "measured"
+    else:
+        bf16, peak_src = 1900.0, "fallback"
+    fp8_peak = 2.0 * bf16  # FP8 tensor kind: measured bf16 burst x nominal fp8/bf16 ratio (4.5/2.25)
+    achieved = gemm_ops / gemm_s / 1e12
+    roofline = {"bound": "tensor", "achieved": achieved, "peak": fp8_peak, "unit": "TFLOP/s",
+                "frac": achieved / fp8_peak, "traffic": None,
+                "kernel": "w4a4_linear (GEMM + LoRA up + affine)",
+                "peak_source": f"{peak_src} bf16 burst x 2 (fp8 kind)",
+                "gemm_us_per_step": gemm_s * 1e6, "quantize_us_per_step": q_s * 1e6,
+                "per_linear_gemm_us": {n: g_ms[n] / args.steps * 1e3 for n in names},
+                "per_linear_quantize_us": {n: q_ms[n] / args.steps * 1e3 for n in names},
+                "gemm_algorithmic_bytes": sum(metrics.gemm_bytes(**DECODER_LAYER_M700[n]) for n in names)}
+
+    # end to end through the public API: pinned host X in, Y back to pinned host
+    e2e = None
+    if not args.no_e2e:
+        Xh = {n: torch.empty_like(L[n]["X"][0], device="cpu").pin_memory() for n in names}
+        Yh = {n: torch.empty_like(L[n]["Y"][0], device="cpu").pin_memory() for n in names}
+        for n in names:
+            Xh[n].copy_(L[n]["X"][0])
+        h2d = sum(Xh[n].numel() * 2 for n in names)
+        d2h = sum(Yh[n].numel() * 2 for n in names)
+
+        def e2e_step(i):
+            rep = i % R
+            for n in names:
+                d = L[n]
+                c = d["c"]
+                d["X"][rep].copy_(Xh[n], non_blocking=True)
+                w4.w4a4_quantize_act(d["X"][rep], d["packed"][rep], d["ws"][rep], c.r, stream)
+                w4.w4a4_linear(d["ws"][rep], d["packed"][rep], d["cs"][rep], d["b"][rep], d["Y"][rep], c.K, c.r,
+                               w4.KERNEL_AUTO, stream)
+                Yh[n].copy_(d["Y"][rep], non_blocking=True)
+
+        for i in range(args.warmup):
+            e2e_step(i)
+        torch.cuda.synchronize()
+        ev0.record(stream)
+        for i in range(args.steps):
+            e2e_step(i)
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        e_ms = ev0.elapsed_time(ev1) / args.steps
+        if world > 1:
+            t = torch.tensor([e_ms], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e_ms = float(t.item())
+        e2e = {"value": world * layer_ops() / (e_ms * 1e-3) / 1e12, "unit": UNIT, "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "ms_per_step": e_ms}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        ops, sec, rows = time_oracle(args.cpu_budget)
+        cpu = {"value": ops / sec / 1e12, "unit": UNIT, "cores": 1, "kind": "oracle",
+               "sample": f"rows 0..{rows - 1} of each of the 4 linears ({ops / 1e9:.2f} Gop, {sec:.1f} s)"}
+
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    if rank != 0:
+        return 0
+    clocks = sampler.summary() if sampler else None
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "int4 codes (fp8 e4m3 operands), fp32 accumulate, fp16 out",
+        "data": "synthetic",
+        "config": base_config({"replicas": R, "l2": f"inputs larger than L2: {footprint / 2**20:.0f} MiB cycled",
+                               "dispatch": dispatch}),
+        "gpu_launches": args.steps * 2 * len(names),
+        "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--replicas", type=int, default=8)
+    ap.add_argument("--ref-rows", type=int, default=32)
+    ap.add_argument("--cpu-budget", type=float, default=12.0)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    rank = _env_int("RANK", 0)
+    world = _env_int("WORLD_SIZE", 1)
+    local_rank = _env_int("LOCAL_RANK", 0)
+    if args.impl == "reference":
+        return run_reference(args, rank, world)
+    return run_ours(args, rank, world, local_rank)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,171 @@
+/*
+ * w4a4.h -- C ABI of the GB300 (sm_103a) W4A4 + LoRA quantized linear layer.
+ *
+ *   Y = colscale (.) ( sum_g sA[m,g] sW[n,g] (qA . qW)_g + (X L_down) L_up ) + bias
+ *
+ * Sources (page title, section):
+ *   [VC]  "W4A4 CUDA Kernel for Voice Clone: From Profiling to 2.6x Faster Than
+ *         FP16": 2.1-2.3 (INT4 weights, fp16 per-group-64 scales, LoRA factors),
+ *         3.4 (the three kernels of one linear), 3.6 (fused quantize + LoRA down),
+ *         3.7 (INT4 GEMM + per-group dequant + LoRA up), 3.10 (weights repacked once
+ *         at load).
+ *   [INT4] "INT4 Kernel Architecture, in depth": "How the weights are stored"
+ *         (nibble packing, reordering for the kernel), "Failure modes" (no silent
+ *         fallback; log the kernel chosen), "One token versus a thousand" (shape
+ *         dispatch, split-K).
+ *   [BW]  "High-Performance Kernel Design for W4A4 Quantized Matrix Multiplication
+ *         on Blackwell Architecture", section 1 (scaled low-bit GEMM + low-rank
+ *         residual + column-wise affine).
+ *
+ * Conventions for every entry point
+ *   - All data pointers are DEVICE pointers of the current CUDA device, owned by
+ *     the caller.  The library never allocates, frees or keeps device memory,
+ *     and keeps no state besides a per-device property cache and the text of
+ *     the last dispatch decision.
+ *   - fp16 tensors are passed as uint16_t bit patterns (IEEE binary16).
+ *   - Work is enqueued on `stream` (may be 0); nothing synchronises unless the
+ *     function says so.  Argument checks happen on the host before any launch,
+ *     and a rejected call launches nothing.
+ *   - Every pointer must be 16-byte aligned; shapes must satisfy
+ *     K % 64 == 0, K >= 64, N % 16 == 0, N >= 16, r % 16 == 0, 0 <= r <= 128,
+ *     M >= 0 (M == 0 is a no-op that returns W4A4_OK).  Anything else returns
+ *     an error status: there is no fallback path.
+ *   - After each launch, a CUDA launch error is reported as W4A4_ERR_CUDA.
+ *
+ * Packed weight buffer (layout version W4A4_LAYOUT_VERSION), G = K/64 groups:
+ *   offset 0                         Ld   L_down in tensor-core fragment order:
+ *       [K/16][r/8][32 lanes][2 x 32-bit], lane L's word w holds the fp16 pair
+ *       L_down[16 s + 2 (L % 4) + 8 w + {0,1}][8 t + L / 4] for k-step s, tile t.
+ *   offset align256(K*r*2)           qW   [G][N][32 bytes]
+ *       One 32-byte record per (group g, output row n) holding the 64 codes
+ *       as nibbles in OFFSET-BINARY form (nibble = code + 8, 0..15).  Within a
+ *       record, the 32-bit little-endian word at byte 8*q + 4*h (q = 0..3,
+ *       h = 0..1) holds, in nibble j (bits 4j..4j+3), the code of
+ *           k = 64 g + 32 h + (j < 4 ? 4 q + j : 16 + 4 q + (j - 4)).
+ *   next align256                    sW   [G][N] fp16 group scales
+ *   next align256                    Lu   L_up as [r/16][N][32 bytes]: row n of
+ *       plane p holds L_up[16 p .. 16 p + 15][n] (fp16), its two 16-byte halves
+ *       swapped when (n >> 2) & 1 (the 32-byte shared-memory swizzle).
+ *   total = w4a4_packed_weights_bytes(N, K, r)
+ *
+ * Activation workspace (written by w4a4_quantize_act, read by w4a4_linear),
+ * MT = ceil(M / 128) tiles of 128 rows:
+ *   offset 0                 qA  [MT][G][2][128][32 bytes]: the code of row m,
+ *       column k is stored as an FP8 E4M3 byte (every integer in [-8, 7] is exact
+ *       in E4M3) in plane (k % 64) / 32, row m % 128, byte k % 32, with the two
+ *       16-byte halves of a row swapped when ((m % 128) >> 2) & 1.
+ *   next align256            sS  [MT][G][128][2] fp32: (sA, SA) per row and group,
+ *       SA = sum of the group's 64 codes (exact integer in fp32).
+ *   next align256            La  [MT][r/16][128][32 bytes]: lora_act = X L_down
+ *       rounded to fp16, row m, column j in plane j/16, same 32-byte swizzle.
+ *   Rows >= roundup(M, 16) of the workspace are never written and never
+ *   influence Y.  total = w4a4_act_workspace_bytes(M, K, r)
+ */
+#ifndef W4A4_H_
+#define W4A4_H_
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define W4A4_GROUP 64
+#define W4A4_LAYOUT_VERSION 1
+#define W4A4_MAX_RANK 128
+
+typedef enum {
+    W4A4_OK = 0,
+    W4A4_ERR_INVALID_ARG = 1,      /* null pointer where data is needed, negative size */
+    W4A4_ERR_UNSUPPORTED_SHAPE = 2,/* K % 64, N % 16, r % 16 or r > 128 violated */
+    W4A4_ERR_MISALIGNED = 3,       /* a pointer is not 16-byte aligned */
+    W4A4_ERR_WORKSPACE = 4,        /* a buffer size is below the size query's result */
+    W4A4_ERR_CUDA = 5,             /* the CUDA runtime reported an error */
+    W4A4_ERR_TIMEOUT = 6,          /* a bounded device-side wait gave up */
+    W4A4_ERR_NO_DEVICE = 7         /* no usable sm_103 device is current */
+} w4a4_status;
+
+/* Kernel selection for w4a4_linear_select / w4a4_debug_group_partials. */
+typedef enum {
+    W4A4_KERNEL_AUTO = 0,   /* by M: small-M kernel for M <= threshold, else tensor-core tiles */
+    W4A4_KERNEL_TC = 1,     /* tcgen05 (TMEM accumulators, bulk-copy pipeline) */
+    W4A4_KERNEL_SMALLM = 2  /* weight-streaming kernel (warp-level MMA, split over K) */
+} w4a4_kernel;
+
+/* ---- size queries (bytes of caller-allocated device buffers) ---- */
+size_t w4a4_packed_weights_bytes(int N, int K, int r);
+size_t w4a4_act_workspace_bytes(int M, int K, int r);
+
+/* ---- offline weight packing ([VC] 2.1-2.3, 3.10; [INT4] "How the weights are stored")
+ * W      fp32 [N, K] row-major (nn.Linear out x in).
+ * L_down fp16 [K, r] row-major, L_up fp16 [r, N] row-major (both NULL when r == 0).
+ * Quantises each (row n, group g): sW = fp16(max(absmax/7, 2^-14)) with IEEE
+ * division and round-to-nearest-even, qW = clamp(rint(W / sW), -8, 7); writes
+ * the packed buffer described above.  Runs once per layer; enqueued on stream. */
+w4a4_status w4a4_pack_weights(const float* W, const uint16_t* L_down, const uint16_t* L_up,
+                              int N, int K, int r, void* packed, size_t packed_bytes,
+                              cudaStream_t stream);
+
+/* Same, from given integer codes int8 [N, K] (values must lie in [-8, 7]) and
+ * fp16 scales [N, K/64]: lets callers bring codes of their own quantiser. */
+w4a4_status w4a4_pack_weight_codes(const int8_t* codes, const uint16_t* scales,
+                                   const uint16_t* L_down, const uint16_t* L_up,
+                                   int N, int K, int r, void* packed, size_t packed_bytes,
+                                   cudaStream_t stream);
+
+/* ---- fused activation quantisation + LoRA down ([VC] 3.6)
+ * X fp16 [M, K] row-major.  Per (row m, group g): sA = max(absmax/7, 1e-10)
+ * (fp32, IEEE division), qA = clamp(rint(X / sA), -8, 7), SA = sum of codes;
+ * in the same pass lora_act[m, :] = X[m, :] L_down (fp16 inputs, fp32
+ * accumulation, deterministic order), stored as fp16.  L_down is read from the
+ * packed weight buffer.  Writes the activation workspace. */
+w4a4_status w4a4_quantize_act(const uint16_t* X, const void* packed, int M, int K, int r,
+                              void* act_ws, size_t act_ws_bytes, cudaStream_t stream);
+
+/* ---- W4A4 GEMM + LoRA up + column affine ([VC] 3.7, [BW] 1)
+ * acc[m,n] = sum_g sA[m,g] sW[n,g] P[m,n,g] + sum_j fp16(lora_act[m,j]) L_up[j,n]
+ * in fp32, P exact per group; Y[m,n] = fp16_rn(colscale[n] * acc + bias[n]).
+ * colscale fp16 [N]; bias fp16 [N] or NULL (zero); Y fp16 [M, N] row-major.
+ * The kernel is chosen by M (see w4a4_last_dispatch). */
+w4a4_status w4a4_linear(const void* act_ws, size_t act_ws_bytes, const void* packed,
+                        size_t packed_bytes, const uint16_t* colscale, const uint16_t* bias,
+                        int M, int N, int K, int r, uint16_t* Y, cudaStream_t stream);
+
+/* Same as w4a4_linear with an explicit kernel choice (tests, measurements). */
+w4a4_status w4a4_linear_select(const void* act_ws, size_t act_ws_bytes, const void* packed,
+                               size_t packed_bytes, const uint16_t* colscale, const uint16_t* bias,
+                               int M, int N, int K, int r, uint16_t* Y, int kernel,
+                               cudaStream_t stream);
+
+/* ---- debug / validation entry points (small shapes; they synchronise `stream`)
+ * Unpack the packed weights: codes int8 [N, K], scales fp16 [N, K/64],
+ * L_down fp16 [K, r], L_up fp16 [r, N] (the last two may be NULL). */
+w4a4_status w4a4_debug_unpack_weights(const void* packed, int N, int K, int r, int8_t* codes,
+                                      uint16_t* scales, uint16_t* L_down, uint16_t* L_up,
+                                      cudaStream_t stream);
+/* Unpack the workspace: codes int8 [M, K], sA fp32 [M, K/64], SA fp32 [M, K/64]
+ * (may be NULL), lora_act fp32 [M, r] (may be NULL). */
+w4a4_status w4a4_debug_unpack_act(const void* act_ws, int M, int K, int r, int8_t* codes,
+                                  float* sA, float* SA, float* lora_act, cudaStream_t stream);
+/* Exact per-group partial sums P[m, n, g] (int32 [M, N, K/64]) as produced by
+ * the selected GEMM kernel's tensor-core path (its epilogue dumps instead of
+ * scaling). */
+w4a4_status w4a4_debug_group_partials(const void* act_ws, const void* packed, int M, int N, int K,
+                                      int r, int kernel, int32_t* P, cudaStream_t stream);
+/* Reads and clears the device status word written by bounded waits
+ * (W4A4_OK or W4A4_ERR_TIMEOUT); synchronises the device. */
+w4a4_status w4a4_device_status(void);
+
+/* ---- dispatch and diagnostics ([INT4] "Failure modes": log the kernel chosen) */
+const char* w4a4_status_string(int status);
+const char* w4a4_last_dispatch(void);       /* kernel and launch shape of this thread's last call */
+int w4a4_small_m_threshold(void);
+void w4a4_set_small_m_threshold(int m);     /* M <= threshold -> small-M kernel */
+int w4a4_layout_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* W4A4_H_ */

@@ -130,9 +130,9 @@ def group_partials(qA: np.ndarray, qW: np.ndarray) -> np.ndarray:
 def lora_down(X: np.ndarray, L_down: np.ndarray) -> np.ndarray:
     """fp64 [M, r] = X (fp16) @ L_down (fp16 [K, r])."""
     X = _c(X, np.uint16)
-    Ld = _c(L_down, np.uint16)
     M, K = X.shape
-    K2, r = Ld.shape if Ld.ndim == 2 else (K, 0)
+    Ld = np.zeros((K, 0), np.uint16) if L_down is None else _c(L_down, np.uint16).reshape(K, -1)
+    K2, r = Ld.shape
     assert K2 == K
     D = np.zeros((M, r), np.float64)
     if r:
@@ -148,7 +148,8 @@ def linear_from_codes(qA, sA, qW, sW, D, L_up, colscale, bias) -> np.ndarray:
     D = _c(D, np.float64).reshape(M, -1)
     r = D.shape[1]
     Lup = _c(L_up, np.uint16).reshape(r, N) if r else np.zeros((0, N), np.uint16)
-    cs = _c(colscale, np.uint16); b = _c(bias, np.uint16)
+    cs = _c(colscale, np.uint16)
+    b = np.zeros(N, np.uint16) if bias is None else _c(bias, np.uint16)
     Y = np.empty((M, N), np.float64)
     _load().oracle_linear_from_codes(_ptr(qA), _ptr(sA), _ptr(qW), _ptr(sW), _ptr(D), _ptr(Lup),
                                      _ptr(cs), _ptr(b), M, N, K, r, _ptr(Y))

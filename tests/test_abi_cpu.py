@@ -1,0 +1,95 @@
+"""The C-ABI library builds, loads and exports every declared entry point; host
+argument checks reject bad calls before any launch (no GPU needed)."""
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+import w4a4_quantized_gemm_gb300 as w4
+from w4a4_quantized_gemm_gb300 import build as wbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "w4a4.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    wbuild.build()
+    return w4.lib()
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(w4a4_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_header_declares_expected_entry_points():
+    names = declared_functions()
+    for n in ("w4a4_pack_weights", "w4a4_quantize_act", "w4a4_linear"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(L):
+    for name in declared_functions():
+        assert hasattr(L, name), name
+        assert name in w4.SIGNATURES, f"binding has no signature for {name}"
+
+
+def test_size_queries(L):
+    G = 1024 // 64
+    # packed: L_down first, then codes, scales, L_up; 256-byte aligned sections
+    al = lambda x: (x + 255) // 256 * 256
+    exp = al(al(al(1024 * 32 * 2) + G * 4096 * 32) + G * 4096 * 2)
+    exp = al(exp + 32 * 4096 * 2)
+    assert w4.packed_weights_bytes(4096, 1024, 32) == exp
+    MT = (700 + 127) // 128
+    ws = al(al(al(MT * G * 2 * 128 * 32) + MT * G * 128 * 8) + MT * 2 * 128 * 32)
+    assert w4.act_workspace_bytes(700, 1024, 32) == ws
+    assert L.w4a4_packed_weights_bytes(4096, 1000, 32) == 0   # K % 64
+    assert L.w4a4_packed_weights_bytes(4100, 1024, 32) == 0   # N % 16
+    assert L.w4a4_packed_weights_bytes(4096, 1024, 24) == 0   # r % 16
+    assert L.w4a4_packed_weights_bytes(4096, 1024, 144) == 0  # r > 128
+    assert L.w4a4_layout_version() == 1
+
+
+def _vp(x):
+    return ctypes.c_void_p(x)
+
+
+def test_argument_checks_precede_any_launch(L):
+    A = _vp(0x10000)  # never dereferenced: every call below fails on the host
+    big = 1 << 40
+    lin = lambda M, N, K, r, ws=A, pk=A, cs=A, y=A, wsb=big, pkb=big: L.w4a4_linear(
+        ws, wsb, pk, pkb, cs, None, M, N, K, r, y, None)
+    assert lin(64, 1024, 1000, 32) == 2
+    assert lin(64, 1000, 1024, 32) == 2
+    assert lin(64, 1024, 1024, 40) == 2
+    assert lin(64, 1024, 1024, 256) == 2
+    assert lin(-1, 1024, 1024, 32) == 1
+    assert lin(0, 1024, 1024, 32) == 0            # M == 0: no-op
+    assert lin(64, 1024, 1024, 32, ws=None) == 1
+    assert lin(64, 1024, 1024, 32, y=_vp(0x10008)) == 3
+    assert lin(64, 1024, 1024, 32, wsb=100) == 4
+    assert lin(64, 1024, 1024, 32, pkb=100) == 4
+    assert L.w4a4_quantize_act(A, A, 64, 100, 32, A, big, None) == 2
+    assert L.w4a4_quantize_act(_vp(0x10002), A, 64, 128, 32, A, big, None) == 3
+    assert L.w4a4_quantize_act(A, A, 64, 128, 32, A, 10, None) == 4
+    assert L.w4a4_pack_weights(None, A, A, 64, 128, 32, A, big, None) == 1
+    assert L.w4a4_pack_weights(A, None, A, 64, 128, 32, A, big, None) == 1  # r > 0 needs LoRA factors
+    assert L.w4a4_linear_select(A, big, A, big, A, None, 64, 1024, 1024, 32, A, 7, None) == 1
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="valid shapes would launch on a GPU box")
+def test_valid_call_without_device_reports_no_device(L):
+    A = _vp(0x10000)
+    st = L.w4a4_linear(A, 1 << 40, A, 1 << 40, A, None, 64, 1024, 1024, 32, A, None)
+    assert st == 7
+
+
+def test_status_strings(L):
+    for s in range(8):
+        assert L.w4a4_status_string(s)
+    assert b"unknown" in L.w4a4_status_string(99)

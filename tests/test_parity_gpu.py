@@ -1,0 +1,221 @@
+"""Parity of the CUDA path (through the C ABI) against the CPU oracle.
+
+Bit-exact: weight codes and fp16 scales, activation codes and fp32 scales,
+per-group integer partial sums of each GEMM kernel.  Within tolerance
+|Y - y| <= 2e-3 (1 + |y|) (y the oracle's fp64 output): the fp16 output.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import w4a4_quantized_gemm_gb300 as w4
+from synthetic import make_linear_case, random_codes, random_f16
+from tests.helpers import check_tol, pack, quantize, run_linear, to_dev
+
+pytestmark = pytest.mark.gpu
+
+KERNELS = [w4.KERNEL_SMALLM, w4.KERNEL_TC]
+KNAMES = {w4.KERNEL_SMALLM: "smallm", w4.KERNEL_TC: "tc"}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    from w4a4_quantized_gemm_gb300 import build
+    build.build()
+    w4.lib()
+    torch.cuda.init()
+
+
+def _kernel_available(k):
+    return True
+
+
+# ------------------------------------------------------------------ packing
+@pytest.mark.parametrize("N,K,r", [(16, 64, 0), (48, 192, 16), (256, 1024, 32), (4096, 1024, 32)])
+def test_pack_weights_bitexact(N, K, r):
+    c = make_linear_case(1, K, N, r, seed=N + K)
+    t = to_dev(c)
+    packed = pack(c, t)
+    codes, scales, Ld, Lu = w4.w4a4_debug_unpack_weights(packed, N, K, r)
+    qW, sW = oracle.quantize_weights(c.W)
+    assert np.array_equal(codes.cpu().numpy(), qW)
+    assert np.array_equal(scales.cpu().numpy().view(np.uint16), sW)
+    if r:
+        assert np.array_equal(Ld.cpu().numpy().view(np.uint16), c.L_down)
+        assert np.array_equal(Lu.cpu().numpy().view(np.uint16), c.L_up)
+
+
+def test_pack_weight_codes_full_range_roundtrip():
+    rng = np.random.default_rng(3)
+    N, K, r = 64, 256, 16
+    codes = random_codes(rng, (N, K))
+    codes[0, :] = -8
+    codes[1, :] = 7
+    scales = random_f16(rng, (N, K // 64), 1e-3, 1e-2)
+    dev = lambda a: torch.from_numpy(a).cuda()
+    Ld = dev(random_f16(rng, (K, r), -0.1, 0.1).view(np.float16))
+    Lu = dev(random_f16(rng, (r, N), -0.1, 0.1).view(np.float16))
+    packed = torch.empty(w4.packed_weights_bytes(N, K, r), dtype=torch.uint8, device="cuda")
+    w4.w4a4_pack_weight_codes(dev(codes), dev(scales.view(np.float16)), Ld, Lu, packed, r)
+    c2, s2, _, _ = w4.w4a4_debug_unpack_weights(packed, N, K, r)
+    assert np.array_equal(c2.cpu().numpy(), codes)
+    assert np.array_equal(s2.cpu().numpy().view(np.uint16), scales)
+
+
+# -------------------------------------------------------- activation kernel
+@pytest.mark.parametrize("M,K,r", [(1, 64, 0), (17, 128, 16), (64, 1024, 32), (200, 3072, 32), (33, 512, 128)])
+def test_quantize_act_bitexact(M, K, r):
+    c = make_linear_case(M, K, 32, r, seed=M * 7 + K)
+    t = to_dev(c)
+    packed = pack(c, t)
+    ws = quantize(c, t, packed)
+    codes, sA, SA, lora = w4.w4a4_debug_unpack_act(ws, M, K, r)
+    qA, sA_ref = oracle.quantize_act(c.X)
+    assert np.array_equal(codes.cpu().numpy(), qA)
+    assert np.array_equal(sA.cpu().numpy(), sA_ref)
+    assert np.array_equal(SA.cpu().numpy(), qA.reshape(M, -1, 64).sum(axis=2).astype(np.float32))
+    if r:
+        D = oracle.lora_down(c.X, c.L_down)
+        # fp32 accumulation + fp16 storage: half an fp16 ulp plus accumulation noise
+        err = np.abs(lora.cpu().numpy().astype(np.float64) - D)
+        assert np.all(err <= 2.0 ** -11 * np.abs(D) + 1e-5 * (1 + np.abs(D)))
+
+
+def test_quantize_act_zero_and_outlier_rows():
+    M, K = 24, 256
+    c = make_linear_case(M, K, 16, 16, seed=1)
+    X = c.X.copy()
+    X[0, :] = 0                      # all-zero row: scale 1e-10, codes 0
+    X[1, :64] = np.float16(60000).view(np.uint16)   # large values
+    X[2, 64:128] = np.float16(-3.5).view(np.uint16)
+    c.X = X
+    t = to_dev(c)
+    packed = pack(c, t)
+    ws = quantize(c, t, packed)
+    codes, sA, SA, _ = w4.w4a4_debug_unpack_act(ws, M, K, 16)
+    qA, sA_ref = oracle.quantize_act(X)
+    assert np.array_equal(codes.cpu().numpy(), qA)
+    assert np.array_equal(sA.cpu().numpy(), sA_ref)
+    assert sA_ref[0, 0] == np.float32(1e-10)
+
+
+# ------------------------------------------------------------ exact partials
+@pytest.mark.parametrize("kernel", KERNELS, ids=lambda k: KNAMES[k])
+@pytest.mark.parametrize("M,N,K", [(1, 16, 64), (7, 48, 128), (33, 144, 192), (130, 256, 256), (300, 400, 128)])
+def test_group_partials_bitexact(kernel, M, N, K):
+    c = make_linear_case(M, K, N, 0, seed=M + N)
+    t = to_dev(c)
+    packed = pack(c, t)
+    ws = quantize(c, t, packed)
+    P = w4.w4a4_debug_group_partials(ws, packed, M, N, K, 0, kernel).cpu().numpy()
+    ref = oracle.Reference(c.X, c.W, None, None, c.colscale, c.bias)
+    assert np.array_equal(P, oracle.group_partials(ref.qA, ref.qW))
+
+
+@pytest.mark.parametrize("kernel", KERNELS, ids=lambda k: KNAMES[k])
+def test_group_partials_extreme_codes(kernel):
+    """All -8 x -8 (P = 4096), alternating signs (P = 0) and random full-range codes."""
+    rng = np.random.default_rng(9)
+    M, N, K = 40, 64, 256
+    qW = random_codes(rng, (N, K))
+    qW[0, :] = -8
+    qW[1, :] = np.tile([7, -8], K // 2)
+    sW = random_f16(rng, (N, K // 64), 0.01, 0.02)
+    c = make_linear_case(M, K, N, 0, seed=2)
+    X = c.X.view(np.float16).copy()
+    X[0, :] = -7.0  # codes -7 after quantisation (absmax/7 scale)
+    X[1, :] = np.tile(np.float16([3.5, -3.5]), K // 2)
+    c.X = X.view(np.uint16)
+    t = to_dev(c)
+    packed = torch.empty(w4.packed_weights_bytes(N, K, 0), dtype=torch.uint8, device="cuda")
+    w4.w4a4_pack_weight_codes(torch.from_numpy(qW).cuda(), torch.from_numpy(sW.view(np.float16)).cuda(),
+                              None, None, packed, 0)
+    ws = quantize(c, t, packed)
+    P = w4.w4a4_debug_group_partials(ws, packed, M, N, K, 0, kernel).cpu().numpy()
+    qA, _ = oracle.quantize_act(c.X)
+    ref = oracle.group_partials(qA, qW)
+    assert ref[0, 0, 0] == 7 * 8 * 64
+    assert np.array_equal(P, ref)
+
+
+# ------------------------------------------------------------------ output Y
+SHAPES = [(1, 16, 64, 0), (5, 32, 128, 16), (16, 256, 256, 32), (37, 144, 192, 32), (64, 1024, 1024, 32),
+          (129, 272, 320, 32), (200, 512, 512, 64), (300, 128, 1024, 128)]
+
+
+@pytest.mark.parametrize("kernel", KERNELS, ids=lambda k: KNAMES[k])
+@pytest.mark.parametrize("M,N,K,r", SHAPES)
+def test_linear_within_tolerance(kernel, M, N, K, r):
+    c = make_linear_case(M, K, N, r, seed=M + 3 * N + K)
+    t = to_dev(c)
+    packed = pack(c, t)
+    ws = quantize(c, t, packed)
+    Y = run_linear(c, t, packed, ws, kernel)
+    y = oracle.linear(c.X, c.W, c.L_down, c.L_up, c.colscale, c.bias)
+    check_tol(Y, y, f"{KNAMES[kernel]} {M}x{N}x{K} r={r}")
+
+
+@pytest.mark.parametrize("kernel", KERNELS, ids=lambda k: KNAMES[k])
+def test_zero_input_gives_bias_exactly(kernel):
+    c = make_linear_case(20, 256, 64, 32, seed=5)
+    c.X = np.zeros_like(c.X)
+    t = to_dev(c)
+    packed = pack(c, t)
+    ws = quantize(c, t, packed)
+    Y = run_linear(c, t, packed, ws, kernel).cpu().numpy().view(np.uint16)
+    assert np.array_equal(Y, np.broadcast_to(c.bias, Y.shape))
+
+
+@pytest.mark.parametrize("kernel", KERNELS, ids=lambda k: KNAMES[k])
+def test_no_bias_and_determinism(kernel):
+    c = make_linear_case(70, 256, 96, 32, seed=8)
+    t = to_dev(c)
+    packed = pack(c, t)
+    ws = quantize(c, t, packed)
+    Y1 = run_linear(c, t, packed, ws, kernel, bias=False)
+    Y2 = run_linear(c, t, packed, ws, kernel, bias=False)
+    assert torch.equal(Y1, Y2)
+    c0 = make_linear_case(70, 256, 96, 32, seed=8)
+    c0.bias = np.zeros_like(c0.bias)
+    y = oracle.linear(c0.X, c0.W, c0.L_down, c0.L_up, c0.colscale, c0.bias)
+    check_tol(Y1, y, "no bias")
+
+
+def test_m_zero_is_noop():
+    c = make_linear_case(1, 128, 32, 16, seed=1)
+    t = to_dev(c)
+    packed = pack(c, t)
+    ws = torch.empty(256, dtype=torch.uint8, device="cuda")
+    Y = torch.empty((0, 32), dtype=torch.float16, device="cuda")
+    w4.w4a4_quantize_act(t["X"][:0], packed, ws, 16)
+    w4.w4a4_linear(ws, packed, t["colscale"], t["bias"], Y, 128, 16)
+
+
+@pytest.mark.parametrize("kernel", KERNELS, ids=lambda k: KNAMES[k])
+def test_output_guard_regions_untouched(kernel):
+    """Y written only inside [M, N]: canaries before/after the buffer and the
+    columns of a wider row stride stay intact (stand-in for a memory checker)."""
+    M, N, K, r = 45, 80, 192, 16
+    c = make_linear_case(M, K, N, r, seed=4)
+    t = to_dev(c)
+    packed = pack(c, t)
+    ws = quantize(c, t, packed)
+    guard = 4096
+    buf = torch.full((guard + M * N + guard,), 0x5A5A, dtype=torch.int16, device="cuda")
+    Y = buf[guard:guard + M * N].view(torch.float16).view(M, N)
+    w4.w4a4_linear(ws, packed, t["colscale"], t["bias"], Y, K, r, kernel)
+    torch.cuda.synchronize()
+    b = buf.cpu().numpy()
+    assert np.all(b[:guard] == 0x5A5A) and np.all(b[guard + M * N:] == 0x5A5A)
+    y = oracle.linear(c.X, c.W, c.L_down, c.L_up, c.colscale, c.bias)
+    check_tol(Y, y, "guarded")
+
+
+def test_dispatch_is_logged():
+    c = make_linear_case(3, 128, 32, 16, seed=1)
+    t = to_dev(c)
+    packed = pack(c, t)
+    ws = quantize(c, t, packed)
+    run_linear(c, t, packed, ws, w4.KERNEL_SMALLM)
+    assert "gemm_smallm" in w4.w4a4_last_dispatch()

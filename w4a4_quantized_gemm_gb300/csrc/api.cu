@@ -1,0 +1,278 @@
+// C ABI of the W4A4 library: host-side argument checks (before any launch),
+// kernel dispatch by M, status mapping and the dispatch log ("INT4 Kernel
+// Architecture, in depth", "Failure modes": no silent fallback, log which
+// kernel each layer uses).
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
+#include <mutex>
+
+#include "kernels.h"
+
+namespace w4a4 {
+
+namespace {
+thread_local char t_dispatch[256] = "none";
+int g_small_m_threshold = -1;  // -1: read W4A4_SMALL_M on first use
+constexpr int kDefaultSmallM = 1 << 30;  // every M goes to the small-M kernel until the tcgen05 kernel lands
+std::mutex g_mu;
+int g_sm_count[64] = {0};
+
+bool log_enabled() {
+    static int on = -1;
+    if (on < 0) {
+        const char* e = std::getenv("W4A4_LOG");
+        on = (e && e[0] && e[0] != '0') ? 1 : 0;
+    }
+    return on == 1;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+w4a4_status check_kn(int N, int K, int r) {
+    if (N < 0 || K < 0 || r < 0) return W4A4_ERR_INVALID_ARG;
+    if (K < kGroup || K % kGroup != 0) return W4A4_ERR_UNSUPPORTED_SHAPE;
+    if (N < 16 || N % 16 != 0) return W4A4_ERR_UNSUPPORTED_SHAPE;
+    if (r % 16 != 0 || r > W4A4_MAX_RANK) return W4A4_ERR_UNSUPPORTED_SHAPE;
+    return W4A4_OK;
+}
+
+w4a4_status check_device() {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return W4A4_ERR_NO_DEVICE;
+    }
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) {
+        cudaGetLastError();
+        return W4A4_ERR_NO_DEVICE;
+    }
+    if (major != 10 || minor != 3) return W4A4_ERR_NO_DEVICE;  // built for sm_103a only
+    return W4A4_OK;
+}
+
+w4a4_status sync_status(cudaStream_t s) {
+    if (cudaStreamSynchronize(s) != cudaSuccess) {
+        cudaGetLastError();
+        return W4A4_ERR_CUDA;
+    }
+    return W4A4_OK;
+}
+}  // namespace
+
+void set_dispatch(const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(t_dispatch, sizeof(t_dispatch), fmt, ap);
+    va_end(ap);
+    if (log_enabled()) std::fprintf(stderr, "[w4a4] %s\n", t_dispatch);
+}
+
+w4a4_status launch_status() {
+    cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? W4A4_OK : W4A4_ERR_CUDA;
+}
+
+int device_sm_count() {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= 64) return 148;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (g_sm_count[dev] == 0) {
+        int n = 0;
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        g_sm_count[dev] = n > 0 ? n : 148;
+    }
+    return g_sm_count[dev];
+}
+
+}  // namespace w4a4
+
+using namespace w4a4;
+
+extern "C" {
+
+size_t w4a4_packed_weights_bytes(int N, int K, int r) {
+    if (check_kn(N, K, r) != W4A4_OK) return 0;
+    return packed_layout(N, K, r).total;
+}
+
+size_t w4a4_act_workspace_bytes(int M, int K, int r) {
+    if (M < 0 || check_kn(16, K, r) != W4A4_OK) return 0;
+    return act_layout(M, K, r).total;
+}
+
+int w4a4_layout_version(void) { return W4A4_LAYOUT_VERSION; }
+
+const char* w4a4_status_string(int status) {
+    switch (status) {
+        case W4A4_OK: return "ok";
+        case W4A4_ERR_INVALID_ARG: return "invalid argument";
+        case W4A4_ERR_UNSUPPORTED_SHAPE: return "unsupported shape (need K%64==0, N%16==0, r%16==0, r<=128)";
+        case W4A4_ERR_MISALIGNED: return "pointer not 16-byte aligned";
+        case W4A4_ERR_WORKSPACE: return "buffer smaller than the size query";
+        case W4A4_ERR_CUDA: return "CUDA runtime error";
+        case W4A4_ERR_TIMEOUT: return "bounded device wait timed out";
+        case W4A4_ERR_NO_DEVICE: return "no sm_103 device is current";
+        default: return "unknown status";
+    }
+}
+
+const char* w4a4_last_dispatch(void) { return t_dispatch; }
+
+int w4a4_small_m_threshold(void) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (g_small_m_threshold < 0) {
+        const char* e = std::getenv("W4A4_SMALL_M");
+        g_small_m_threshold = e ? std::atoi(e) : kDefaultSmallM;
+    }
+    return g_small_m_threshold;
+}
+
+void w4a4_set_small_m_threshold(int m) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    g_small_m_threshold = m < 0 ? 0 : m;
+}
+
+static w4a4_status pack_common(const float* W, const int8_t* codes, const uint16_t* scales, const uint16_t* L_down,
+                               const uint16_t* L_up, int N, int K, int r, void* packed, size_t packed_bytes,
+                               cudaStream_t stream) {
+    w4a4_status st = check_kn(N, K, r);
+    if (st != W4A4_OK) return st;
+    if (!packed || (!W && !(codes && scales))) return W4A4_ERR_INVALID_ARG;
+    if (r > 0 && (!L_down || !L_up)) return W4A4_ERR_INVALID_ARG;
+    if (!aligned16(packed) || (W && !aligned16(W)) || (L_down && !aligned16(L_down)) || (L_up && !aligned16(L_up)))
+        return W4A4_ERR_MISALIGNED;
+    if (packed_bytes < packed_layout(N, K, r).total) return W4A4_ERR_WORKSPACE;
+    if ((st = check_device()) != W4A4_OK) return st;
+    uint8_t* out = static_cast<uint8_t*>(packed);
+    launch_pack_weights(W, codes, scales, N, K, r, out, stream);
+    if ((st = launch_status()) != W4A4_OK) return st;
+    launch_pack_lora(L_down, L_up, N, K, r, out, stream);
+    set_dispatch("pack_weights N=%d K=%d r=%d", N, K, r);
+    return launch_status();
+}
+
+w4a4_status w4a4_pack_weights(const float* W, const uint16_t* L_down, const uint16_t* L_up, int N, int K, int r,
+                              void* packed, size_t packed_bytes, cudaStream_t stream) {
+    if (!W) return W4A4_ERR_INVALID_ARG;
+    return pack_common(W, nullptr, nullptr, L_down, L_up, N, K, r, packed, packed_bytes, stream);
+}
+
+w4a4_status w4a4_pack_weight_codes(const int8_t* codes, const uint16_t* scales, const uint16_t* L_down,
+                                   const uint16_t* L_up, int N, int K, int r, void* packed, size_t packed_bytes,
+                                   cudaStream_t stream) {
+    if (!codes || !scales) return W4A4_ERR_INVALID_ARG;
+    return pack_common(nullptr, codes, scales, L_down, L_up, N, K, r, packed, packed_bytes, stream);
+}
+
+w4a4_status w4a4_quantize_act(const uint16_t* X, const void* packed, int M, int K, int r, void* act_ws,
+                              size_t act_ws_bytes, cudaStream_t stream) {
+    if (M < 0) return W4A4_ERR_INVALID_ARG;
+    w4a4_status st = check_kn(16, K, r);
+    if (st != W4A4_OK) return st;
+    if (M == 0) return W4A4_OK;
+    if (!X || !act_ws || (r > 0 && !packed)) return W4A4_ERR_INVALID_ARG;
+    if (!aligned16(X) || !aligned16(act_ws) || (packed && !aligned16(packed))) return W4A4_ERR_MISALIGNED;
+    if (act_ws_bytes < act_layout(M, K, r).total) return W4A4_ERR_WORKSPACE;
+    if ((st = check_device()) != W4A4_OK) return st;
+    return launch_quantize_act(X, static_cast<const uint8_t*>(packed), M, K, r, static_cast<uint8_t*>(act_ws),
+                               stream);
+}
+
+static int pick_kernel(int M, int kernel) {
+    if (kernel == W4A4_KERNEL_TC || kernel == W4A4_KERNEL_SMALLM) return kernel;
+    return M <= w4a4_small_m_threshold() ? W4A4_KERNEL_SMALLM : W4A4_KERNEL_TC;
+}
+
+static w4a4_status linear_checks(const void* act_ws, size_t act_ws_bytes, const void* packed, size_t packed_bytes,
+                                 const uint16_t* colscale, const uint16_t* bias, int M, int N, int K, int r,
+                                 const void* out) {
+    if (M < 0) return W4A4_ERR_INVALID_ARG;
+    w4a4_status st = check_kn(N, K, r);
+    if (st != W4A4_OK) return st;
+    if (M == 0) return W4A4_OK;
+    if (!act_ws || !packed || !colscale || !out) return W4A4_ERR_INVALID_ARG;
+    if (!aligned16(act_ws) || !aligned16(packed) || !aligned16(colscale) || (bias && !aligned16(bias)) ||
+        !aligned16(out))
+        return W4A4_ERR_MISALIGNED;
+    if (act_ws_bytes < act_layout(M, K, r).total || packed_bytes < packed_layout(N, K, r).total)
+        return W4A4_ERR_WORKSPACE;
+    return check_device();
+}
+
+w4a4_status w4a4_linear_select(const void* act_ws, size_t act_ws_bytes, const void* packed, size_t packed_bytes,
+                               const uint16_t* colscale, const uint16_t* bias, int M, int N, int K, int r,
+                               uint16_t* Y, int kernel, cudaStream_t stream) {
+    if (kernel < W4A4_KERNEL_AUTO || kernel > W4A4_KERNEL_SMALLM) return W4A4_ERR_INVALID_ARG;
+    w4a4_status st = linear_checks(act_ws, act_ws_bytes, packed, packed_bytes, colscale, bias, M, N, K, r, Y);
+    if (st != W4A4_OK || M == 0) return st;
+    const uint8_t* ws = static_cast<const uint8_t*>(act_ws);
+    const uint8_t* pk = static_cast<const uint8_t*>(packed);
+    if (pick_kernel(M, kernel) == W4A4_KERNEL_TC)
+        return launch_gemm_tc(ws, pk, colscale, bias, M, N, K, r, Y, nullptr, stream);
+    return launch_gemm_smallm(ws, pk, colscale, bias, M, N, K, r, Y, nullptr, stream);
+}
+
+w4a4_status w4a4_linear(const void* act_ws, size_t act_ws_bytes, const void* packed, size_t packed_bytes,
+                        const uint16_t* colscale, const uint16_t* bias, int M, int N, int K, int r, uint16_t* Y,
+                        cudaStream_t stream) {
+    return w4a4_linear_select(act_ws, act_ws_bytes, packed, packed_bytes, colscale, bias, M, N, K, r, Y,
+                              W4A4_KERNEL_AUTO, stream);
+}
+
+w4a4_status w4a4_debug_unpack_weights(const void* packed, int N, int K, int r, int8_t* codes, uint16_t* scales,
+                                      uint16_t* L_down, uint16_t* L_up, cudaStream_t stream) {
+    w4a4_status st = check_kn(N, K, r);
+    if (st != W4A4_OK) return st;
+    if (!packed || !codes || !scales) return W4A4_ERR_INVALID_ARG;
+    if ((st = check_device()) != W4A4_OK) return st;
+    launch_unpack_weights(static_cast<const uint8_t*>(packed), N, K, r, codes, scales, L_down, L_up, stream);
+    if ((st = launch_status()) != W4A4_OK) return st;
+    return sync_status(stream);
+}
+
+w4a4_status w4a4_debug_unpack_act(const void* act_ws, int M, int K, int r, int8_t* codes, float* sA, float* SA,
+                                  float* lora_act, cudaStream_t stream) {
+    if (M < 0) return W4A4_ERR_INVALID_ARG;
+    w4a4_status st = check_kn(16, K, r);
+    if (st != W4A4_OK) return st;
+    if (M == 0) return W4A4_OK;
+    if (!act_ws || !codes || !sA) return W4A4_ERR_INVALID_ARG;
+    if ((st = check_device()) != W4A4_OK) return st;
+    launch_unpack_act(static_cast<const uint8_t*>(act_ws), M, K, r, codes, sA, SA, lora_act, stream);
+    if ((st = launch_status()) != W4A4_OK) return st;
+    return sync_status(stream);
+}
+
+w4a4_status w4a4_debug_group_partials(const void* act_ws, const void* packed, int M, int N, int K, int r,
+                                      int kernel, int32_t* P, cudaStream_t stream) {
+    if (M < 0) return W4A4_ERR_INVALID_ARG;
+    w4a4_status st = check_kn(N, K, r);
+    if (st != W4A4_OK) return st;
+    if (M == 0) return W4A4_OK;
+    if (!act_ws || !packed || !P) return W4A4_ERR_INVALID_ARG;
+    if (!aligned16(act_ws) || !aligned16(packed)) return W4A4_ERR_MISALIGNED;
+    if ((st = check_device()) != W4A4_OK) return st;
+    const uint8_t* ws = static_cast<const uint8_t*>(act_ws);
+    const uint8_t* pk = static_cast<const uint8_t*>(packed);
+    if (pick_kernel(M, kernel) == W4A4_KERNEL_TC)
+        st = launch_gemm_tc(ws, pk, nullptr, nullptr, M, N, K, r, nullptr, P, stream);
+    else
+        st = launch_gemm_smallm(ws, pk, nullptr, nullptr, M, N, K, r, nullptr, P, stream);
+    if (st != W4A4_OK) return st;
+    if ((st = sync_status(stream)) != W4A4_OK) return st;
+    return tc_read_and_clear_status();
+}
+
+w4a4_status w4a4_device_status(void) {
+    if (cudaDeviceSynchronize() != cudaSuccess) {
+        cudaGetLastError();
+        return W4A4_ERR_CUDA;
+    }
+    return tc_read_and_clear_status();
+}
+
+}  // extern "C"

@@ -1,0 +1,32 @@
+// Internal launchers shared between the C-ABI layer (api.cu) and the kernel
+// translation units.  Arguments are validated by the caller.
+#pragma once
+#include "common.cuh"
+
+namespace w4a4 {
+
+// pack.cu
+void launch_pack_weights(const float* W, const int8_t* codes, const uint16_t* scales, int N, int K, int r,
+                         uint8_t* packed, cudaStream_t s);
+void launch_pack_lora(const uint16_t* L_down, const uint16_t* L_up, int N, int K, int r,
+                      uint8_t* packed, cudaStream_t s);
+void launch_unpack_weights(const uint8_t* packed, int N, int K, int r, int8_t* codes, uint16_t* scales,
+                           uint16_t* L_down, uint16_t* L_up, cudaStream_t s);
+
+// quantize.cu
+w4a4_status launch_quantize_act(const uint16_t* X, const uint8_t* packed, int M, int K, int r,
+                                uint8_t* ws, cudaStream_t s);
+void launch_unpack_act(const uint8_t* ws, int M, int K, int r, int8_t* codes, float* sA, float* SA,
+                       float* lora, cudaStream_t s);
+
+// gemm_smallm.cu (warp-level MMA, split over K)
+w4a4_status launch_gemm_smallm(const uint8_t* ws, const uint8_t* packed, const uint16_t* colscale,
+                               const uint16_t* bias, int M, int N, int K, int r, uint16_t* Y,
+                               int32_t* P_dump, cudaStream_t s);
+
+// gemm_tc.cu (tcgen05 + TMEM)
+w4a4_status launch_gemm_tc(const uint8_t* ws, const uint8_t* packed, const uint16_t* colscale,
+                           const uint16_t* bias, int M, int N, int K, int r, uint16_t* Y, int32_t* P_dump,
+                           cudaStream_t s);
+
+}  // namespace w4a4
