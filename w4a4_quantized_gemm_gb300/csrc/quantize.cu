@@ -3,21 +3,31 @@
 // down-projection X . L_down from the same read of X ("W4A4 CUDA Kernel for
 // Voice Clone", 3.6 fused_quantize_repack_act_kernel and its LoRA-down branch).
 //
-// Differences from the page's design, for GB300:
-//  * One CTA owns whole rows (16 per CTA) and its warps split the K groups, so
-//    the LoRA partial sums are reduced inside the CTA in a fixed order: no
+// GB300 design:
+//  * A thread-block cluster of CK CTAs owns 16 rows; each CTA takes a
+//    contiguous range of the K groups.  The fp32 LoRA partials of the CK CTAs
+//    are summed through distributed shared memory in a fixed order: no
 //    atomics, deterministic results, and no separate repack kernel (the
-//    page's pack_lora_act exists only to wait for atomics).
+//    page's pack_lora_act exists only to wait for its atomics).
 //  * Codes are stored as FP8 E4M3 bytes, the operand encoding the tcgen05
 //    tensor core reads (GB300 has no INT4 tensor-core kind).
+//  * Division x / scale is done as a multiplication by the reciprocal, which
+//    gives the same code as the IEEE quotient except when the product lies
+//    within 2^-18 of a rounding boundary (k + 1/2); those rare elements are
+//    recomputed with the IEEE division, so codes equal rint(fl(x / scale)).
+#include <cooperative_groups.h>
+
 #include "kernels.h"
+
+namespace cg = cooperative_groups;
 
 namespace w4a4 {
 namespace {
 
-constexpr int kRows = 16;      // rows per CTA (one m16 tile of the LoRA MMA)
-constexpr int kWarps = 8;
+constexpr int kRows = 16;      // rows per cluster (one m16 tile of the LoRA MMA)
+constexpr int kWarps = 4;
 constexpr int kXsStride = 72;  // halves per staged row (64 + 8 pad: conflict-free ldmatrix)
+constexpr int kMaxCluster = 8;
 
 __device__ __forceinline__ void ldmatrix_x4(uint32_t (&r)[4], const void* p) {
     asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
@@ -25,101 +35,131 @@ __device__ __forceinline__ void ldmatrix_x4(uint32_t (&r)[4], const void* p) {
                  : "r"(smem_u32(p)));
 }
 
+// Two integer-valued floats -> E4M3 bytes: lo -> bits 0-7, hi -> bits 8-15.
+__device__ __forceinline__ uint32_t cvt_e4m3x2(float lo, float hi) {
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;\n" : "=h"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// rint(fl(x / s)) from the reciprocal product (see the file comment): y is within
+// 2^-20 of x/s and fl(x/s) within 2^-21, so away from k + 1/2 both round alike.
+__device__ __forceinline__ float code_of(float x, float s, float inv) {
+    const float y = x * inv;
+    const float q = rintf(y);
+    const float d = fabsf(y - q);  // distance to the nearest integer, in [0, 0.5]
+    if (d >= 0.5f - 3.814697265625e-06f) return rintf(__fdiv_rn(x, s));  // within 2^-18 of k + 1/2
+    return q;
+}
+
 template <int R>  // LoRA rank, multiple of 16 (0 = no LoRA branch)
 __global__ void __launch_bounds__(kWarps * 32) quantize_act_kernel(const uint16_t* __restrict__ X,
                                                                    const uint2* __restrict__ Ldp, int M,
                                                                    int K, uint8_t* __restrict__ ws) {
-    extern __shared__ __align__(16) uint8_t smem[];
-    uint16_t* xs = reinterpret_cast<uint16_t*>(smem);                           // [warps][16][72]
-    float* red = reinterpret_cast<float*>(smem + kWarps * kRows * kXsStride * 2);  // [warps][16][R]
+    __shared__ __align__(16) uint16_t xs[kWarps][kRows * kXsStride];
+    __shared__ __align__(16) float red[R > 0 ? kWarps * kRows * R : 1];
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int G = K / kGroup;
     const ActLayout AL = act_layout(M, K, R);
-    const int row0 = blockIdx.x * kRows;
+    cg::cluster_group cluster = cg::this_cluster();
+    const int CK = int(cluster.num_blocks());
+    const int crank = int(cluster.block_rank());
+    const int row0 = (blockIdx.x / CK) * kRows;
     const int mt = row0 / kTileM;
+    const int g_begin = (G * crank) / CK, g_end = (G * (crank + 1)) / CK;
 
     // quantisation role: lane owns row (lane/2), columns 32*(lane%2) .. +31 of a group
     const int qrow = lane >> 1, qhalf = lane & 1;
     const int m = row0 + qrow;
-    const int rr = m % kTileM;  // row within the 128-row tile
+    const int rr = m % kTileM;
     const bool valid = m < M;
 
-    constexpr int NT = R / 8;  // LoRA n8 tiles
+    constexpr int NT = R / 8;
     float acc[NT > 0 ? NT : 1][4];
 #pragma unroll
     for (int t = 0; t < (NT > 0 ? NT : 1); ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.f;
 
-    uint16_t* xw = xs + warp * kRows * kXsStride;
-    for (int g = warp; g < G; g += kWarps) {
-        uint4 xv[4];
-        const uint16_t* src = X + (size_t)m * K + (size_t)g * kGroup + qhalf * 32;
+    uint16_t* xw = xs[warp];
+    const uint16_t* xrow = X + (size_t)m * K + qhalf * 32;
+    int g = g_begin + warp;
+    uint4 xv[4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) xv[i] = valid ? ldg_nc_v4(src + 8 * i) : make_uint4(0, 0, 0, 0);
+    for (int i = 0; i < 4; ++i)
+        xv[i] = (valid && g < g_end) ? ldg_nc_v4(xrow + (size_t)g * kGroup + 8 * i) : make_uint4(0, 0, 0, 0);
+    for (; g < g_end; g += kWarps) {
+        // prefetch the warp's next group while this one is processed
+        uint4 nv[4];
+        const int gn = g + kWarps;
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            nv[i] = (valid && gn < g_end) ? ldg_nc_v4(xrow + (size_t)gn * kGroup + 8 * i) : make_uint4(0, 0, 0, 0);
         float x[32];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             const uint32_t w[4] = {xv[i].x, xv[i].y, xv[i].z, xv[i].w};
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-                x[8 * i + 2 * j] = __half2float(__ushort_as_half(uint16_t(w[j] & 0xffffu)));
-                x[8 * i + 2 * j + 1] = __half2float(__ushort_as_half(uint16_t(w[j] >> 16)));
+                const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[j]));
+                x[8 * i + 2 * j] = f.x;
+                x[8 * i + 2 * j + 1] = f.y;
             }
         }
         float amax = 0.f;
 #pragma unroll
         for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(x[i]));
         amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-        // scale = max(absmax / 7, 1e-10), code = clamp(rint(x / scale), -8, 7), IEEE division
+        // scale = max(absmax / 7, 1e-10) with IEEE division.  Codes lie in [-7, 7]:
+        // |x| <= absmax and scale >= fl(absmax / 7), so |x / scale| <= 7 (1 + 2^-23)
+        // rounds to at most 7 and the clamp to [-8, 7] never acts.
         const float s = fmaxf(__fdiv_rn(amax, 7.0f), 1e-10f);
+        const float inv = __frcp_rn(s);
+        float csum = 0.f;
         uint32_t packed[8];
-        int csum = 0;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-            uint32_t word = 0;
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const int c = int(fminf(fmaxf(rintf(__fdiv_rn(x[4 * i + j], s)), -8.0f), 7.0f));
-                csum += c;
-                word |= e4m3_of_int(c) << (8 * j);
-            }
-            packed[i] = word;
+            const float c0 = code_of(x[4 * i], s, inv), c1 = code_of(x[4 * i + 1], s, inv);
+            const float c2 = code_of(x[4 * i + 2], s, inv), c3 = code_of(x[4 * i + 3], s, inv);
+            csum += (c0 + c1) + (c2 + c3);
+            packed[i] = cvt_e4m3x2(c0, c1) | (cvt_e4m3x2(c2, c3) << 16);
         }
         csum += __shfl_xor_sync(0xffffffffu, csum, 1);
-        // codes -> plane qhalf of (mt, g), row rr, two 16-byte chunks (swizzled)
         uint8_t* plane = ws + AL.qA + ((size_t)(mt * G + g) * 2 + qhalf) * (kTileM * 32);
         *reinterpret_cast<uint4*>(plane + rr * 32 + swz32(rr, 0) * 16) =
             make_uint4(packed[0], packed[1], packed[2], packed[3]);
         *reinterpret_cast<uint4*>(plane + rr * 32 + swz32(rr, 1) * 16) =
             make_uint4(packed[4], packed[5], packed[6], packed[7]);
         if (qhalf == 0)
-            *reinterpret_cast<float2*>(ws + AL.sS + ((size_t)(mt * G + g) * kTileM + rr) * 8) =
-                make_float2(s, float(csum));
+            *reinterpret_cast<float2*>(ws + AL.sS + ((size_t)(mt * G + g) * kTileM + rr) * 8) = make_float2(s, csum);
 
         if constexpr (R > 0) {
-            // stage the fp16 tile for the LoRA-down MMA (A operand via ldmatrix)
+            // LoRA down: the fp16 tile through ldmatrix into mma.m16n8k16 (fp32 accumulate)
 #pragma unroll
             for (int i = 0; i < 4; ++i)
                 *reinterpret_cast<uint4*>(xw + qrow * kXsStride + qhalf * 32 + 8 * i) = xv[i];
             __syncwarp();
+            const uint2* bp = Ldp + ((size_t)(g * 4) * NT) * 32 + lane;
+            uint2 b[4][NT];
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks)
+#pragma unroll
+                for (int t = 0; t < NT; ++t) b[ks][t] = __ldg(bp + (ks * NT + t) * 32);
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks) {
                 uint32_t a[4];
                 const int lr = (lane & 7) + ((lane >> 3) & 1) * 8, lc = ((lane >> 4) & 1) * 8 + ks * 16;
                 ldmatrix_x4(a, xw + lr * kXsStride + lc);
-                const uint2* bp = Ldp + ((size_t)(g * 4 + ks) * NT) * 32 + lane;
 #pragma unroll
-                for (int t = 0; t < NT; ++t) {
-                    const uint2 b = __ldg(bp + t * 32);
-                    mma_f16_16816(acc[t], a, b.x, b.y);
-                }
+                for (int t = 0; t < NT; ++t) mma_f16_16816(acc[t], a, b[ks][t].x, b[ks][t].y);
             }
             __syncwarp();
         }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) xv[i] = nv[i];
     }
 
     if constexpr (R > 0) {
-        // fixed-order reduction of the warps' LoRA partials, then fp16 into the tile layout
+        // warps' partials -> smem, summed in a fixed order inside the CTA, then across the cluster
         const int gid = lane >> 2, tig = lane & 3;
         float* rw = red + warp * kRows * R;
 #pragma unroll
@@ -130,17 +170,25 @@ __global__ void __launch_bounds__(kWarps * 32) quantize_act_kernel(const uint16_
             rw[(gid + 8) * R + 8 * t + 2 * tig + 1] = acc[t][3];
         }
         __syncthreads();
-        uint16_t* La = reinterpret_cast<uint16_t*>(ws + AL.La);
         for (int idx = threadIdx.x; idx < kRows * R; idx += kWarps * 32) {
-            const int row = idx / R, j = idx % R;
-            float v = 0.f;
+            float v = red[idx];
 #pragma unroll
-            for (int w = 0; w < kWarps; ++w) v += red[w * kRows * R + idx];
+            for (int w = 1; w < kWarps; ++w) v += red[w * kRows * R + idx];
+            red[idx] = v;  // CTA partial in warp 0's slot
+        }
+        cluster.sync();
+        // cluster rank c finalises elements c, c + CK, ... of the 16 x R block
+        uint16_t* La = reinterpret_cast<uint16_t*>(ws + AL.La);
+        for (int idx = crank + CK * int(threadIdx.x); idx < kRows * R; idx += CK * kWarps * 32) {
+            float v = 0.f;
+            for (int c = 0; c < CK; ++c) v += cluster.map_shared_rank(red, c)[idx];
+            const int row = idx / R, j = idx % R;
             const int r2 = (row0 + row) % kTileM;
             const int p = j >> 4, jj = j & 15;
             La[((size_t)(mt * (R / 16) + p) * kTileM + r2) * 16 + swz32(r2, jj >> 3) * 8 + (jj & 7)] =
                 __half_as_ushort(__float2half_rn(v));
         }
+        cluster.sync();  // peers' shared memory stays alive until every read is done
     }
 }
 
@@ -172,17 +220,28 @@ __global__ void unpack_act_kernel(const uint8_t* __restrict__ ws, int M, int K, 
 
 template <int R>
 w4a4_status launch_q(const uint16_t* X, const uint8_t* packed, int M, int K, uint8_t* ws, cudaStream_t s) {
-    const size_t smem = kWarps * kRows * kXsStride * 2 + (size_t)kWarps * kRows * R * 4;
-    static bool attr_set = false;  // per process; identical for every device
-    if (!attr_set) {
-        if (cudaFuncSetAttribute(quantize_act_kernel<R>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 int(smem)) != cudaSuccess)
-            return W4A4_ERR_CUDA;
-        attr_set = true;
+    const int G = K / kGroup;
+    const int CK = G < kMaxCluster ? G : kMaxCluster;
+    const int row_blocks = (M + kRows - 1) / kRows;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(unsigned(row_blocks * CK));
+    cfg.blockDim = dim3(kWarps * 32);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = unsigned(CK);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, quantize_act_kernel<R>, X, reinterpret_cast<const uint2*>(packed),
+                                             M, K, ws);
+    set_dispatch("quantize_act rows/cluster=%d cluster=%d grid=%d rank=%d", kRows, CK, row_blocks * CK, R);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return W4A4_ERR_CUDA;
     }
-    const unsigned grid = unsigned((M + kRows - 1) / kRows);
-    quantize_act_kernel<R><<<grid, kWarps * 32, smem, s>>>(X, reinterpret_cast<const uint2*>(packed), M, K, ws);
-    set_dispatch("quantize_act rows/CTA=%d grid=%u rank=%d", kRows, grid, R);
     return launch_status();
 }
 
