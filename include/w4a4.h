@@ -139,6 +139,24 @@ w4a4_status w4a4_linear_select(const void* act_ws, size_t act_ws_bytes, const vo
                                int M, int N, int K, int r, uint16_t* Y, int kernel,
                                cudaStream_t stream);
 
+/* ---- allocation-free variant of the whole layer
+ * The pages have no counterpart to this entry point.  It serves callers that
+ * cannot allocate device memory (code running inside an allocator, a runtime
+ * that owns all memory, a plugin interface that only passes in the inputs and
+ * outputs): it runs w4a4_quantize_act and w4a4_linear back to back with the
+ * activation workspace in a fixed array of W4A4_NOALLOC_WORKSPACE_BYTES that
+ * the library keeps in each device's memory from load until process exit.
+ * X fp16 [M, K], packed/colscale/bias/Y as for w4a4_linear.  Returns
+ * W4A4_ERR_WORKSPACE, before any launch, when w4a4_act_workspace_bytes(M, K, r)
+ * exceeds the array.  The first call on a device looks up the array's device
+ * address (make that first call before any stream capture).  All calls share
+ * the array: calls that overlap on the GPU race.  It allocates and frees
+ * nothing. */
+#define W4A4_NOALLOC_WORKSPACE_BYTES (8u << 20)
+w4a4_status w4a4_linear_noalloc(const uint16_t* X, const void* packed, size_t packed_bytes,
+                                const uint16_t* colscale, const uint16_t* bias, int M, int N, int K, int r,
+                                uint16_t* Y, cudaStream_t stream);
+
 /* ---- debug / validation entry points (small shapes; they synchronise `stream`)
  * Unpack the packed weights: codes int8 [N, K], scales fp16 [N, K/64],
  * L_down fp16 [K, r], L_up fp16 [r, N] (the last two may be NULL). */

@@ -46,6 +46,7 @@ SIGNATURES = {
     "w4a4_quantize_act": (I, [P, P, I, I, I, P, Z, P]),
     "w4a4_linear": (I, [P, Z, P, Z, P, P, I, I, I, I, P, P]),
     "w4a4_linear_select": (I, [P, Z, P, Z, P, P, I, I, I, I, P, I, P]),
+    "w4a4_linear_noalloc": (I, [P, P, Z, P, P, I, I, I, I, P, P]),
     "w4a4_debug_unpack_weights": (I, [P, I, I, I, P, P, P, P, P]),
     "w4a4_debug_unpack_act": (I, [P, I, I, I, P, P, P, P, P]),
     "w4a4_debug_group_partials": (I, [P, P, I, I, I, I, I, P, P]),
@@ -134,6 +135,18 @@ def w4a4_linear(act_ws, packed, colscale, bias, Y, K: int, r: int, kernel: int =
     M, N = Y.shape
     _check(lib().w4a4_linear_select(_ptr(act_ws), _nbytes(act_ws), _ptr(packed), _nbytes(packed), _ptr(colscale),
                                     _ptr(bias), M, N, K, r, _ptr(Y), kernel, _stream(stream)), "w4a4_linear")
+
+
+def w4a4_linear_noalloc(X, packed, colscale, bias, Y, r: int, stream=None):
+    """Quantise X and run the layer with the library's built-in workspace (no
+    allocation anywhere; see include/w4a4.h for its size limit and sharing rules)."""
+    M, K = X.shape
+    N = Y.shape[1]
+    _check(lib().w4a4_linear_noalloc(_ptr(X), _ptr(packed), _nbytes(packed), _ptr(colscale), _ptr(bias), M, N, K,
+                                     r, _ptr(Y), _stream(stream)), "w4a4_linear_noalloc")
+
+
+NOALLOC_WORKSPACE_BYTES = 8 << 20
 
 
 def w4a4_debug_unpack_weights(packed, N: int, K: int, r: int, stream=None):
