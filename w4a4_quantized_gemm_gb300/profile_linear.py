@@ -1,0 +1,70 @@
+"""Profiling driver: one W4A4 linear of the M=700 decoder layer, called in a loop.
+
+    python -m w4a4_quantized_gemm_gb300.profile_linear <qkv|o|gate_up|down|prefill_up|prefill_down|m1|m32> [iters]
+
+Each iteration runs the layer's two kernels (quantize + LoRA down, then GEMM +
+LoRA up + affine) on one of R replicas of the inputs, so that consecutive
+launches read distinct buffers (the replicas total more than the 129 MB L2
+for the M=700 shapes).  Meant to be run under a profiler that captures one
+launch after a few warm-up ones (e.g. `-k regex:gemm -s 25 -c 1`).  Prints
+one line with the kernel the dispatcher chose.
+"""
+from __future__ import annotations
+
+import os
+import sys
+
+import numpy as np
+
+sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+
+from synthetic import DECODER_LAYER_M700, make_linear_case  # noqa: E402
+
+SHAPES = dict(DECODER_LAYER_M700)
+SHAPES.update({
+    "prefill_up": dict(M=8192, K=4096, N=14336, r=32),
+    "prefill_down": dict(M=8192, K=14336, N=4096, r=32),
+    "m1": dict(M=1, K=4096, N=4096, r=32),
+    "m32": dict(M=32, K=4096, N=4096, r=32),
+})
+
+
+def main() -> int:
+    import torch
+
+    from w4a4_quantized_gemm_gb300 import build as wbuild
+    wbuild.build()
+    import w4a4_quantized_gemm_gb300 as w4
+
+    name = sys.argv[1] if len(sys.argv) > 1 else "qkv"
+    iters = int(sys.argv[2]) if len(sys.argv) > 2 else 30
+    s = SHAPES[name]
+    M, K, N, r = s["M"], s["K"], s["N"], s["r"]
+    c = make_linear_case(M=M, K=K, N=N, r=r, seed=0)
+    dev = torch.device("cuda", 0)
+    per_rep = N * K // 2 + 2 * M * (K + N)
+    R = 1 if per_rep > 256 * 2 ** 20 else max(2, min(24, (300 * 2 ** 20) // per_rep))
+    X = torch.from_numpy(c.X.view(np.float16).copy()).to(dev)
+    W = torch.from_numpy(c.W).to(dev)
+    Ld = torch.from_numpy(c.L_down.view(np.float16).copy()).to(dev)
+    Lu = torch.from_numpy(c.L_up.view(np.float16).copy()).to(dev)
+    cs = torch.from_numpy(c.colscale.view(np.float16).copy()).to(dev)
+    b = torch.from_numpy(c.bias.view(np.float16).copy()).to(dev)
+    packed = torch.empty(w4.packed_weights_bytes(N, K, r), dtype=torch.uint8, device=dev)
+    w4.w4a4_pack_weights(W, Ld, Lu, packed, r)
+    del W
+    Xs = [X.clone() for _ in range(R)]
+    Ps = [packed.clone() for _ in range(R)]
+    WS = [torch.empty(w4.act_workspace_bytes(M, K, r), dtype=torch.uint8, device=dev) for _ in range(R)]
+    Ys = [torch.empty((M, N), dtype=torch.float16, device=dev) for _ in range(R)]
+    for i in range(iters):
+        j = i % R
+        w4.w4a4_quantize_act(Xs[j], Ps[j], WS[j], r)
+        w4.w4a4_linear(WS[j], Ps[j], cs, b, Ys[j], K, r)
+    torch.cuda.synchronize()
+    print(f"{name}: M={M} K={K} N={N} r={r} replicas={R} iters={iters} dispatch={w4.w4a4_last_dispatch()}")
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())
