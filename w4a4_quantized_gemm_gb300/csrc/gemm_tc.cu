@@ -9,18 +9,30 @@
 //
 // Structure (the warp-specialised persistent design of the Blackwell W4A4
 // article, section 3.2, rebuilt for tcgen05): one CTA per SM walks tiles in a
-// static round-robin; warps have fixed roles and talk through mbarriers:
-//   warp 0      producer: 1-D bulk copies of activation codes, (sA, SA),
-//               packed weight nibbles and scales into a STAGES-deep ring, and
-//               the tile's LoRA operands;
-//   warp 1      MMA issuer (one thread) + tensor-memory owner: per group two
-//               kind::f8f6f4 MMAs (K = 32 each) into one of two TMEM buffers,
-//               per tile one kind::f16 LoRA-up MMA chain;
-//   warps 2-3   nibble -> E4M3 expansion of the weight tile into the
-//               32-byte-swizzled B operand, fp16 -> fp32 weight scales;
-//   warps 4-11  epilogue: TMEM -> registers, per-group scale-FMA into fp32
-//               running sums (two warpgroups, 64 columns each), then the
-//               column affine and the fp16 store.
+// static round-robin; warps have fixed roles and talk through mbarriers.
+// Work moves in jobs of two K groups, so that every role synchronises once per
+// two groups.  Tensor memory holds two job buffers (2 x 2 x 128 columns):
+//   warps 20,22,23  producers: per job the 1-D bulk copies of activation
+//               codes, weight nibbles, and (sA, SA) + weight scales into an
+//               S-deep stage ring, one warp each so that the issues overlap;
+//               per tile the LoRA operands;
+//   warp 21     MMA issuer (one thread) + tensor-memory owner: per tile a
+//               kind::f16 LoRA-up chain, per group two kind::f8f6f4 MMAs
+//               (M = N = 128, K = 32) into its 128 columns of a job buffer;
+//   warps 16-19 nibble -> E4M3 expansion of the weight tiles into the
+//               32-byte-swizzled B operand (32 rows each, one warp per SM
+//               sub-partition) and the groups' scales as fp32 into a scale
+//               ring that outlives the stage;
+//   warps 0-15  epilogue, four warps per TMEM lane quarter and 32 columns
+//               each: per job the two product slices come out of tensor
+//               memory in 16-column chunks and two FMAs per element (packed
+//               fp32 pairs) fold each group into the running sums held in
+//               registers; at the end of a tile the column affine and the
+//               fp16 store.
+// The per-group fp32 scaling (two FMAs per output) is the floor of this
+// kernel; its instruction count, not the tensor pipe, sets the pace, so the
+// epilogue is spread over 16 warps and every fixed per-group cost is paid
+// once per job.
 // Every wait is bounded (2 s); on give-up the kernel records
 // W4A4_ERR_TIMEOUT in its status word, unwinds every role, waits for its own
 // copies and MMAs, frees tensor memory and returns.
@@ -36,33 +48,60 @@ using namespace tc;
 
 constexpr int BN = 128;  // output columns per tile (MMA N)
 constexpr int BM = 128;  // output rows per tile (MMA M, TMEM lanes)
-constexpr int STAGES = 5;
-constexpr int NUM_THREADS = 384;
-constexpr int WARP_PRODUCER = 0, WARP_MMA = 1, WARP_EXPAND0 = 2, NUM_EXPAND_WARPS = 2;
-constexpr int WARP_EPI0 = 4, NUM_EPI_WARPS = 8;
-constexpr uint32_t TMEM_COLS = 512;  // two BN-column buffers used; whole TMEM held (one CTA per SM)
+constexpr int GPJ = 2;   // K groups per job: every role synchronises once per job
+constexpr int NUM_THREADS = 768;
+constexpr int NUM_EPI_WARPS = 16, WARP_EXP0 = 16, NUM_EXP_WARPS = 4;
+constexpr int WARP_PRODUCER = 20, WARP_MMA = 21, WARP_PRODUCER_W = 22, WARP_PRODUCER_S = 23;
+constexpr int NUM_PRODUCERS = 3;
+constexpr int EPI_COLS = BN / 4;  // columns per epilogue warp
+constexpr int EXP_ROWS = BN / NUM_EXP_WARPS;
+constexpr int EPI_REGS = 96, OTHER_REGS = 48;
+static_assert(NUM_EPI_WARPS * 32 * EPI_REGS + (NUM_THREADS - NUM_EPI_WARPS * 32) * OTHER_REGS <= 65536,
+              "register split exceeds the register file");
+constexpr int NPB = 2;  // job buffers in tensor memory, GPJ x 128 columns each
+constexpr uint32_t TMEM_COLS = 512;
+static_assert(NPB * GPJ * BN <= int(TMEM_COLS), "job buffers must fit in tensor memory");
+constexpr int SS = 4;  // scale-ring depth (jobs)
 constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;
 constexpr uint64_t DRAIN_LIMIT_NS = 200000000ull;
+// Sleep between barrier polls, per role: the producers and the expansion run
+// stages ahead and can wake late; the MMA issuer and the epilogue are on the
+// critical path.
+constexpr uint32_t BACKOFF_PRODUCER = 256, BACKOFF_EXPAND = 128, BACKOFF_MMA = 32, BACKOFF_EPI = 64;
 
-// Shared-memory map (byte offsets from a 1024-aligned base).
-constexpr uint32_t kStageA = 2 * BM * 32;  // 2 planes x 128 rows x 32 B
-constexpr uint32_t kStageB = 2 * BN * 32;
-constexpr uint32_t OFF_A = 0;
-constexpr uint32_t OFF_B = OFF_A + STAGES * kStageA;
-constexpr uint32_t OFF_WP = OFF_B + STAGES * kStageB;
-constexpr uint32_t OFF_SS = OFF_WP + STAGES * BN * 32;
-constexpr uint32_t OFF_SW16 = OFF_SS + STAGES * BM * 8;
-constexpr uint32_t OFF_SWF = OFF_SW16 + STAGES * BN * 2;
-constexpr uint32_t OFF_LA = OFF_SWF + STAGES * BN * 4;
-constexpr int kNumBars = 3 * STAGES + 7;
+// Stage (one job = GPJ groups): activation codes (per group 2 planes x 128 rows
+// x 32 B), weight nibbles (per group 128 rows x 32 B), the expanded B operand
+// (per group 2 planes x 128 rows x 32 B), (sA, SA) per row and group, fp16
+// weight scales.  Operand planes are 256-byte aligned.
+constexpr uint32_t kA = 2 * BM * 32, kW = BN * 32, kB = 2 * BN * 32, kS = BM * 8, kSw = BN * 2;
+constexpr uint32_t ST_A = 0, ST_W = ST_A + GPJ * kA, ST_B = ST_W + GPJ * kW, ST_S = ST_B + GPJ * kB,
+                   ST_SW = ST_S + GPJ * kS;
+constexpr uint32_t kStage = ST_SW + GPJ * kSw;
+// Scale-ring entry, per group of the job: fp32 sW of the tile's 128 columns,
+// then (sA, SA) of its 128 rows.
+constexpr uint32_t kScaleG = BN * 4 + BM * 8;
+constexpr uint32_t kScale = GPJ * kScaleG;
+static_assert(kStage % 256 == 0 && ST_B % 256 == 0 && ST_W % 256 == 0 && kA % 256 == 0 && kB % 256 == 0,
+              "operand planes need 256 B alignment");
 
-__host__ __device__ constexpr uint32_t off_lu(int rp) { return OFF_LA + uint32_t(rp) * BM * 32; }
-__host__ __device__ constexpr uint32_t off_bar(int rp) { return (off_lu(rp) + uint32_t(rp) * BN * 32 + 7u) & ~7u; }
-// + 1024 for aligning the base, + 8 KB of unused tail slack
-__host__ __device__ constexpr uint32_t smem_bytes(int rp) { return off_bar(rp) + kNumBars * 8 + 8 + 1024 + 8192; }
-static_assert(smem_bytes(8) <= 227 * 1024, "shared-memory budget exceeded at rank 128");
+struct Map {
+    uint32_t ST, SC, LA, LU, BAR, SLOT, total;
+};
+__host__ __device__ constexpr Map smem_map(int S, int rp) {
+    Map m{};
+    m.ST = 0;
+    m.SC = m.ST + uint32_t(S) * kStage;
+    m.LA = m.SC + SS * kScale;
+    m.LU = m.LA + uint32_t(rp) * BM * 32;
+    m.BAR = m.LU + uint32_t(rp) * BN * 32;
+    m.SLOT = m.BAR + (3 * S + 2 * SS + 2 * NPB + 3) * 8;
+    m.total = m.SLOT + 16 + 1024;  // + base alignment
+    return m;
+}
+static_assert(smem_map(4, 2).total <= 227 * 1024, "4 stages must fit at rank 32");
+static_assert(smem_map(3, 8).total <= 227 * 1024, "3 stages must fit at rank 128");
 
-template <bool DUMP>
+template <int S, bool DUMP>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_tc_kernel(const uint8_t* __restrict__ ws, const uint8_t* __restrict__ packed,
                    const uint16_t* __restrict__ colscale, const uint16_t* __restrict__ bias, int M, int N, int K,
@@ -74,44 +113,49 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int G = K / kGroup;
+    const int J = (G + GPJ - 1) / GPJ;  // jobs per tile
     const int RP = DUMP ? 0 : r / 16;
     const ActLayout AL = act_layout(M, K, r);
     const PackedLayout PL = packed_layout(N, K, r);
     const int MT = AL.MT, NT = (N + BN - 1) / BN;
     const int tiles = MT * NT;
+    const Map mp = smem_map(S, RP);
 
-    const uint32_t LU = off_lu(RP);
-    const uint32_t BAR = off_bar(RP);
-    auto full = [&](int s) { return base + BAR + 8u * s; };
-    auto bready = [&](int s) { return base + BAR + 8u * (STAGES + s); };
-    auto empty = [&](int s) { return base + BAR + 8u * (2 * STAGES + s); };
-    auto tfull = [&](int b) { return base + BAR + 8u * (3 * STAGES + b); };
-    auto tempty = [&](int b) { return base + BAR + 8u * (3 * STAGES + 2 + b); };
-    const uint32_t lfull = base + BAR + 8u * (3 * STAGES + 4);
-    const uint32_t lempty = base + BAR + 8u * (3 * STAGES + 5);
-    const uint32_t mmadone = base + BAR + 8u * (3 * STAGES + 6);
-    const uint32_t TSLOT = BAR + 8u * kNumBars;
-    volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(gbase + TSLOT);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + TSLOT + 4);
+    auto full = [&](int s) { return base + mp.BAR + 8u * s; };             // copies landed (producers + tx)
+    auto bready = [&](int s) { return base + mp.BAR + 8u * (S + s); };     // B operand expanded
+    auto empty = [&](int s) { return base + mp.BAR + 8u * (2 * S + s); };  // MMAs done with the stage
+    auto sfull = [&](int q) { return base + mp.BAR + 8u * (3 * S + q); };  // scale entry written
+    auto sempty = [&](int q) { return base + mp.BAR + 8u * (3 * S + SS + q); };  // epilogue done with it
+    auto tfull = [&](int b) { return base + mp.BAR + 8u * (3 * S + 2 * SS + b); };
+    auto tempty = [&](int b) { return base + mp.BAR + 8u * (3 * S + 2 * SS + NPB + b); };
+    const uint32_t lfull = base + mp.BAR + 8u * (3 * S + 2 * SS + 2 * NPB);
+    const uint32_t lempty = lfull + 8u;
+    const uint32_t mmadone = lfull + 16u;
+    volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(gbase + mp.SLOT);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + mp.SLOT + 4);
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < STAGES; ++s) {
-            mbar_init(full(s), 1);
-            mbar_init(bready(s), NUM_EXPAND_WARPS);
-            mbar_init(empty(s), 1 + NUM_EPI_WARPS);
+        for (int s = 0; s < S; ++s) {
+            mbar_init(full(s), NUM_PRODUCERS);
+            mbar_init(bready(s), NUM_EXP_WARPS);
+            mbar_init(empty(s), 1);
         }
-        for (int b = 0; b < 2; ++b) {
+        for (int q = 0; q < SS; ++q) {
+            mbar_init(sfull(q), NUM_EXP_WARPS);
+            mbar_init(sempty(q), NUM_EPI_WARPS);
+        }
+        for (int b = 0; b < NPB; ++b) {
             mbar_init(tfull(b), 1);
             mbar_init(tempty(b), NUM_EPI_WARPS);
         }
-        mbar_init(lfull, 1);
+        mbar_init(lfull, 2);
         mbar_init(lempty, 1);
         mbar_init(mmadone, 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
     if (warp == WARP_MMA) {
-        tmem_alloc(base + TSLOT, TMEM_COLS);
+        tmem_alloc(base + mp.SLOT, TMEM_COLS);
         tmem_relinquish();
     }
     tc_fence_before();
@@ -125,115 +169,160 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         *abort_flag = 1;
     };
 
-    if (warp == WARP_PRODUCER) {
-        if (lane == 0) {
-            uint32_t it = 0, lp = 0, lora_issued = 0;
-            bool ok = true;
-            for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
-                const int mt = t % MT, n0 = (t / MT) * BN;
-                const int rows = min(BN, N - n0);
-                if (RP > 0) {
-                    if (!wait_parity(lempty, lp ^ 1u, abort_flag, WAIT_LIMIT_NS)) {
-                        ok = false;
-                        break;
-                    }
-                    mbar_expect_tx(lfull, uint32_t(RP) * (BM * 32 + rows * 32));
-                    bulk_g2s(base + OFF_LA, ws + AL.La + size_t(mt) * RP * (BM * 32), uint32_t(RP) * BM * 32, lfull);
-                    for (int p = 0; p < RP; ++p)
-                        bulk_g2s(base + LU + uint32_t(p) * BN * 32, packed + PL.Lu + (size_t(p) * N + n0) * 32,
-                                 uint32_t(rows) * 32, lfull);
-                    lp ^= 1u;
-                    lora_issued = 1;
-                }
-                for (int g = 0; g < G; ++g) {
-                    const int s = int(it % STAGES);
-                    const uint32_t ph = (it / STAGES) & 1u;
-                    if (!wait_parity(empty(s), ph ^ 1u, abort_flag, WAIT_LIMIT_NS)) {
-                        ok = false;
-                        break;
-                    }
-                    mbar_expect_tx(full(s), kStageA + BM * 8 + uint32_t(rows) * 34);
-                    const size_t ag = size_t(mt) * G + g;
-                    bulk_g2s(base + OFF_A + s * kStageA, ws + AL.qA + ag * kStageA, kStageA, full(s));
-                    bulk_g2s(base + OFF_SS + s * (BM * 8), ws + AL.sS + ag * (BM * 8), BM * 8, full(s));
-                    bulk_g2s(base + OFF_WP + s * (BN * 32), packed + PL.qW + (size_t(g) * N + n0) * 32,
-                             uint32_t(rows) * 32, full(s));
-                    bulk_g2s(base + OFF_SW16 + s * (BN * 2), packed + PL.sW + (size_t(g) * N + n0) * 2,
-                             uint32_t(rows) * 2, full(s));
-                    ++it;
-                }
-            }
-            if (!ok) fail();
-            // drain: the copies of the last STAGES iterations (distinct stages) and the last LoRA load
-            for (uint32_t k = (it > STAGES ? it - STAGES : 0u); k < it; ++k)
-                wait_parity(full(int(k % STAGES)), (k / STAGES) & 1u, &no_abort, DRAIN_LIMIT_NS);
-            if (lora_issued) wait_parity(lfull, lp ^ 1u, &no_abort, DRAIN_LIMIT_NS);
-        }
-    } else if (warp == WARP_MMA) {
-        if (lane == 0) {
-            constexpr uint32_t IDESC = idesc_m128(BN);
-            uint32_t it = 0, jc = 0, lp = 0;
-            bool ok = true;
-            for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
-                if (RP > 0) {
-                    const uint32_t b = jc & 1u, tph = (jc >> 1) & 1u;
-                    if (!wait_parity(tempty(b), tph ^ 1u, abort_flag, WAIT_LIMIT_NS) ||
-                        !wait_parity(lfull, lp, abort_flag, WAIT_LIMIT_NS)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    for (int p = 0; p < RP; ++p)
-                        mma_f16(tmem + b * BN, sdesc_sw32(base + OFF_LA + uint32_t(p) * BM * 32),
-                                sdesc_sw32(base + LU + uint32_t(p) * BN * 32), IDESC, p > 0 ? 1u : 0u);
-                    mma_commit(tfull(b));
-                    mma_commit(lempty);
-                    ++jc;
-                    lp ^= 1u;
-                }
-                for (int g = 0; g < G; ++g) {
-                    const int s = int(it % STAGES);
-                    const uint32_t ph = (it / STAGES) & 1u;
-                    const uint32_t b = jc & 1u, tph = (jc >> 1) & 1u;
-                    if (!wait_parity(full(s), ph, abort_flag, WAIT_LIMIT_NS) ||
-                        !wait_parity(bready(s), ph, abort_flag, WAIT_LIMIT_NS) ||
-                        !wait_parity(tempty(b), tph ^ 1u, abort_flag, WAIT_LIMIT_NS)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    const uint32_t a0 = base + OFF_A + s * kStageA, b0 = base + OFF_B + s * kStageB;
-                    mma_f8(tmem + b * BN, sdesc_sw32(a0), sdesc_sw32(b0), IDESC, 0u);
-                    mma_f8(tmem + b * BN, sdesc_sw32(a0 + BM * 32), sdesc_sw32(b0 + BN * 32), IDESC, 1u);
-                    mma_commit(empty(s));
-                    mma_commit(tfull(b));
-                    ++it;
-                    ++jc;
-                }
-            }
-            if (!ok) fail();
-            mma_commit(mmadone);  // every MMA issued above has completed once this arrives
-            wait_parity(mmadone, 0u, &no_abort, DRAIN_LIMIT_NS);
-        }
-    } else if (warp < WARP_EPI0) {
-        // ---- expansion: packed offset-binary nibbles -> E4M3 B operand planes
-        const int et = (warp - WARP_EXPAND0) * 32 + lane;
-        uint32_t it = 0;
+    // Register re-budgeting: each role re-sizes its warpgroup on entry (the
+    // four warps of a warpgroup always take the same branch).
+    if (warp >= WARP_EXP0) regs_dec<OTHER_REGS>();
+
+    if (warp == WARP_PRODUCER || warp == WARP_PRODUCER_W || warp == WARP_PRODUCER_S) {
+        // role 0 = activation codes + LoRA activations, 1 = weight nibbles + L_up,
+        // 2 = (sA, SA) and the fp16 weight scales.  Each arrives on the stage's
+        // barrier with its own byte count.  Lane 0 issues; the warp walks the loop.
+        const int role = warp == WARP_PRODUCER ? 0 : warp == WARP_PRODUCER_W ? 1 : 2;
+        uint32_t it = 0, lp = 0, lora_issued = 0;
         bool ok = true;
         for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
-            for (int g = 0; g < G; ++g) {
-                const int s = int(it % STAGES);
-                const uint32_t ph = (it / STAGES) & 1u;
-                if (!wait_parity(full(s), ph, abort_flag, WAIT_LIMIT_NS)) {
+            const int mt = t % MT, n0 = (t / MT) * BN;
+            const int rows = min(BN, N - n0);
+            if (RP > 0 && role < 2) {
+                if (!warp_wait_parity(lempty, lp ^ 1u, abort_flag, WAIT_LIMIT_NS, BACKOFF_PRODUCER)) {
                     ok = false;
                     break;
                 }
-                uint8_t* bp = gbase + OFF_B + s * kStageB;
-                const uint8_t* wp = gbase + OFF_WP + s * (BN * 32);
-                const uint16_t* sw16 = reinterpret_cast<const uint16_t*>(gbase + OFF_SW16 + s * (BN * 2));
-                float* swf = reinterpret_cast<float*>(gbase + OFF_SWF + s * (BN * 4));
-#pragma unroll
-                for (int row = et; row < BN; row += NUM_EXPAND_WARPS * 32) {
+                if (lane == 0) {
+                    if (role == 0) {
+                        mbar_expect_tx(lfull, uint32_t(RP) * BM * 32);
+                        bulk_g2s(base + mp.LA, ws + AL.La + size_t(mt) * RP * (BM * 32), uint32_t(RP) * BM * 32,
+                                 lfull);
+                    } else {
+                        mbar_expect_tx(lfull, uint32_t(RP) * rows * 32);
+                        for (int p = 0; p < RP; ++p)
+                            bulk_g2s(base + mp.LU + uint32_t(p) * BN * 32, packed + PL.Lu + (size_t(p) * N + n0) * 32,
+                                     uint32_t(rows) * 32, lfull);
+                    }
+                }
+                __syncwarp();
+                lp ^= 1u;
+                lora_issued = 1;
+            }
+            for (int jb = 0; jb < J; ++jb) {
+                const int g0 = jb * GPJ, ng = min(GPJ, G - g0);
+                const int s = int(it % S);
+                const uint32_t ph = (it / S) & 1u;
+                if (!warp_wait_parity(empty(s), ph ^ 1u, abort_flag, WAIT_LIMIT_NS, BACKOFF_PRODUCER)) {
+                    ok = false;
+                    break;
+                }
+                if (lane == 0) {
+                    const uint32_t sb = base + mp.ST + uint32_t(s) * kStage;
+                    const size_t ag = size_t(mt) * G + g0;
+                    if (role == 0) {
+                        mbar_expect_tx(full(s), uint32_t(ng) * kA);
+                        bulk_g2s(sb + ST_A, ws + AL.qA + ag * kA, uint32_t(ng) * kA, full(s));
+                    } else if (role == 1) {
+                        mbar_expect_tx(full(s), uint32_t(ng * rows) * 32);
+                        for (int j = 0; j < ng; ++j)
+                            bulk_g2s(sb + ST_W + uint32_t(j) * kW, packed + PL.qW + (size_t(g0 + j) * N + n0) * 32,
+                                     uint32_t(rows) * 32, full(s));
+                    } else {
+                        mbar_expect_tx(full(s), uint32_t(ng) * kS + uint32_t(ng * rows) * 2);
+                        bulk_g2s(sb + ST_S, ws + AL.sS + ag * kS, uint32_t(ng) * kS, full(s));
+                        for (int j = 0; j < ng; ++j)
+                            bulk_g2s(sb + ST_SW + uint32_t(j) * kSw, packed + PL.sW + (size_t(g0 + j) * N + n0) * 2,
+                                     uint32_t(rows) * 2, full(s));
+                    }
+                }
+                __syncwarp();
+                ++it;
+            }
+        }
+        if (!ok && lane == 0) fail();
+        // drain: the copies of the last S jobs (distinct stages) and the last LoRA load
+        if (lane == 0) {
+            for (uint32_t k = (it > uint32_t(S) ? it - S : 0u); k < it; ++k)
+                wait_parity(full(int(k % S)), (k / S) & 1u, &no_abort, DRAIN_LIMIT_NS);
+            if (lora_issued) wait_parity(lfull, lp ^ 1u, &no_abort, DRAIN_LIMIT_NS);
+        }
+        __syncwarp();
+    } else if (warp == WARP_MMA) {
+        constexpr uint32_t IDESC = idesc_m128(BN);
+        uint32_t it = 0, jc = 0, lp = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
+            if (RP > 0) {
+                // the LoRA product takes a job buffer of its own (first 128 columns)
+                const uint32_t b = jc % NPB, tph = (jc / NPB) & 1u;
+                if (!warp_wait_parity(tempty(b), tph ^ 1u, abort_flag, WAIT_LIMIT_NS, BACKOFF_MMA) ||
+                    !warp_wait_parity(lfull, lp, abort_flag, WAIT_LIMIT_NS, BACKOFF_MMA)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                if (lane == 0) {
+                    for (int p = 0; p < RP; ++p)
+                        mma_f16(tmem + b * (GPJ * BN), sdesc_sw32(base + mp.LA + uint32_t(p) * BM * 32),
+                                sdesc_sw32(base + mp.LU + uint32_t(p) * BN * 32), IDESC, p > 0 ? 1u : 0u);
+                    mma_commit(tfull(b));
+                    mma_commit(lempty);
+                }
+                __syncwarp();
+                ++jc;
+                lp ^= 1u;
+            }
+            for (int jb = 0; jb < J; ++jb) {
+                const int ng = min(GPJ, G - jb * GPJ);
+                const int s = int(it % S);
+                const uint32_t ph = (it / S) & 1u;
+                const uint32_t b = jc % NPB, tph = (jc / NPB) & 1u;
+                if (!warp_wait_parity(full(s), ph, abort_flag, WAIT_LIMIT_NS, BACKOFF_MMA) ||
+                    !warp_wait_parity(bready(s), ph, abort_flag, WAIT_LIMIT_NS, BACKOFF_MMA) ||
+                    !warp_wait_parity(tempty(b), tph ^ 1u, abort_flag, WAIT_LIMIT_NS, BACKOFF_MMA)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                if (lane == 0) {
+                    const uint32_t sb = base + mp.ST + uint32_t(s) * kStage;
+                    for (int j = 0; j < ng; ++j) {
+                        const uint32_t d = tmem + b * (GPJ * BN) + uint32_t(j) * BN;
+                        const uint32_t a0 = sb + ST_A + uint32_t(j) * kA, b0 = sb + ST_B + uint32_t(j) * kB;
+                        mma_f8(d, sdesc_sw32(a0), sdesc_sw32(b0), IDESC, 0u);
+                        mma_f8(d, sdesc_sw32(a0 + BM * 32), sdesc_sw32(b0 + BN * 32), IDESC, 1u);
+                    }
+                    mma_commit(tfull(b));
+                    mma_commit(empty(s));
+                }
+                __syncwarp();
+                ++it;
+                ++jc;
+            }
+        }
+        if (!ok && lane == 0) fail();
+        if (lane == 0) {
+            mma_commit(mmadone);  // every MMA issued above has completed once this arrives
+            wait_parity(mmadone, 0u, &no_abort, DRAIN_LIMIT_NS);
+        }
+        __syncwarp();
+    } else if (warp >= WARP_EXP0 && warp < WARP_EXP0 + NUM_EXP_WARPS) {
+        // ---- expansion: packed offset-binary nibbles -> E4M3 B operand planes, scales -> fp32
+        const int e = warp - WARP_EXP0;
+        const int row = e * EXP_ROWS + lane;
+        static_assert(EXP_ROWS == 32, "one expansion row per lane");
+        uint32_t it = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
+            for (int jb = 0; jb < J; ++jb) {
+                const int ng = min(GPJ, G - jb * GPJ);
+                const int s = int(it % S), q = int(it % SS);
+                const uint32_t ph = (it / S) & 1u, sph = (it / SS) & 1u;
+                if (!warp_wait_parity(full(s), ph, abort_flag, WAIT_LIMIT_NS, BACKOFF_EXPAND) ||
+                    !warp_wait_parity(sempty(q), sph ^ 1u, abort_flag, WAIT_LIMIT_NS, BACKOFF_EXPAND)) {
+                    ok = false;
+                    break;
+                }
+                uint8_t* sp = gbase + mp.ST + uint32_t(s) * kStage;
+                uint8_t* scp = gbase + mp.SC + uint32_t(q) * kScale;
+                for (int j = 0; j < ng; ++j) {
+                    const uint8_t* wp = sp + ST_W + uint32_t(j) * kW;
                     const uint4 w01 = *reinterpret_cast<const uint4*>(wp + row * 32);
                     const uint4 w23 = *reinterpret_cast<const uint4*>(wp + row * 32 + 16);
                     // words: w01 = (q0h0, q0h1, q1h0, q1h1), w23 = (q2h0, q2h1, q3h0, q3h1)
@@ -243,24 +332,33 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     const uint4 p1c0 = make_uint4(expand4(w01.y), expand4(w01.w), expand4(w23.y), expand4(w23.w));
                     const uint4 p1c1 = make_uint4(expand4(w01.y >> 16), expand4(w01.w >> 16), expand4(w23.y >> 16),
                                                   expand4(w23.w >> 16));
+                    uint8_t* bp = sp + ST_B + uint32_t(j) * kB;
                     *reinterpret_cast<uint4*>(bp + row * 32 + swz32(row, 0) * 16) = p0c0;
                     *reinterpret_cast<uint4*>(bp + row * 32 + swz32(row, 1) * 16) = p0c1;
                     *reinterpret_cast<uint4*>(bp + BN * 32 + row * 32 + swz32(row, 0) * 16) = p1c0;
                     *reinterpret_cast<uint4*>(bp + BN * 32 + row * 32 + swz32(row, 1) * 16) = p1c1;
-                    swf[row] = __half2float(__ushort_as_half(sw16[row]));
+                    uint8_t* sg = scp + uint32_t(j) * kScaleG;
+                    reinterpret_cast<float*>(sg)[row] = __half2float(
+                        __ushort_as_half(reinterpret_cast<const uint16_t*>(sp + ST_SW + uint32_t(j) * kSw)[row]));
+                    // (sA, SA) of this lane's row (rows and weight rows share the index range 0..127)
+                    reinterpret_cast<float2*>(sg + BN * 4)[row] =
+                        reinterpret_cast<const float2*>(sp + ST_S + uint32_t(j) * kS)[row];
                 }
                 fence_proxy_async_smem();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(bready(s));
+                if (lane == 0) {
+                    mbar_arrive(bready(s));
+                    mbar_arrive(sfull(q));
+                }
                 ++it;
             }
         }
         if (!ok) fail();
-    } else {
+    } else if (warp < NUM_EPI_WARPS) {
         // ---- epilogue
-        const int ew = warp - WARP_EPI0;
-        const int c0 = (ew >> 2) * 64;  // column half of the tile
-        const int lq = warp & 3;        // TMEM lane quarter this warp may access
+        regs_inc<EPI_REGS>();
+        const int lq = warp & 3;                // TMEM lane quarter this warp may access
+        const int c0 = (warp >> 2) * EPI_COLS;  // column slice of the tile
         const int row = lq * 32 + lane;
         const uint32_t tl = tmem + (uint32_t(lq * 32) << 16) + uint32_t(c0);
         uint32_t it = 0, jc = 0;
@@ -268,87 +366,96 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
             const int mt = t % MT, n0 = (t / MT) * BN;
             const int m = mt * BM + row;
-            float acc[64];
-#pragma unroll
-            for (int c = 0; c < 64; ++c) acc[c] = 0.f;
+            uint64_t acc[EPI_COLS / 2];  // running sums as packed column pairs
             if (RP > 0) {
-                const uint32_t b = jc & 1u, tph = (jc >> 1) & 1u;
-                if (!wait_parity(tfull(b), tph, abort_flag, WAIT_LIMIT_NS)) {
+                const uint32_t b = jc % NPB, tph = (jc / NPB) & 1u;
+                if (!warp_wait_parity(tfull(b), tph, abort_flag, WAIT_LIMIT_NS, BACKOFF_EPI)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                __syncwarp();
-                float v0[32], v1[32];
-                tmem_ld32(tl + b * BN, v0);
-                tmem_ld32(tl + b * BN + 32, v1);
+                float l[EPI_COLS];
+                tmem_ld32(tl + b * (GPJ * BN), l);
                 tmem_wait_ld();
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(tempty(b));
 #pragma unroll
-                for (int c = 0; c < 32; ++c) {
-                    acc[c] = v0[c];
-                    acc[32 + c] = v1[c];
-                }
+                for (int c = 0; c < EPI_COLS / 2; ++c) acc[c] = f2_pack(l[2 * c], l[2 * c + 1]);
                 ++jc;
+            } else {
+#pragma unroll
+                for (int c = 0; c < EPI_COLS / 2; ++c) acc[c] = 0ull;
             }
-            for (int g = 0; g < G; ++g) {
-                const int s = int(it % STAGES);
-                const uint32_t ph = (it / STAGES) & 1u;
-                const uint32_t b = jc & 1u, tph = (jc >> 1) & 1u;
-                if (!wait_parity(tfull(b), tph, abort_flag, WAIT_LIMIT_NS) ||
-                    !wait_parity(full(s), ph, abort_flag, WAIT_LIMIT_NS) ||
-                    !wait_parity(bready(s), ph, abort_flag, WAIT_LIMIT_NS)) {
+            for (int jb = 0; jb < J; ++jb) {
+                const int g0 = jb * GPJ;
+                const bool two = g0 + 1 < G;
+                const int q = int(it % SS);
+                const uint32_t sph = (it / SS) & 1u;
+                const uint32_t b = jc % NPB, tph = (jc / NPB) & 1u;
+                if (!warp_wait_parity(tfull(b), tph, abort_flag, WAIT_LIMIT_NS, BACKOFF_EPI) ||
+                    !warp_wait_parity(sfull(q), sph, abort_flag, WAIT_LIMIT_NS, BACKOFF_EPI)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                __syncwarp();
-                float v[64];
-                {
-                    float v0[32], v1[32];
-                    tmem_ld32(tl + b * BN, v0);
-                    tmem_ld32(tl + b * BN + 32, v1);
+                const uint8_t* sc0 = gbase + mp.SC + uint32_t(q) * kScale;
+                const uint8_t* sc1 = sc0 + kScaleG;
+                const float2 sv0 = reinterpret_cast<const float2*>(sc0 + BN * 4)[row];
+                const float2 sv1 = two ? reinterpret_cast<const float2*>(sc1 + BN * 4)[row] : make_float2(0.f, 0.f);
+                const float cm0 = (-8.f * sv0.y) * sv0.x, cm1 = (-8.f * sv1.y) * sv1.x;
+                const uint64_t sa0 = f2_pack(sv0.x, sv0.x), cc0 = f2_pack(cm0, cm0);
+                const uint64_t sa1 = f2_pack(sv1.x, sv1.x), cc1 = f2_pack(cm1, cm1);
+                const uint32_t tb = tl + b * (GPJ * BN);
+#pragma unroll
+                for (int ch = 0; ch < EPI_COLS / 16; ++ch) {
+                    float d0[16], d1[16];
+                    tmem_ld16(tb + ch * 16, d0);
+                    if (two) tmem_ld16(tb + BN + ch * 16, d1);
                     tmem_wait_ld();
-#pragma unroll
-                    for (int c = 0; c < 32; ++c) {
-                        v[c] = v0[c];
-                        v[32 + c] = v1[c];
+                    if (ch == EPI_COLS / 16 - 1) {
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(tempty(b));
                     }
-                }
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(tempty(b));
-                const float2 sv = reinterpret_cast<const float2*>(gbase + OFF_SS + s * (BM * 8))[row];
-                if constexpr (DUMP) {
-                    if (m < M) {
+                    if constexpr (DUMP) {
+                        if (m < M) {
 #pragma unroll
-                        for (int c = 0; c < 64; ++c) {
-                            const int n = n0 + c0 + c;
-                            if (n < N) P[(size_t(m) * N + n) * G + g] = int32_t(v[c] - 8.f * sv.y);
+                            for (int c = 0; c < 16; ++c) {
+                                const int n = n0 + c0 + ch * 16 + c;
+                                if (n < N) {
+                                    P[(size_t(m) * N + n) * G + g0] = int32_t(d0[c] - 8.f * sv0.y);
+                                    if (two) P[(size_t(m) * N + n) * G + g0 + 1] = int32_t(d1[c] - 8.f * sv1.y);
+                                }
+                            }
+                        }
+                    } else {
+                        // t = sA D - 8 SA sA, acc += sW t, two columns per instruction
+                        uint64_t* a = acc + ch * 8;
+                        const ulonglong2* w0 = reinterpret_cast<const ulonglong2*>(sc0 + (c0 + ch * 16) * 4);
+#pragma unroll
+                        for (int c4 = 0; c4 < 4; ++c4) {
+                            const ulonglong2 w = w0[c4];
+                            a[2 * c4] = ffma2_b64(w.x, ffma2_b64(sa0, f2_pack(d0[4 * c4], d0[4 * c4 + 1]), cc0),
+                                                  a[2 * c4]);
+                            a[2 * c4 + 1] = ffma2_b64(
+                                w.y, ffma2_b64(sa0, f2_pack(d0[4 * c4 + 2], d0[4 * c4 + 3]), cc0), a[2 * c4 + 1]);
+                        }
+                        if (two) {
+                            const ulonglong2* w1 = reinterpret_cast<const ulonglong2*>(sc1 + (c0 + ch * 16) * 4);
+#pragma unroll
+                            for (int c4 = 0; c4 < 4; ++c4) {
+                                const ulonglong2 w = w1[c4];
+                                a[2 * c4] = ffma2_b64(w.x, ffma2_b64(sa1, f2_pack(d1[4 * c4], d1[4 * c4 + 1]), cc1),
+                                                      a[2 * c4]);
+                                a[2 * c4 + 1] = ffma2_b64(
+                                    w.y, ffma2_b64(sa1, f2_pack(d1[4 * c4 + 2], d1[4 * c4 + 3]), cc1), a[2 * c4 + 1]);
+                            }
                         }
                     }
-                } else {
-                    const float cm = (-8.f * sv.y) * sv.x;
-                    const float2 sa2 = make_float2(sv.x, sv.x), cm2 = make_float2(cm, cm);
-                    const float4* swf = reinterpret_cast<const float4*>(gbase + OFF_SWF + s * (BN * 4) + c0 * 4);
-#pragma unroll
-                    for (int c4 = 0; c4 < 16; ++c4) {
-                        const float4 w = swf[c4];
-                        const float2 t0 = ffma2(sa2, make_float2(v[4 * c4], v[4 * c4 + 1]), cm2);
-                        const float2 t1 = ffma2(sa2, make_float2(v[4 * c4 + 2], v[4 * c4 + 3]), cm2);
-                        const float2 a0 = ffma2(make_float2(w.x, w.y), t0, make_float2(acc[4 * c4], acc[4 * c4 + 1]));
-                        const float2 a1 =
-                            ffma2(make_float2(w.z, w.w), t1, make_float2(acc[4 * c4 + 2], acc[4 * c4 + 3]));
-                        acc[4 * c4] = a0.x;
-                        acc[4 * c4 + 1] = a0.y;
-                        acc[4 * c4 + 2] = a1.x;
-                        acc[4 * c4 + 3] = a1.y;
-                    }
                 }
                 __syncwarp();
-                if (lane == 0) mbar_arrive(empty(s));
+                if (lane == 0) mbar_arrive(sempty(q));
                 ++it;
                 ++jc;
             }
@@ -356,7 +463,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             if constexpr (!DUMP) {
                 if (m < M) {
 #pragma unroll
-                    for (int ch = 0; ch < 8; ++ch) {
+                    for (int ch = 0; ch < EPI_COLS / 8; ++ch) {
                         const int n = n0 + c0 + ch * 8;
                         if (n < N) {
                             const uint4 csv = __ldg(reinterpret_cast<const uint4*>(colscale + n));
@@ -369,8 +476,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                             for (int j = 0; j < 4; ++j) {
                                 const float2 cs2 = __half22float2(*reinterpret_cast<const __half2*>(&cw[j]));
                                 const float2 b2 = __half22float2(*reinterpret_cast<const __half2*>(&bw[j]));
-                                const float y0 = fmaf(cs2.x, acc[ch * 8 + 2 * j], b2.x);
-                                const float y1 = fmaf(cs2.y, acc[ch * 8 + 2 * j + 1], b2.y);
+                                const float2 av = f2_unpack(acc[ch * 4 + j]);
+                                const float y0 = fmaf(cs2.x, av.x, b2.x);
+                                const float y1 = fmaf(cs2.y, av.y, b2.y);
                                 const __half2 h = __floats2half2_rn(y0, y1);
                                 out[j] = *reinterpret_cast<const uint32_t*>(&h);
                             }
@@ -390,25 +498,41 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (warp == WARP_MMA) tmem_dealloc(tmem, TMEM_COLS);
 }
 
-template <bool DUMP>
+// Registers per thread the kernel was compiled for (cached per instantiation).
+template <int S, bool DUMP>
+int launch_regs() {
+    static int regs = -1;
+    if (regs < 0) {
+        cudaFuncAttributes fa{};
+        if (cudaFuncGetAttributes(&fa, gemm_tc_kernel<S, DUMP>) != cudaSuccess) return 0;
+        regs = fa.numRegs;
+    }
+    return regs;
+}
+
+template <int S, bool DUMP>
 w4a4_status launch_impl(const uint8_t* ws, const uint8_t* packed, const uint16_t* cs, const uint16_t* bias, int M,
                         int N, int K, int r, uint16_t* Y, int32_t* P, cudaStream_t s) {
     static int attr_done[64] = {0};
     int dev = 0;
     cudaGetDevice(&dev);
+    const int rp = DUMP ? 0 : r / 16;
     if (dev >= 0 && dev < 64 && !attr_done[dev]) {
-        if (cudaFuncSetAttribute(gemm_tc_kernel<DUMP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 int(smem_bytes(8))) != cudaSuccess)
+        if (cudaFuncSetAttribute(gemm_tc_kernel<S, DUMP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 int(smem_map(S, S == 4 ? 2 : 8).total)) != cudaSuccess)
             return W4A4_ERR_CUDA;
         attr_done[dev] = 1;
     }
-    const int rp = DUMP ? 0 : r / 16;
+    // the setmaxnreg split needs the launch-time register pool to cover it
+    if (launch_regs<S, DUMP>() * NUM_THREADS <
+        NUM_EPI_WARPS * 32 * EPI_REGS + (NUM_THREADS - NUM_EPI_WARPS * 32) * OTHER_REGS)
+        return W4A4_ERR_CUDA;
     const int MT = (M + BM - 1) / BM, NT = (N + BN - 1) / BN;
     const int tiles = MT * NT;
     const int grid = tiles < device_sm_count() ? tiles : device_sm_count();
-    gemm_tc_kernel<DUMP><<<grid, NUM_THREADS, smem_bytes(rp), s>>>(ws, packed, cs, bias, M, N, K, r, Y, P);
-    set_dispatch("gemm_tc tcgen05.f8f6f4 tile=%dx%d stages=%d tiles=%d grid=%d%s", BM, BN, STAGES, tiles, grid,
-                 DUMP ? " (partials dump)" : "");
+    gemm_tc_kernel<S, DUMP><<<grid, NUM_THREADS, smem_map(S, rp).total, s>>>(ws, packed, cs, bias, M, N, K, r, Y, P);
+    set_dispatch("gemm_tc tcgen05.f8f6f4 tile=%dx%d groups/job=%d stages=%d tiles=%d grid=%d%s", BM, BN, GPJ, S,
+                 tiles, grid, DUMP ? " (partials dump)" : "");
     return launch_status();
 }
 
@@ -416,8 +540,9 @@ w4a4_status launch_impl(const uint8_t* ws, const uint8_t* packed, const uint16_t
 
 w4a4_status launch_gemm_tc(const uint8_t* ws, const uint8_t* packed, const uint16_t* colscale, const uint16_t* bias,
                            int M, int N, int K, int r, uint16_t* Y, int32_t* P_dump, cudaStream_t s) {
-    if (P_dump) return launch_impl<true>(ws, packed, colscale, bias, M, N, K, r, Y, P_dump, s);
-    return launch_impl<false>(ws, packed, colscale, bias, M, N, K, r, Y, nullptr, s);
+    if (P_dump) return launch_impl<4, true>(ws, packed, colscale, bias, M, N, K, r, Y, P_dump, s);
+    if (r > 32) return launch_impl<3, false>(ws, packed, colscale, bias, M, N, K, r, Y, nullptr, s);
+    return launch_impl<4, false>(ws, packed, colscale, bias, M, N, K, r, Y, nullptr, s);
 }
 
 w4a4_status tc_read_and_clear_status() {
