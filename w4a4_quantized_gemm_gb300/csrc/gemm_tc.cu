@@ -84,28 +84,41 @@ constexpr uint32_t kScale = GPJ * kScaleG;
 static_assert(kStage % 256 == 0 && ST_B % 256 == 0 && ST_W % 256 == 0 && kA % 256 == 0 && kB % 256 == 0,
               "operand planes need 256 B alignment");
 
+// Split-K reduction (a cluster of KS CTAs shares a tile): each 32-column
+// slice of the tile has an owner rank (slice % KS); the other ranks put their
+// fp32 sums for it into the owner's buffer, one 4 KB block per (sender, owned
+// slice, lane quarter), 16-byte chunks of the 32 lanes interleaved.
+constexpr int MAX_KS = 4;
+constexpr uint32_t kRedBlock = 32 * EPI_COLS * 4;
+constexpr uint32_t kRed = 64 * 1024;  // max over KS of (KS - 1) * ceil(4 / KS) * 4 blocks
+__host__ __device__ constexpr int owned_slices(int KS) { return (4 + KS - 1) / KS; }
+static_assert((2 - 1) * 2 * 4 * kRedBlock <= kRed && (3 - 1) * 2 * 4 * kRedBlock <= kRed &&
+                  (4 - 1) * 1 * 4 * kRedBlock <= kRed, "reduction buffer too small");
+
 struct Map {
-    uint32_t ST, SC, LA, LU, BAR, SLOT, total;
+    uint32_t ST, SC, LA, LU, RED, BAR, SLOT, total;
 };
-__host__ __device__ constexpr Map smem_map(int S, int rp) {
+__host__ __device__ constexpr Map smem_map(int S, int rp, bool split) {
     Map m{};
     m.ST = 0;
     m.SC = m.ST + uint32_t(S) * kStage;
     m.LA = m.SC + SS * kScale;
     m.LU = m.LA + uint32_t(rp) * BM * 32;
-    m.BAR = m.LU + uint32_t(rp) * BN * 32;
-    m.SLOT = m.BAR + (3 * S + 2 * SS + 2 * NPB + 3) * 8;
+    m.RED = m.LU + uint32_t(rp) * BN * 32;
+    m.BAR = m.RED + (split ? kRed : 0u);
+    m.SLOT = m.BAR + (3 * S + 2 * SS + 2 * NPB + 6) * 8;
     m.total = m.SLOT + 16 + 1024;  // + base alignment
     return m;
 }
-static_assert(smem_map(4, 2).total <= 227 * 1024, "4 stages must fit at rank 32");
-static_assert(smem_map(3, 8).total <= 227 * 1024, "3 stages must fit at rank 128");
+static_assert(smem_map(4, 2, false).total <= 227 * 1024, "4 stages must fit at rank 32");
+static_assert(smem_map(3, 8, false).total <= 227 * 1024, "3 stages must fit at rank 128");
+static_assert(smem_map(3, 2, true).total <= 227 * 1024, "3 stages + the reduction buffer must fit at rank 32");
 
-template <int S, bool DUMP>
+template <int S, bool DUMP, bool SPLIT>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_tc_kernel(const uint8_t* __restrict__ ws, const uint8_t* __restrict__ packed,
                    const uint16_t* __restrict__ colscale, const uint16_t* __restrict__ bias, int M, int N, int K,
-                   int r, uint16_t* __restrict__ Y, int32_t* __restrict__ P) {
+                   int r, uint16_t* __restrict__ Y, int32_t* __restrict__ P, int KS) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -114,12 +127,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int G = K / kGroup;
     const int J = (G + GPJ - 1) / GPJ;  // jobs per tile
-    const int RP = DUMP ? 0 : r / 16;
+    // split-K: the KS CTAs of a cluster share a tile, rank kr taking jobs [j0, j1);
+    // otherwise every CTA is its own "cluster" of one
+    const int kr = SPLIT ? int(cluster_ctarank()) : 0;
+    if (!SPLIT) KS = 1;
+    const int cid = int(blockIdx.x) / KS, ncl = int(gridDim.x) / KS;
+    const int j0 = kr * J / KS, j1 = (kr + 1) * J / KS;
+    const int RPB = DUMP ? 0 : r / 16;  // LoRA operand planes held in shared memory
+    const int RP = kr == 0 ? RPB : 0;   // the LoRA term is added by rank 0 only
     const ActLayout AL = act_layout(M, K, r);
     const PackedLayout PL = packed_layout(N, K, r);
     const int MT = AL.MT, NT = (N + BN - 1) / BN;
     const int tiles = MT * NT;
-    const Map mp = smem_map(S, RP);
+    const Map mp = smem_map(S, RPB, SPLIT);
 
     auto full = [&](int s) { return base + mp.BAR + 8u * s; };             // copies landed (producers + tx)
     auto bready = [&](int s) { return base + mp.BAR + 8u * (S + s); };     // B operand expanded
@@ -131,6 +151,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const uint32_t lfull = base + mp.BAR + 8u * (3 * S + 2 * SS + 2 * NPB);
     const uint32_t lempty = lfull + 8u;
     const uint32_t mmadone = lfull + 16u;
+    const uint32_t red_full = lfull + 24u;   // (owner) the senders' blocks for this tile have landed
+    const uint32_t red_empty = lfull + 32u;  // (sender) the owners have consumed this CTA's blocks
+    const uint32_t own_done = lfull + 40u;   // (owner) this CTA's owner warps have read the blocks
+    const int own = SPLIT ? (kr < 4 % KS ? 4 / KS + 1 : 4 / KS) : 4;  // slices owned by this rank
     volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(gbase + mp.SLOT);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + mp.SLOT + 4);
 
@@ -151,6 +175,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         mbar_init(lfull, 2);
         mbar_init(lempty, 1);
         mbar_init(mmadone, 1);
+        if (SPLIT) {
+            mbar_init(red_full, 1);                  // the owner's expect-tx; the senders complete bytes
+            mbar_init(red_empty, uint32_t(KS - 1));  // one arrive per owner CTA
+            mbar_init(own_done, uint32_t(own * 4));  // one arrive per owner warp
+        }
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -180,7 +209,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const int role = warp == WARP_PRODUCER ? 0 : warp == WARP_PRODUCER_W ? 1 : 2;
         uint32_t it = 0, lp = 0, lora_issued = 0;
         bool ok = true;
-        for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
+        for (int t = cid; t < tiles && ok; t += ncl) {
             const int mt = t % MT, n0 = (t / MT) * BN;
             const int rows = min(BN, N - n0);
             if (RP > 0 && role < 2) {
@@ -204,7 +233,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 lp ^= 1u;
                 lora_issued = 1;
             }
-            for (int jb = 0; jb < J; ++jb) {
+            for (int jb = j0; jb < j1; ++jb) {
                 const int g0 = jb * GPJ, ng = min(GPJ, G - g0);
                 const int s = int(it % S);
                 const uint32_t ph = (it / S) & 1u;
@@ -247,7 +276,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         constexpr uint32_t IDESC = idesc_m128(BN);
         uint32_t it = 0, jc = 0, lp = 0;
         bool ok = true;
-        for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
+        for (int t = cid; t < tiles && ok; t += ncl) {
             if (RP > 0) {
                 // the LoRA product takes a job buffer of its own (first 128 columns)
                 const uint32_t b = jc % NPB, tph = (jc / NPB) & 1u;
@@ -268,7 +297,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 ++jc;
                 lp ^= 1u;
             }
-            for (int jb = 0; jb < J; ++jb) {
+            for (int jb = j0; jb < j1; ++jb) {
                 const int ng = min(GPJ, G - jb * GPJ);
                 const int s = int(it % S);
                 const uint32_t ph = (it / S) & 1u;
@@ -309,8 +338,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         static_assert(EXP_ROWS == 32, "one expansion row per lane");
         uint32_t it = 0;
         bool ok = true;
-        for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
-            for (int jb = 0; jb < J; ++jb) {
+        for (int t = cid; t < tiles && ok; t += ncl) {
+            for (int jb = j0; jb < j1; ++jb) {
                 const int ng = min(GPJ, G - jb * GPJ);
                 const int s = int(it % S), q = int(it % SS);
                 const uint32_t ph = (it / S) & 1u, sph = (it / SS) & 1u;
@@ -361,9 +390,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const int c0 = (warp >> 2) * EPI_COLS;  // column slice of the tile
         const int row = lq * 32 + lane;
         const uint32_t tl = tmem + (uint32_t(lq * 32) << 16) + uint32_t(c0);
-        uint32_t it = 0, jc = 0;
+        uint32_t it = 0, jc = 0, tc = 0;
         bool ok = true;
-        for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
+        for (int t = cid; t < tiles && ok; t += ncl) {
             const int mt = t % MT, n0 = (t / MT) * BN;
             const int m = mt * BM + row;
             uint64_t acc[EPI_COLS / 2];  // running sums as packed column pairs
@@ -387,7 +416,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
                 for (int c = 0; c < EPI_COLS / 2; ++c) acc[c] = 0ull;
             }
-            for (int jb = 0; jb < J; ++jb) {
+            for (int jb = j0; jb < j1; ++jb) {
                 const int g0 = jb * GPJ;
                 const bool two = g0 + 1 < G;
                 const int q = int(it % SS);
@@ -460,6 +489,63 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 ++jc;
             }
             if (!ok) break;
+            if constexpr (SPLIT && !DUMP) {
+                const int sl = warp >> 2, owner = sl % KS;
+                if (owner != kr) {
+                    // send this slice's sums to its owner once it has consumed the previous ones
+                    if (!warp_wait_parity_cluster(red_empty, (tc & 1u) ^ 1u, abort_flag, WAIT_LIMIT_NS)) {
+                        ok = false;
+                        break;
+                    }
+                    const int src = kr < owner ? kr : kr - 1;
+                    const uint32_t blk = base + mp.RED +
+                                         uint32_t(((src * owned_slices(KS) + sl / KS) * 4 + lq)) * kRedBlock;
+                    const uint32_t rblk = mapa_shared(blk, uint32_t(owner));
+                    const uint32_t rbar = mapa_shared(red_full, uint32_t(owner));
+#pragma unroll
+                    for (int c4 = 0; c4 < EPI_COLS / 4; ++c4) {
+                        const float2 lo = f2_unpack(acc[2 * c4]), hi = f2_unpack(acc[2 * c4 + 1]);
+                        st_async_v4(rblk + uint32_t(c4 * 32 + lane) * 16u, make_float4(lo.x, lo.y, hi.x, hi.y), rbar);
+                    }
+                    ++tc;
+                    continue;  // the owner stores this slice
+                }
+                // owner: one thread posts the bytes this CTA receives for the tile
+                if (sl == kr && lq == 0 && lane == 0)
+                    mbar_expect_tx(red_full, uint32_t(own * 4 * (KS - 1)) * kRedBlock);
+                if (!warp_wait_parity(red_full, tc & 1u, abort_flag, WAIT_LIMIT_NS, BACKOFF_EPI)) {
+                    ok = false;
+                    break;
+                }
+                // add the other ranks' sums in rank order
+                for (int src_rank = 0; src_rank < KS; ++src_rank) {
+                    if (src_rank == kr) continue;
+                    const int src = src_rank < kr ? src_rank : src_rank - 1;
+                    const uint8_t* blk =
+                        gbase + mp.RED + uint32_t(((src * owned_slices(KS) + sl / KS) * 4 + lq)) * kRedBlock;
+#pragma unroll
+                    for (int c4 = 0; c4 < EPI_COLS / 4; ++c4) {
+                        const float4 v = *reinterpret_cast<const float4*>(blk + (c4 * 32 + lane) * 16);
+                        const float2 lo = f2_unpack(acc[2 * c4]), hi = f2_unpack(acc[2 * c4 + 1]);
+                        acc[2 * c4] = f2_pack(lo.x + v.x, lo.y + v.y);
+                        acc[2 * c4 + 1] = f2_pack(hi.x + v.z, hi.y + v.w);
+                    }
+                }
+                // once every owner warp of this CTA has read its blocks, one thread hands
+                // the buffer back to the senders
+                __syncwarp();
+                if (lane == 0) mbar_arrive(own_done);
+                if (sl == kr && lq == 0) {
+                    if (!warp_wait_parity(own_done, tc & 1u, abort_flag, WAIT_LIMIT_NS, BACKOFF_EPI)) {
+                        ok = false;
+                        break;
+                    }
+                    if (lane == 0)
+                        for (int src_rank = 0; src_rank < KS; ++src_rank)
+                            if (src_rank != kr) mbar_arrive_remote(mapa_shared(red_empty, uint32_t(src_rank)));
+                }
+            }
+            ++tc;
             if constexpr (!DUMP) {
                 if (m < M) {
 #pragma unroll
@@ -494,55 +580,145 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
     tc_fence_before();
     __syncthreads();
+    if (SPLIT) cluster_sync_all();  // peers may still be using this CTA's shared memory
     tc_fence_after();
     if (warp == WARP_MMA) tmem_dealloc(tmem, TMEM_COLS);
 }
 
 // Registers per thread the kernel was compiled for (cached per instantiation).
-template <int S, bool DUMP>
+template <int S, bool DUMP, bool SPLIT>
 int launch_regs() {
     static int regs = -1;
     if (regs < 0) {
         cudaFuncAttributes fa{};
-        if (cudaFuncGetAttributes(&fa, gemm_tc_kernel<S, DUMP>) != cudaSuccess) return 0;
+        if (cudaFuncGetAttributes(&fa, gemm_tc_kernel<S, DUMP, SPLIT>) != cudaSuccess) return 0;
         regs = fa.numRegs;
     }
     return regs;
 }
 
-template <int S, bool DUMP>
+template <int S, bool DUMP, bool SPLIT>
 w4a4_status launch_impl(const uint8_t* ws, const uint8_t* packed, const uint16_t* cs, const uint16_t* bias, int M,
-                        int N, int K, int r, uint16_t* Y, int32_t* P, cudaStream_t s) {
+                        int N, int K, int r, uint16_t* Y, int32_t* P, int KS, cudaStream_t s) {
+    auto kern = gemm_tc_kernel<S, DUMP, SPLIT>;
     static int attr_done[64] = {0};
     int dev = 0;
     cudaGetDevice(&dev);
     const int rp = DUMP ? 0 : r / 16;
+    const uint32_t smem_max = smem_map(S, S == 4 ? 2 : (SPLIT ? 2 : 8), SPLIT).total;
     if (dev >= 0 && dev < 64 && !attr_done[dev]) {
-        if (cudaFuncSetAttribute(gemm_tc_kernel<S, DUMP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 int(smem_map(S, S == 4 ? 2 : 8).total)) != cudaSuccess)
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem_max)) != cudaSuccess)
             return W4A4_ERR_CUDA;
         attr_done[dev] = 1;
     }
     // the setmaxnreg split needs the launch-time register pool to cover it
-    if (launch_regs<S, DUMP>() * NUM_THREADS <
+    if (launch_regs<S, DUMP, SPLIT>() * NUM_THREADS <
         NUM_EPI_WARPS * 32 * EPI_REGS + (NUM_THREADS - NUM_EPI_WARPS * 32) * OTHER_REGS)
         return W4A4_ERR_CUDA;
     const int MT = (M + BM - 1) / BM, NT = (N + BN - 1) / BN;
     const int tiles = MT * NT;
-    const int grid = tiles < device_sm_count() ? tiles : device_sm_count();
-    gemm_tc_kernel<S, DUMP><<<grid, NUM_THREADS, smem_map(S, rp).total, s>>>(ws, packed, cs, bias, M, N, K, r, Y, P);
-    set_dispatch("gemm_tc tcgen05.f8f6f4 tile=%dx%d groups/job=%d stages=%d tiles=%d grid=%d%s", BM, BN, GPJ, S,
-                 tiles, grid, DUMP ? " (partials dump)" : "");
+    const uint32_t smem = smem_map(S, rp, SPLIT).total;
+    if (!SPLIT) {
+        const int grid = tiles < device_sm_count() ? tiles : device_sm_count();
+        kern<<<grid, NUM_THREADS, smem, s>>>(ws, packed, cs, bias, M, N, K, r, Y, P, 1);
+        set_dispatch("gemm_tc tcgen05.f8f6f4 tile=%dx%d groups/job=%d stages=%d tiles=%d grid=%d%s", BM, BN, GPJ, S,
+                     tiles, grid, DUMP ? " (partials dump)" : "");
+        return launch_status();
+    }
+    // clusters of KS CTAs, as many as can be resident at once (persistent over tiles)
+    cudaLaunchConfig_t cfg{};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = unsigned(KS);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cfg.blockDim = dim3(NUM_THREADS);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cfg.gridDim = dim3(unsigned(tiles * KS));
+    int active = 0;
+    if (cudaOccupancyMaxActiveClusters(&active, kern, &cfg) != cudaSuccess || active < 1) {
+        cudaGetLastError();
+        return W4A4_ERR_CUDA;
+    }
+    const int clusters = tiles < active ? tiles : active;
+    cfg.gridDim = dim3(unsigned(clusters * KS));
+    if (cudaLaunchKernelEx(&cfg, kern, ws, packed, cs, bias, M, N, K, r, Y, P, KS) != cudaSuccess) {
+        cudaGetLastError();
+        return W4A4_ERR_CUDA;
+    }
+    set_dispatch("gemm_tc tcgen05.f8f6f4 tile=%dx%d groups/job=%d stages=%d split-K=%d (cluster) tiles=%d grid=%d%s",
+                 BM, BN, GPJ, S, KS, tiles, clusters * KS, DUMP ? " (partials dump)" : "");
     return launch_status();
 }
 
 }  // namespace
 
+// Clusters of `ks` split-K CTAs that can be resident at once (cached per device and ks).
+static int resident_clusters(int ks) {
+    static int cache[64][MAX_KS + 1] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= 64) return 0;
+    if (cache[dev][ks] == 0) {
+        auto kern = gemm_tc_kernel<3, false, true>;
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 int(smem_map(3, 2, true).total)) != cudaSuccess) {
+            cudaGetLastError();
+            return 0;
+        }
+        cudaLaunchConfig_t cfg{};
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = unsigned(ks);
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        cfg.blockDim = dim3(NUM_THREADS);
+        cfg.dynamicSmemBytes = smem_map(3, 2, true).total;
+        cfg.gridDim = dim3(unsigned(ks * 64));
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) {
+            cudaGetLastError();
+            n = -1;
+        }
+        cache[dev][ks] = n;
+    }
+    return cache[dev][ks];
+}
+
+// Split factor along K: the one that minimises (rounds of tiles) x (jobs per
+// CTA + the cross-CTA reduction, about 1.5 jobs) for the machine's resident
+// clusters; rank 128 LoRA operands leave no room for the reduction buffer.
+static int split_factor(int M, int N, int K, int r) {
+    const int tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
+    const int jobs = (K / kGroup + GPJ - 1) / GPJ;
+    if (r > 32 || tiles <= 0) return 1;
+    const int sms = device_sm_count();
+    double best = double((tiles + sms - 1) / sms) * jobs;
+    int best_ks = 1;
+    for (int ks = 2; ks <= MAX_KS && ks <= jobs; ++ks) {
+        const int cl = resident_clusters(ks);
+        if (cl < 1) continue;
+        const double cost = double((tiles + cl - 1) / cl) * (double((jobs + ks - 1) / ks) + 1.5);
+        if (cost < best) {
+            best = cost;
+            best_ks = ks;
+        }
+    }
+    return best_ks;
+}
+
 w4a4_status launch_gemm_tc(const uint8_t* ws, const uint8_t* packed, const uint16_t* colscale, const uint16_t* bias,
                            int M, int N, int K, int r, uint16_t* Y, int32_t* P_dump, cudaStream_t s) {
-    if (P_dump) return launch_impl<4, true>(ws, packed, colscale, bias, M, N, K, r, Y, P_dump, s);
-    if (r > 32) return launch_impl<3, false>(ws, packed, colscale, bias, M, N, K, r, Y, nullptr, s);
-    return launch_impl<4, false>(ws, packed, colscale, bias, M, N, K, r, Y, nullptr, s);
+    if (P_dump) return launch_impl<4, true, false>(ws, packed, colscale, bias, M, N, K, r, Y, P_dump, 1, s);
+    const int ks = split_factor(M, N, K, r);
+    if (ks > 1) return launch_impl<3, false, true>(ws, packed, colscale, bias, M, N, K, r, Y, nullptr, ks, s);
+    if (r > 32) return launch_impl<3, false, false>(ws, packed, colscale, bias, M, N, K, r, Y, nullptr, 1, s);
+    return launch_impl<4, false, false>(ws, packed, colscale, bias, M, N, K, r, Y, nullptr, 1, s);
 }
 
 w4a4_status tc_read_and_clear_status() {

@@ -77,6 +77,75 @@ __device__ __forceinline__ bool warp_wait_parity(uint32_t bar, uint32_t parity, 
     return __all_sync(0xffffffffu, ok);
 }
 
+// ---- thread-block clusters: distributed shared memory --------------------
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;\n" : "=r"(r));
+    return r;
+}
+// Address of the same shared-memory location in CTA `rank` of this cluster.
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t saddr, uint32_t rank) {
+    uint32_t d;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;\n" : "=r"(d) : "r"(saddr), "r"(rank));
+    return d;
+}
+__device__ __forceinline__ void st_cluster_v4(uint32_t addr, float4 v) {
+    asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};\n" ::"r"(addr), "f"(v.x), "f"(v.y), "f"(v.z),
+                 "f"(v.w)
+                 : "memory");
+}
+// Asynchronous 16-byte store into another CTA's shared memory that completes
+// 16 bytes of transaction count on an mbarrier of that CTA (both addresses
+// from mapa_shared); no fence is needed for the receiver to see the data once
+// it observes the barrier phase.
+__device__ __forceinline__ void st_async_v4(uint32_t remote_addr, float4 v, uint32_t remote_bar) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];\n" ::"r"(
+                     remote_addr),
+                 "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w), "r"(remote_bar)
+                 : "memory");
+}
+// Named barrier over `nthreads` threads (a multiple of 32) of this CTA.
+__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
+    asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(nthreads) : "memory");
+}
+// Arrive on an mbarrier of another CTA of the cluster, releasing this thread's
+// earlier (distributed) shared-memory writes to whoever acquires the phase.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t remote_bar) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];\n" ::"r"(remote_bar) : "memory");
+}
+// Cluster-scope acquire of a completed phase (pairs with mbar_arrive_remote).
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n.reg .pred p;\nmbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
+        "selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+__device__ __forceinline__ bool warp_wait_parity_cluster(uint32_t bar, uint32_t parity, volatile int* abort,
+                                                         uint64_t limit_ns) {
+    bool ok = mbar_try_wait_cluster(bar, parity);
+    if (!ok) {
+        const uint64_t t0 = globaltimer_ns();
+        for (uint32_t n = 1;; ++n) {
+            __nanosleep(64);
+            if (mbar_try_wait_cluster(bar, parity)) {
+                ok = true;
+                break;
+            }
+            if ((n & 15u) == 0 && (*abort || globaltimer_ns() - t0 > limit_ns)) break;
+        }
+    }
+    return __all_sync(0xffffffffu, ok);
+}
+// Every thread of every CTA of the cluster: no CTA leaves before the others are
+// done with its shared memory.
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;\n" ::: "memory");
+}
+
 __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
 }
