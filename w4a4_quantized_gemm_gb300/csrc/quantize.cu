@@ -4,8 +4,8 @@
 // Voice Clone", 3.6 fused_quantize_repack_act_kernel and its LoRA-down branch).
 //
 // GB300 design:
-//  * A thread-block cluster of CK CTAs owns 16 rows; each CTA takes a
-//    contiguous range of the K groups.  The fp32 LoRA partials of the CK CTAs
+//  * A thread-block cluster of CK CTAs (8 warps each) owns 16 rows; each CTA
+//    takes a contiguous range of the K groups, about two per warp.  The fp32 LoRA partials of the CK CTAs
 //    are summed through distributed shared memory in a fixed order: no
 //    atomics, deterministic results, and no separate repack kernel (the
 //    page's pack_lora_act exists only to wait for its atomics).
@@ -15,6 +15,8 @@
 //    gives the same code as the IEEE quotient except when the product lies
 //    within 2^-18 of a rounding boundary (k + 1/2); those rare elements are
 //    recomputed with the IEEE division, so codes equal rint(fl(x / scale)).
+//    The check is branch-free per element; the warp takes the slow path only
+//    when one of its lanes flagged such an element.
 #include <cooperative_groups.h>
 
 #include "kernels.h"
@@ -25,9 +27,12 @@ namespace w4a4 {
 namespace {
 
 constexpr int kRows = 16;      // rows per cluster (one m16 tile of the LoRA MMA)
-constexpr int kWarps = 4;
+constexpr int kWarps = 8;
 constexpr int kXsStride = 72;  // halves per staged row (64 + 8 pad: conflict-free ldmatrix)
 constexpr int kMaxCluster = 8;
+__host__ __device__ constexpr int q_smem_bytes(int R) {
+    return kWarps * kRows * kXsStride * 2 + (R > 0 ? kWarps * kRows * R * 4 : 0);
+}
 
 __device__ __forceinline__ void ldmatrix_x4(uint32_t (&r)[4], const void* p) {
     asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
@@ -42,22 +47,13 @@ __device__ __forceinline__ uint32_t cvt_e4m3x2(float lo, float hi) {
     return r;
 }
 
-// rint(fl(x / s)) from the reciprocal product (see the file comment): y is within
-// 2^-20 of x/s and fl(x/s) within 2^-21, so away from k + 1/2 both round alike.
-__device__ __forceinline__ float code_of(float x, float s, float inv) {
-    const float y = x * inv;
-    const float q = rintf(y);
-    const float d = fabsf(y - q);  // distance to the nearest integer, in [0, 0.5]
-    if (d >= 0.5f - 3.814697265625e-06f) return rintf(__fdiv_rn(x, s));  // within 2^-18 of k + 1/2
-    return q;
-}
-
 template <int R>  // LoRA rank, multiple of 16 (0 = no LoRA branch)
 __global__ void __launch_bounds__(kWarps * 32) quantize_act_kernel(const uint16_t* __restrict__ X,
                                                                    const uint2* __restrict__ Ldp, int M,
                                                                    int K, uint8_t* __restrict__ ws) {
-    __shared__ __align__(16) uint16_t xs[kWarps][kRows * kXsStride];
-    __shared__ __align__(16) float red[R > 0 ? kWarps * kRows * R : 1];
+    extern __shared__ __align__(16) uint8_t qsm[];
+    uint16_t(*xs)[kRows * kXsStride] = reinterpret_cast<uint16_t(*)[kRows * kXsStride]>(qsm);
+    float* red = reinterpret_cast<float*>(qsm + kWarps * kRows * kXsStride * 2);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int G = K / kGroup;
@@ -89,6 +85,18 @@ __global__ void __launch_bounds__(kWarps * 32) quantize_act_kernel(const uint16_
         xv[i] = (valid && g < g_end) ? ldg_nc_v4(xrow + (size_t)g * kGroup + 8 * i) : make_uint4(0, 0, 0, 0);
     for (; g < g_end; g += kWarps) {
         // prefetch the warp's next group while this one is processed
+        // this group's LoRA-down fragments, in flight while the group is quantised
+        // (up to rank 48; larger ranks load them where they are used)
+        constexpr bool kPrefetchB = R > 0 && R <= 48;
+        constexpr int NTB = kPrefetchB ? NT : 1;
+        uint2 b[4][NTB];
+        if constexpr (kPrefetchB) {
+            const uint2* bp = Ldp + ((size_t)(g * 4) * NT) * 32 + lane;
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks)
+#pragma unroll
+                for (int t = 0; t < NT; ++t) b[ks][t] = __ldg(bp + (ks * NT + t) * 32);
+        }
         uint4 nv[4];
         const int gn = g + kWarps;
 #pragma unroll
@@ -114,14 +122,36 @@ __global__ void __launch_bounds__(kWarps * 32) quantize_act_kernel(const uint16_
         // rounds to at most 7 and the clamp to [-8, 7] never acts.
         const float s = fmaxf(__fdiv_rn(amax, 7.0f), 1e-10f);
         const float inv = __frcp_rn(s);
+        // codes on the reciprocal path, branch-free; elements within 2^-18 of a
+        // rounding boundary are flagged and redone with the IEEE quotient below
+        // (x[] is overwritten by the codes; the fp16 inputs stay in xv)
+        float* c = x;
+        bool near_tie = false;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            const float y = x[i] * inv;
+            c[i] = rintf(y);
+            near_tie |= fabsf(y - c[i]) >= 0.5f - 3.814697265625e-06f;
+        }
+        // (rare) rint(fl(x / s)) with the IEEE quotient where the reciprocal product
+        // lies within 2^-18 of k + 1/2: y is within 2^-20 of x/s and fl(x/s) within
+        // 2^-21, so everywhere else both round alike
+        if (__any_sync(0xffffffffu, near_tie)) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                const uint32_t wv = (&xv[i >> 3].x)[(i & 7) >> 1];
+                const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&wv));
+                const float xi = (i & 1) ? f.y : f.x;
+                const float y = xi * inv;
+                if (fabsf(y - c[i]) >= 0.5f - 3.814697265625e-06f) c[i] = rintf(__fdiv_rn(xi, s));
+            }
+        }
         float csum = 0.f;
         uint32_t packed[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-            const float c0 = code_of(x[4 * i], s, inv), c1 = code_of(x[4 * i + 1], s, inv);
-            const float c2 = code_of(x[4 * i + 2], s, inv), c3 = code_of(x[4 * i + 3], s, inv);
-            csum += (c0 + c1) + (c2 + c3);
-            packed[i] = cvt_e4m3x2(c0, c1) | (cvt_e4m3x2(c2, c3) << 16);
+            csum += (c[4 * i] + c[4 * i + 1]) + (c[4 * i + 2] + c[4 * i + 3]);
+            packed[i] = cvt_e4m3x2(c[4 * i], c[4 * i + 1]) | (cvt_e4m3x2(c[4 * i + 2], c[4 * i + 3]) << 16);
         }
         csum += __shfl_xor_sync(0xffffffffu, csum, 1);
         uint8_t* plane = ws + AL.qA + ((size_t)(mt * G + g) * 2 + qhalf) * (kTileM * 32);
@@ -138,19 +168,22 @@ __global__ void __launch_bounds__(kWarps * 32) quantize_act_kernel(const uint16_
             for (int i = 0; i < 4; ++i)
                 *reinterpret_cast<uint4*>(xw + qrow * kXsStride + qhalf * 32 + 8 * i) = xv[i];
             __syncwarp();
-            const uint2* bp = Ldp + ((size_t)(g * 4) * NT) * 32 + lane;
-            uint2 b[4][NT];
-#pragma unroll
-            for (int ks = 0; ks < 4; ++ks)
-#pragma unroll
-                for (int t = 0; t < NT; ++t) b[ks][t] = __ldg(bp + (ks * NT + t) * 32);
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks) {
+                uint2 bl[NT];
+                if constexpr (!kPrefetchB) {
+                    const uint2* bp = Ldp + ((size_t)(g * 4) * NT) * 32 + lane;
+#pragma unroll
+                    for (int t = 0; t < NT; ++t) bl[t] = __ldg(bp + (ks * NT + t) * 32);
+                }
                 uint32_t a[4];
                 const int lr = (lane & 7) + ((lane >> 3) & 1) * 8, lc = ((lane >> 4) & 1) * 8 + ks * 16;
                 ldmatrix_x4(a, xw + lr * kXsStride + lc);
 #pragma unroll
-                for (int t = 0; t < NT; ++t) mma_f16_16816(acc[t], a, b[ks][t].x, b[ks][t].y);
+                for (int t = 0; t < NT; ++t) {
+                    const uint2 bb = kPrefetchB ? b[ks][t % NTB] : bl[t];
+                    mma_f16_16816(acc[t], a, bb.x, bb.y);
+                }
             }
             __syncwarp();
         }
@@ -221,12 +254,25 @@ __global__ void unpack_act_kernel(const uint8_t* __restrict__ ws, int M, int K, 
 template <int R>
 w4a4_status launch_q(const uint16_t* X, const uint8_t* packed, int M, int K, uint8_t* ws, cudaStream_t s) {
     const int G = K / kGroup;
-    const int CK = G < kMaxCluster ? G : kMaxCluster;
+    // split K over a (small) cluster so that each warp quantises about two groups
+    int CK = (G + 2 * kWarps - 1) / (2 * kWarps);
+    if (CK > kMaxCluster) CK = kMaxCluster;
+    if (CK < 1) CK = 1;
     const int row_blocks = (M + kRows - 1) / kRows;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(unsigned(row_blocks * CK));
     cfg.blockDim = dim3(kWarps * 32);
-    cfg.dynamicSmemBytes = 0;
+    static int attr_done[64] = {0};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    constexpr int smem = q_smem_bytes(R);
+    if (dev >= 0 && dev < 64 && !attr_done[dev]) {
+        if (cudaFuncSetAttribute(quantize_act_kernel<R>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+            cudaSuccess)
+            return W4A4_ERR_CUDA;
+        attr_done[dev] = 1;
+    }
+    cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
