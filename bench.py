@@ -13,6 +13,8 @@ timed inputs out of L2, the step cycles through R replicas of the layer
 
 Prints one JSON line (metric: effective TOPS = (2MNK + 2Mr(K+N)) / time).
   --impl reference : the CPU oracle timed on the host cores (bounded sample).
+  --workload stack : instead, the 28-layer stack of those four linears with
+                     RMSNorm glue (112 linears, one CUDA graph per forward pass).
 """
 from __future__ import annotations
 
@@ -35,6 +37,8 @@ from w4a4_quantized_gemm_gb300 import metrics  # noqa: E402
 METRIC = "W4A4+LoRA linear effective TOPS (decoder-layer linears, M=700)"
 UNIT = "TOPS"
 WORKLOAD = "qwen3_1024_decoder_layer_linears_M700"
+STACK_METRIC = "W4A4+LoRA linear effective TOPS (28-layer stack, M=700, RMSNorm glue, CUDA graph)"
+STACK_WORKLOAD = "qwen3_1024_28_layer_stack_M700"
 L2_BYTES = 129 * 2 ** 20
 
 
@@ -374,6 +378,180 @@ def run_ours(args, rank, world, local_rank):
     return 0
 
 
+# ------------------------------------------------------------ config 5: stack
+def stack_ops(M: int = 700) -> int:
+    from synthetic import STACK_LAYERS, STACK_LINEARS
+    return STACK_LAYERS * sum(metrics.linear_ops(M, N, K, 32) for _, K, N in STACK_LINEARS)
+
+
+def stack_config(extra=None):
+    from synthetic import STACK_LAYERS, STACK_LINEARS
+    cfg = {"workload": STACK_WORKLOAD, "M": 700, "group": 64, "rank": 32, "layers": STACK_LAYERS,
+           "linears_per_layer": {n: [k, nn] for n, k, nn in STACK_LINEARS},
+           "glue": "fp32/fp64 RMSNorm (unit gain, eps 1e-6) of the columns the next linear reads"}
+    if extra:
+        cfg.update(extra)
+    return cfg
+
+
+def time_stack_oracle(budget_s: float, max_rows: int = 8):
+    """The oracle's chain through all 112 linears for a few rows, until the budget."""
+    import oracle
+    from synthetic import STACK_LAYERS, STACK_LINEARS, make_stack_input, make_stack_linear
+    oracle.build()
+    X = make_stack_input(700)[:max_rows]
+    rows, ops, t0 = 0, 0, time.perf_counter()
+    nl = len(STACK_LINEARS)
+    for n in (1, 1, 2, 4):
+        if rows >= max_rows or time.perf_counter() - t0 >= budget_s:
+            break
+        x = X[rows:rows + n]
+        for i in range(STACK_LAYERS * nl):
+            c = make_stack_linear(i // nl, i % nl)
+            y = oracle.linear(x, c.W, c.L_down, c.L_up, c.colscale, c.bias)
+            x = oracle.rmsnorm_f16(oracle.f64_to_f16_array(y), STACK_LINEARS[(i + 1) % nl][1])
+            ops += metrics.linear_ops(n, c.N, c.K, c.r)
+        rows += n
+    return ops, time.perf_counter() - t0, rows
+
+
+def run_stack_reference(args, rank, world):
+    if rank != 0:
+        return 0
+    steps = []
+    for i in range(args.warmup + args.steps):
+        ops, sec, rows = time_stack_oracle(1e9, max_rows=1)
+        if i >= args.warmup:
+            steps.append((ops, sec))
+    ops = sum(o for o, _ in steps)
+    sec = sum(t for _, t in steps)
+    value = ops / sec / 1e12
+    sample = "1 of 700 rows through all 112 linears and their RMSNorm glue per step"
+    print(json.dumps({
+        "impl": "reference", "metric": STACK_METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * sec / len(steps),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int64/f64",
+        "data": "synthetic", "config": stack_config({"sample": sample}),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}), flush=True)
+    return 0
+
+
+def run_stack(args, rank, world, local_rank):
+    import torch
+    import torch.distributed as dist
+
+    torch.cuda.set_device(local_rank)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    from w4a4_quantized_gemm_gb300 import build as wbuild
+    wbuild.build()
+    import w4a4_quantized_gemm_gb300 as w4
+    from synthetic import STACK_LAYERS, STACK_LINEARS, make_stack_input, make_stack_linear
+    from w4a4_quantized_gemm_gb300.stack import W4A4Stack
+
+    dev = torch.device("cuda", local_rank)
+    nl = len(STACK_LINEARS)
+    stack = W4A4Stack((make_stack_linear(l, j) for l in range(STACK_LAYERS) for j in range(nl)), 700, dev)
+    X0h = torch.from_numpy(make_stack_input(700).view(np.float16).copy())
+    stack.X0.copy_(X0h.to(dev))
+    weight_bytes = sum(L["packed"].numel() for L in stack.layers)
+    fwd = stack.capture()
+
+    def gemm_only(st):
+        for i, L in enumerate(stack.layers):
+            w4.w4a4_linear(L["ws"], L["packed"], L["cs"], L["b"], L["Y"], L["K"], L["r"], w4.KERNEL_AUTO, st)
+
+    stack.forward()
+    torch.cuda.synchronize()
+    g_gemm = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_gemm):
+        gemm_only(torch.cuda.current_stream())
+    torch.cuda.synchronize()
+
+    def timed(graph, steps):
+        for _ in range(args.warmup):
+            graph.replay()
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(steps):
+            graph.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1)
+
+    sampler = ClockSampler(local_rank) if rank == 0 else None
+    if sampler:
+        sampler.__enter__()
+        time.sleep(0.3)
+    ms = timed(fwd, args.steps)
+    if sampler:
+        sampler.__exit__()
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    ms_per_step = ms / args.steps
+    ops = stack_ops()
+    value = world * ops / (ms_per_step * 1e-3) / 1e12
+    gemm_s = timed(g_gemm, args.steps) / args.steps * 1e-3
+    peaks = {}
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            peaks = json.load(f)
+    except (OSError, ValueError):
+        pass
+    bf16, peak_src = (float(peaks["bf16_tflops"]), "measured") if "bf16_tflops" in peaks else (1900.0, "fallback")
+    achieved = ops / gemm_s / 1e12
+    roofline = {"bound": "tensor", "achieved": achieved, "peak": 2.0 * bf16, "unit": "TFLOP/s",
+                "frac": achieved / (2.0 * bf16), "traffic": None,
+                "kernel": "w4a4_linear (GEMM + LoRA up + affine), 112 launches per forward",
+                "peak_source": f"{peak_src} bf16 burst x 2 (fp8 kind)",
+                "gemm_us_per_step": gemm_s * 1e6, "forward_us": ms_per_step * 1e3,
+                "packed_weight_bytes": weight_bytes}
+
+    e2e = None
+    if not args.no_e2e:
+        Xh = X0h.pin_memory()
+        Oh = torch.empty_like(stack.out, device="cpu").pin_memory()
+        g_e2e = torch.cuda.CUDAGraph()
+        stack.forward()
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g_e2e):
+            stack.X0.copy_(Xh, non_blocking=True)
+            stack.forward(torch.cuda.current_stream())
+            Oh.copy_(stack.out, non_blocking=True)
+        torch.cuda.synchronize()
+        e_ms = timed(g_e2e, args.steps) / args.steps
+        e2e = {"value": world * ops / (e_ms * 1e-3) / 1e12, "unit": UNIT, "ms_per_step": e_ms,
+               "h2d_bytes_per_step": Xh.numel() * 2, "d2h_bytes_per_step": Oh.numel() * 2,
+               "how": "one CUDA graph: H2D of the stack input from pinned host, the 336 C-ABI launches, D2H of the output"}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        c_ops, c_sec, c_rows = time_stack_oracle(args.cpu_budget)
+        cpu = {"value": c_ops / c_sec / 1e12, "unit": UNIT, "cores": 1, "kind": "oracle",
+               "sample": f"{c_rows} of 700 rows through all 112 linears and their glue ({c_sec:.1f} s)"}
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    if rank != 0:
+        return 0
+    print(json.dumps({
+        "metric": STACK_METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "int4 codes (fp8 e4m3 operands), fp32 accumulate, fp16 out",
+        "data": "synthetic",
+        "config": stack_config({"l2": f"packed weights {weight_bytes / 2**20:.0f} MiB > L2, streamed every pass"}),
+        "gpu_launches": args.steps * stack.launches_per_forward(),
+        "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+        "clocks": sampler.summary() if sampler else None}), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -385,12 +563,17 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", choices=["layer", "stack"], default="layer")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
     rank = _env_int("RANK", 0)
     world = _env_int("WORLD_SIZE", 1)
     local_rank = _env_int("LOCAL_RANK", 0)
+    if args.workload == "stack":
+        if args.impl == "reference":
+            return run_stack_reference(args, rank, world)
+        return run_stack(args, rank, world, local_rank)
     if args.impl == "reference":
         return run_reference(args, rank, world)
     return run_ours(args, rank, world, local_rank)

@@ -157,6 +157,20 @@ w4a4_status w4a4_linear_noalloc(const uint16_t* X, const void* packed, size_t pa
                                 const uint16_t* colscale, const uint16_t* bias, int M, int N, int K, int r,
                                 uint16_t* Y, cudaStream_t stream);
 
+/* RMSNorm glue of a stack of linears (unit gain), "W4A4 CUDA Kernel for Voice
+ * Clone", 3.9 (RMSNorm between the linears of a decoder layer; the page gives no
+ * epsilon, W4A4_RMSNORM_EPS is the Qwen3 value).  For each row m < M of Y
+ * (fp16, row stride ld_y elements) it reads the first K columns and writes
+ *   X[m, k] = fp16( Y[m, k] / sqrt( sum_k Y[m, k]^2 / K + eps ) )
+ * into X (fp16 [M, K], row-major).  Squares are exact in fp32 and summed in
+ * fp64; 1/sqrt(mean + eps) is taken in fp64 and each product y * inv is rounded
+ * once, fp64 -> fp16, to nearest even, so the result is the same bits as any
+ * implementation of this arithmetic up to the order of the fp64 additions.
+ * K % 8 == 0, K >= 8, ld_y >= K, ld_y % 8 == 0, 16-byte aligned pointers;
+ * Y and X must not overlap.  M == 0 is a no-op. */
+#define W4A4_RMSNORM_EPS 1e-6
+w4a4_status w4a4_rmsnorm_f16(const uint16_t* Y, int M, int ld_y, int K, uint16_t* X, cudaStream_t stream);
+
 /* ---- debug / validation entry points (small shapes; they synchronise `stream`)
  * Unpack the packed weights: codes int8 [N, K], scales fp16 [N, K/64],
  * L_down fp16 [K, r], L_up fp16 [r, N] (the last two may be NULL). */

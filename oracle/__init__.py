@@ -57,6 +57,10 @@ def _load():
         lib.oracle_f16_to_f32.restype = ctypes.c_float
         lib.oracle_f32_to_f16.argtypes = [ctypes.c_float]
         lib.oracle_f32_to_f16.restype = ctypes.c_uint16
+        lib.oracle_f64_to_f16.argtypes = [ctypes.c_double]
+        lib.oracle_f64_to_f16.restype = ctypes.c_uint16
+        lib.oracle_rmsnorm_f16.argtypes = [P, I, I, I, ctypes.c_double, P]
+        lib.oracle_f64_to_f16_array.argtypes = [P, I, P]
         lib.oracle_quantize_act.argtypes = [P, I, I, P, P]
         lib.oracle_quantize_weights.argtypes = [P, I, I, P, P]
         lib.oracle_group_partials.argtypes = [P, P, I, I, I, P]
@@ -195,3 +199,30 @@ def linear_sampled(X, W, L_down, L_up, colscale, bias, rows, cols) -> np.ndarray
     res = np.empty_like(out)
     res[order] = out
     return res
+
+
+RMSNORM_EPS = 1e-6
+
+
+def f64_to_f16(x: float) -> int:
+    """Nearest binary16 (ties to even) of a double, in one rounding; returns the bits."""
+    return int(_load().oracle_f64_to_f16(float(x)))
+
+
+def f64_to_f16_array(a: np.ndarray) -> np.ndarray:
+    """Elementwise nearest binary16 (ties to even) of doubles -> uint16 bits, same shape."""
+    a = _c(a, np.float64)
+    out = np.empty(a.shape, np.uint16)
+    _load().oracle_f64_to_f16_array(_ptr(a), a.size, _ptr(out))
+    return out
+
+
+def rmsnorm_f16(Y: np.ndarray, K: int, eps: float = RMSNORM_EPS) -> np.ndarray:
+    """RMSNorm with unit gain of the first K columns of each row of Y (fp16 bits,
+    uint16 [M, ld]) -> fp16 bits uint16 [M, K] ("W4A4 CUDA Kernel for Voice
+    Clone", 3.9): x = fp16(y / sqrt(mean(y^2) + eps)), sum in double."""
+    Y = _c(Y, np.uint16)
+    M, ld = Y.shape
+    X = np.empty((M, K), dtype=np.uint16)
+    _load().oracle_rmsnorm_f16(_ptr(Y), M, ld, K, float(eps), _ptr(X))
+    return X

@@ -71,6 +71,51 @@ uint16_t oracle_f32_to_f16(float f) {
     return (uint16_t)(sign | bits);
 }
 
+/* double value -> nearest binary16, ties to even, in one rounding (no detour
+ * through binary32, which could round twice). */
+uint16_t oracle_f64_to_f16(double d) {
+    if (isnan(d)) return (uint16_t)0x7e00u;
+    uint16_t sign = signbit(d) ? 0x8000u : 0u;
+    double v = fabs(d);
+    if (v >= 65520.0) return (uint16_t)(sign | 0x7c00u);      /* past 65504 + half a step */
+    int e2;
+    frexp(v, &e2);
+    int be = e2 - 1;
+    if (v == 0.0 || be < -14) be = -14;
+    double quantum = ldexp(1.0, be - 10);
+    double n = rint(v / quantum);         /* v / quantum is exact (power-of-two scaling) */
+    uint32_t bits;
+    if (be == -14 && n < 1024.0) {
+        bits = (uint32_t)n;
+    } else {
+        if (n == 2048.0) { be += 1; n = 1024.0; }
+        bits = ((uint32_t)(be + 15) << 10) | ((uint32_t)n - 1024u);
+    }
+    return (uint16_t)(sign | bits);
+}
+
+void oracle_f64_to_f16_array(const double* d, int64_t n, uint16_t* out) {
+    for (int64_t i = 0; i < n; ++i) out[i] = oracle_f64_to_f16(d[i]);
+}
+
+/* ---- RMSNorm glue of a stack of linears (Voice Clone post, 3.9), unit gain.
+ * For each row m of Y (fp16 bits, row stride ld) over its first K columns:
+ *   X[m, k] = fp16( Y[m, k] / sqrt( (sum_k Y[m, k]^2) / K + eps ) ),
+ * the sum of squares in double (each square of a binary16 value is exact),
+ * 1/sqrt(.) in double, one rounding to binary16 at the end.                  */
+void oracle_rmsnorm_f16(const uint16_t* Y, int64_t M, int64_t ld, int64_t K, double eps, uint16_t* X) {
+    for (int64_t m = 0; m < M; ++m) {
+        const uint16_t* y = Y + m * ld;
+        double ss = 0.0;
+        for (int64_t k = 0; k < K; ++k) {
+            double v = (double)oracle_f16_to_f32(y[k]);
+            ss += v * v;
+        }
+        double inv = 1.0 / sqrt(ss / (double)K + eps);
+        for (int64_t k = 0; k < K; ++k) X[m * K + k] = oracle_f64_to_f16((double)oracle_f16_to_f32(y[k]) * inv);
+    }
+}
+
 static int8_t clamp_code(float q) {
     if (q < -8.0f) q = -8.0f;
     if (q > 7.0f) q = 7.0f;

@@ -95,3 +95,49 @@ def random_codes(rng: np.random.Generator, shape, lo=-8, hi=7) -> np.ndarray:
 
 def random_f16(rng: np.random.Generator, shape, lo: float, hi: float) -> np.ndarray:
     return _f16_bits(rng.uniform(lo, hi, size=shape).astype(np.float32))
+
+
+# ---- config 5: a stack of decoder layers -------------------------------------
+# Each layer has the four linears below, in this order; every linear of every
+# layer gets fresh weights from ``default_rng([0, layer, j])`` (j = position in
+# the layer), drawn in the order W, L_down, L_up, colscale, bias.  The stack's
+# input is ``make_activations`` of ``default_rng(seed)`` at K = 1024.
+STACK_LAYERS = 28
+STACK_LINEARS = (("qkv", 1024, 4096), ("o", 2048, 1024), ("gate_up", 1024, 6144), ("down", 3072, 1024))
+
+
+@dataclass
+class StackLinear:
+    layer: int
+    j: int
+    name: str
+    K: int
+    N: int
+    r: int
+    W: np.ndarray         # float32 [N, K]
+    L_down: np.ndarray    # uint16 [K, r]
+    L_up: np.ndarray      # uint16 [r, N]
+    colscale: np.ndarray  # uint16 [N]
+    bias: np.ndarray      # uint16 [N]
+
+
+def make_stack_linear(layer: int, j: int, r: int = 32) -> StackLinear:
+    name, K, N = STACK_LINEARS[j]
+    rng = np.random.default_rng([0, layer, j])
+    W = (rng.standard_normal((N, K), dtype=np.float32) * np.float32(0.02)).astype(np.float32)
+    L_down = _f16_bits(rng.standard_normal((K, r), dtype=np.float32) * np.float32(0.02))
+    L_up = _f16_bits(rng.standard_normal((r, N), dtype=np.float32) * np.float32(0.02))
+    colscale = _f16_bits(rng.uniform(0.5, 1.5, size=N).astype(np.float32))
+    bias = _f16_bits(rng.standard_normal(N, dtype=np.float32) * np.float32(0.1))
+    return StackLinear(layer, j, name, K, N, r, np.ascontiguousarray(W), L_down, L_up, colscale, bias)
+
+
+def make_stack_input(M: int, seed: int = 0) -> np.ndarray:
+    """The stack's first input, fp16 bits uint16 [M, 1024]."""
+    X, _ = make_activations(np.random.default_rng(seed), M, STACK_LINEARS[0][1])
+    return X
+
+
+def stack_next_k(j: int) -> int:
+    """Columns of linear j's output that feed the next linear (wrapping to the next layer)."""
+    return STACK_LINEARS[(j + 1) % len(STACK_LINEARS)][1]

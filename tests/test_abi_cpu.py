@@ -80,6 +80,11 @@ def test_argument_checks_precede_any_launch(L):
     assert L.w4a4_pack_weights(None, A, A, 64, 128, 32, A, big, None) == 1
     assert L.w4a4_pack_weights(A, None, A, 64, 128, 32, A, big, None) == 1  # r > 0 needs LoRA factors
     assert L.w4a4_linear_select(A, big, A, big, A, None, 64, 1024, 1024, 32, A, 7, None) == 1
+    assert L.w4a4_rmsnorm_f16(A, 64, 1024, 1004, A, None) == 2    # K % 8 != 0
+    assert L.w4a4_rmsnorm_f16(A, 64, 1000, 1024, A, None) == 1    # ld_y < K
+    assert L.w4a4_rmsnorm_f16(A, 64, 1028, 1024, A, None) == 2    # ld_y % 8 != 0
+    assert L.w4a4_rmsnorm_f16(_vp(0x10002), 64, 1024, 1024, A, None) == 3
+    assert L.w4a4_rmsnorm_f16(A, 0, 1024, 1024, A, None) == 0     # M == 0: no-op
 
 
 @pytest.mark.skipif(torch.cuda.is_available(), reason="valid shapes would launch on a GPU box")

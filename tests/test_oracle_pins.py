@@ -249,3 +249,55 @@ def test_linear_sampled_matches_full():
     cols = rng.integers(0, 36, 50)
     s = oracle.linear_sampled(c.X, c.W, c.L_down, c.L_up, c.colscale, c.bias, rows, cols)
     assert np.array_equal(s, full[rows, cols])
+
+
+# ---------------------------------------------------------------- stack glue
+def test_f64_to_f16_matches_numpy_single_rounding():
+    """The double -> binary16 encoder rounds once, to nearest even: numpy's
+    float64 -> float16 cast does the same, over normals, subnormals, exact
+    midpoints between binary16 neighbours and the overflow boundary."""
+    rng = np.random.default_rng(5)
+    vals = [rng.standard_normal(20000) * 10.0 ** rng.uniform(-9, 5, 20000)]
+    h = np.arange(0, 0x7c00, 7, dtype=np.uint16).view(np.float16).astype(np.float64)
+    nxt = np.nextafter(h.astype(np.float16), np.float16(np.inf)).astype(np.float64)
+    mid = (h + nxt) / 2.0                            # exact midpoints: ties
+    vals += [h, mid, -mid, np.nextafter(mid, 0.0), np.nextafter(mid, np.inf),
+             np.array([65504.0, 65519.99, 65520.0, 1e-8, 2.0 ** -25, 3 * 2.0 ** -26, 0.0, -0.0])]
+    v = np.concatenate(vals)
+    got = oracle.f64_to_f16_array(v)
+    want = v.astype(np.float16).view(np.uint16)
+    assert np.array_equal(got, want)
+
+
+def _h(x):
+    return np.asarray(x, np.float32).astype(np.float16).view(np.uint16)
+
+
+def test_rmsnorm_closed_forms():
+    """Constant rows normalise to exactly 1 (or -1): c / sqrt(c^2 + 1e-6) is within
+    2^-20 of 1 for |c| >= 1/8; a zero row stays zero; columns past K are ignored."""
+    Y = np.zeros((4, 24), np.uint16)
+    Y[0, :16] = _h(2.0)
+    Y[1, :16] = _h(-0.125)
+    Y[3, :16] = _h(3.0)
+    Y[:, 16:] = _h(60000.0)                          # outside the K = 16 columns
+    X = oracle.rmsnorm_f16(Y, 16)
+    assert X.shape == (4, 16)
+    assert np.all(X[0] == _h(1.0)) and np.all(X[1] == _h(-1.0)) and np.all(X[3] == _h(1.0))
+    assert np.all(X[2] == 0)
+
+
+def test_rmsnorm_invariants():
+    """Odd in y (sign flip flips the output); scaling a row by a power of two
+    (exact in fp16) changes only eps's share, so outputs move by at most one
+    fp16 ulp, and rarely; output rows have mean square 1 up to the fp16 rounding."""
+    rng = np.random.default_rng(6)
+    y = rng.standard_normal((9, 256)).astype(np.float32)
+    Y = _h(y)
+    X = oracle.rmsnorm_f16(Y, 256)
+    assert np.array_equal(oracle.rmsnorm_f16(_h(-y), 256), X ^ np.uint16(0x8000))
+    X4 = oracle.rmsnorm_f16(_h(y * 4.0), 256)
+    ulps = np.abs(X4.astype(np.int32) - X.astype(np.int32))
+    assert ulps.max() <= 1 and (ulps > 0).mean() < 0.01
+    xf = X.view(np.float16).astype(np.float64)
+    assert np.all(np.abs((xf ** 2).mean(axis=1) - 1.0) < 2e-3)

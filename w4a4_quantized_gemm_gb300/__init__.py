@@ -47,6 +47,7 @@ SIGNATURES = {
     "w4a4_linear": (I, [P, Z, P, Z, P, P, I, I, I, I, P, P]),
     "w4a4_linear_select": (I, [P, Z, P, Z, P, P, I, I, I, I, P, I, P]),
     "w4a4_linear_noalloc": (I, [P, P, Z, P, P, I, I, I, I, P, P]),
+    "w4a4_rmsnorm_f16": (I, [P, I, I, I, P, P]),
     "w4a4_debug_unpack_weights": (I, [P, I, I, I, P, P, P, P, P]),
     "w4a4_debug_unpack_act": (I, [P, I, I, I, P, P, P, P, P]),
     "w4a4_debug_group_partials": (I, [P, P, I, I, I, I, I, P, P]),
@@ -147,6 +148,14 @@ def w4a4_linear_noalloc(X, packed, colscale, bias, Y, r: int, stream=None):
 
 
 NOALLOC_WORKSPACE_BYTES = 8 << 20
+
+
+def w4a4_rmsnorm_f16(Y, K: int, X, stream=None):
+    """RMSNorm (unit gain) of the first K columns of each row of Y into X [M, K]."""
+    M, ld = Y.shape
+    if X.shape[0] != M or X.shape[1] != K:
+        raise W4A4Error(1, "w4a4_rmsnorm_f16")
+    _check(lib().w4a4_rmsnorm_f16(_ptr(Y), M, ld, K, _ptr(X), _stream(stream)), "w4a4_rmsnorm_f16")
 
 
 def w4a4_debug_unpack_weights(packed, N: int, K: int, r: int, stream=None):

@@ -223,6 +223,18 @@ w4a4_status w4a4_linear(const void* act_ws, size_t act_ws_bytes, const void* pac
                               W4A4_KERNEL_AUTO, stream);
 }
 
+w4a4_status w4a4_rmsnorm_f16(const uint16_t* Y, int M, int ld_y, int K, uint16_t* X, cudaStream_t stream) {
+    if (M < 0 || K < 0 || ld_y < K) return W4A4_ERR_INVALID_ARG;
+    if (K < 8 || K % 8 != 0 || ld_y % 8 != 0) return W4A4_ERR_UNSUPPORTED_SHAPE;
+    if (M == 0) return W4A4_OK;
+    if (!Y || !X) return W4A4_ERR_INVALID_ARG;
+    if (!aligned16(Y) || !aligned16(X)) return W4A4_ERR_MISALIGNED;
+    w4a4_status st = check_device();
+    if (st != W4A4_OK) return st;
+    launch_rmsnorm_f16(Y, M, ld_y, K, W4A4_RMSNORM_EPS, X, stream);
+    return launch_status();
+}
+
 w4a4_status w4a4_debug_unpack_weights(const void* packed, int N, int K, int r, int8_t* codes, uint16_t* scales,
                                       uint16_t* L_down, uint16_t* L_up, cudaStream_t stream) {
     w4a4_status st = check_kn(N, K, r);

@@ -29,4 +29,7 @@ w4a4_status launch_gemm_tc(const uint8_t* ws, const uint8_t* packed, const uint1
                            const uint16_t* bias, int M, int N, int K, int r, uint16_t* Y, int32_t* P_dump,
                            cudaStream_t s);
 
+// rmsnorm.cu (stack glue between linears)
+void launch_rmsnorm_f16(const uint16_t* Y, int M, int ld_y, int K, double eps, uint16_t* X, cudaStream_t s);
+
 }  // namespace w4a4
