@@ -462,12 +462,24 @@ def run_stack(args, rank, world, local_rank):
         for i, L in enumerate(stack.layers):
             w4.w4a4_linear(L["ws"], L["packed"], L["cs"], L["b"], L["Y"], L["K"], L["r"], w4.KERNEL_AUTO, st)
 
+    def quant_only(st):
+        for L in stack.layers:
+            w4.w4a4_quantize_act(L["X"], L["packed"], L["ws"], L["r"], st)
+
+    def glue_only(st):
+        for i in range(len(stack.layers)):
+            stack.run_glue(i, st)
+
     stack.forward()
     torch.cuda.synchronize()
-    g_gemm = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g_gemm):
-        gemm_only(torch.cuda.current_stream())
-    torch.cuda.synchronize()
+    parts = {}
+    for name, fn in (("gemm", gemm_only), ("quantize", quant_only), ("glue", glue_only)):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            fn(torch.cuda.current_stream())
+        torch.cuda.synchronize()
+        parts[name] = g
+    g_gemm = parts["gemm"]
 
     def timed(graph, steps):
         for _ in range(args.warmup):
@@ -511,6 +523,8 @@ def run_stack(args, rank, world, local_rank):
                 "kernel": "w4a4_linear (GEMM + LoRA up + affine), 112 launches per forward",
                 "peak_source": f"{peak_src} bf16 burst x 2 (fp8 kind)",
                 "gemm_us_per_step": gemm_s * 1e6, "forward_us": ms_per_step * 1e3,
+                "quantize_us_per_step": timed(parts["quantize"], args.steps) / args.steps * 1e3,
+                "glue_us_per_step": timed(parts["glue"], args.steps) / args.steps * 1e3,
                 "packed_weight_bytes": weight_bytes}
 
     e2e = None

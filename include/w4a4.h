@@ -166,7 +166,7 @@ w4a4_status w4a4_linear_noalloc(const uint16_t* X, const void* packed, size_t pa
  * fp64; 1/sqrt(mean + eps) is taken in fp64 and each product y * inv is rounded
  * once, fp64 -> fp16, to nearest even, so the result is the same bits as any
  * implementation of this arithmetic up to the order of the fp64 additions.
- * K % 8 == 0, K >= 8, ld_y >= K, ld_y % 8 == 0, 16-byte aligned pointers;
+ * K % 8 == 0, 8 <= K <= 16384, ld_y >= K, ld_y % 8 == 0, 16-byte aligned pointers;
  * Y and X must not overlap.  M == 0 is a no-op. */
 #define W4A4_RMSNORM_EPS 1e-6
 w4a4_status w4a4_rmsnorm_f16(const uint16_t* Y, int M, int ld_y, int K, uint16_t* X, cudaStream_t stream);

@@ -85,6 +85,7 @@ def test_argument_checks_precede_any_launch(L):
     assert L.w4a4_rmsnorm_f16(A, 64, 1028, 1024, A, None) == 2    # ld_y % 8 != 0
     assert L.w4a4_rmsnorm_f16(_vp(0x10002), 64, 1024, 1024, A, None) == 3
     assert L.w4a4_rmsnorm_f16(A, 0, 1024, 1024, A, None) == 0     # M == 0: no-op
+    assert L.w4a4_rmsnorm_f16(A, 4, 16392, 16392, A, None) == 2   # K > 16384
 
 
 @pytest.mark.skipif(torch.cuda.is_available(), reason="valid shapes would launch on a GPU box")

@@ -46,12 +46,13 @@ def _assert_f16_equal(got: np.ndarray, want: np.ndarray, what: str):
     assert ulps.max() <= 1 and (ulps > 0).sum() <= 1, f"{what}: {(ulps > 0).sum()} elements differ, max {ulps.max()}"
 
 
-def test_rmsnorm_matches_oracle():
-    """Ragged row count, a row stride wider than K, an all-zero row, outliers."""
-    rng = np.random.default_rng(11)
-    M, ld, K = 37, 6144, 3072
+@pytest.mark.parametrize("M,ld,K", [(37, 6144, 3072), (19, 14336, 14336), (5, 1040, 1032)])
+def test_rmsnorm_matches_oracle(M, ld, K):
+    """Ragged row counts, a row stride wider than K, rows held in registers and
+    rows read twice (K > 4096), K not a multiple of 256, an all-zero row, outliers."""
+    rng = np.random.default_rng(11 + K)
     Y, _ = make_activations(rng, M, ld)
-    Y[5] = 0
+    Y[min(5, M - 1)] = 0
     X = torch.empty((M, K), dtype=torch.float16, device="cuda")
     w4.w4a4_rmsnorm_f16(_f16(Y), K, X)
     torch.cuda.synchronize()

@@ -225,7 +225,7 @@ w4a4_status w4a4_linear(const void* act_ws, size_t act_ws_bytes, const void* pac
 
 w4a4_status w4a4_rmsnorm_f16(const uint16_t* Y, int M, int ld_y, int K, uint16_t* X, cudaStream_t stream) {
     if (M < 0 || K < 0 || ld_y < K) return W4A4_ERR_INVALID_ARG;
-    if (K < 8 || K % 8 != 0 || ld_y % 8 != 0) return W4A4_ERR_UNSUPPORTED_SHAPE;
+    if (K < 8 || K % 8 != 0 || K > 16384 || ld_y % 8 != 0) return W4A4_ERR_UNSUPPORTED_SHAPE;
     if (M == 0) return W4A4_OK;
     if (!Y || !X) return W4A4_ERR_INVALID_ARG;
     if (!aligned16(Y) || !aligned16(X)) return W4A4_ERR_MISALIGNED;

@@ -6,63 +6,137 @@
 // linears; the page gives no epsilon, 1e-6 is the Qwen3 value).
 //
 // The arithmetic is fixed so that any implementation of it gives the same
-// fp16 bits: each square of an fp16 value is exact in fp32, the sum is
-// accumulated in fp64, 1 / sqrt(mean + eps) is taken in fp64 with IEEE
-// division and square root, and the product y * inv is rounded once, from
-// fp64 to fp16, to nearest even.  Only the order of the fp64 additions may
-// differ, which moves the result by a few fp64 ulps.
+// fp16 bits: each square of an fp16 value is exact in fp32, the sum is taken
+// to (at least) fp64 accuracy, 1 / sqrt(mean + eps) is taken in fp64 with IEEE
+// division and square root, and the product y * inv is rounded once, from its
+// fp64 value to fp16, to nearest even.
 //
-// One warp per row: each lane reads 16 bytes (8 values) per step, coalesced;
-// the row is read twice (the second time from L1/L2).
+// GB300's fp64 rate is low, so neither pass runs fp64 per element:
+//  * the sum is an error-free two-term fp32 accumulation (hi + lo, Knuth's
+//    two-sum), combined in fp64 per row: its error is ~2^-44 relative,
+//    far below what could move an fp16 result;
+//  * the product is formed in fp32 (within 2^-23 relative of the fp64 one);
+//    only where that lands within 2 fp32 ulps of a midpoint between two fp16
+//    numbers (or in the fp16 subnormal range) is it redone in fp64, so the
+//    rounding to fp16 is the one the fp64 product gets.
+//
+// One CTA per row: each thread reads its 16-byte chunks once (coalesced), keeps
+// them in registers, and writes the normalised values.
 #include "kernels.h"
 
 namespace w4a4 {
 namespace {
 
-constexpr int kRowsPerCta = 8;  // one warp per row
 
-__global__ void __launch_bounds__(kRowsPerCta * 32) rmsnorm_f16_kernel(const uint16_t* __restrict__ Y, int M,
-                                                                       int ld_y, int K, double eps,
-                                                                       uint16_t* __restrict__ X) {
-    const int lane = threadIdx.x & 31;
-    const int m = blockIdx.x * kRowsPerCta + (threadIdx.x >> 5);
-    if (m >= M) return;
-    const uint16_t* yr = Y + (size_t)m * ld_y;
-    double ss = 0.0;
-    for (int k = lane * 8; k < K; k += 32 * 8) {
-        const uint4 v = *reinterpret_cast<const uint4*>(yr + k);
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+// Two-term (Knuth two-sum) accumulation of the exact fp32 squares of 8 fp16 values.
+__device__ __forceinline__ void add_squares(const uint4 v, float& hi, float& lo) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[j]));
-            ss += double(f.x * f.x) + double(f.y * f.y);  // each square exact in fp32
+    for (int j = 0; j < 4; ++j) {
+        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[j]));
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const float q = h ? __fmul_rn(f.y, f.y) : __fmul_rn(f.x, f.x);  // exact
+            const float s = __fadd_rn(hi, q);                                 // s + e == hi + q exactly
+            const float bp = __fsub_rn(s, hi);
+            const float e = __fadd_rn(__fsub_rn(hi, __fsub_rn(s, bp)), __fsub_rn(q, bp));
+            hi = s;
+            lo = __fadd_rn(lo, e);
         }
     }
+}
+
+// fp16(y * inv) for 8 values, rounded as the fp64 product would be.  The fp32
+// product is within one fp32 ulp of the fp64 one (inv rounded to fp32, then
+// the product rounded), so where it lies more than 2 ulps from a midpoint
+// between fp16 numbers both round alike; the few others are redone in fp64.
+__device__ __forceinline__ uint4 scale_to_f16(const uint4 v, double inv, float invf) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    float y[8], t[8];
+    uint32_t flags = 0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[j]));
+        y[2 * j] = f.x;
+        y[2 * j + 1] = f.y;
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        t[i] = __fmul_rn(y[i], invf);
+        // the 13 fp32 mantissa bits below fp16 precision: 0x1000 is a midpoint
+        const int low = int(__float_as_uint(t[i]) & 0x1FFFu) - 0x1000;
+        const bool near = (fabsf(t[i]) < 6.103515625e-05f && t[i] != 0.f) || (low >= -2 && low <= 2);
+        flags |= uint32_t(near) << i;
+    }
+    uint16_t h[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) h[i] = __half_as_ushort(__float2half_rn(t[i]));
+    if (__any_sync(0xffffffffu, flags != 0)) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            if (flags & (1u << i)) h[i] = __half_as_ushort(__double2half(double(y[i]) * inv));
+    }
+    return make_uint4(uint32_t(h[0]) | (uint32_t(h[1]) << 16), uint32_t(h[2]) | (uint32_t(h[3]) << 16),
+                      uint32_t(h[4]) | (uint32_t(h[5]) << 16), uint32_t(h[6]) | (uint32_t(h[7]) << 16));
+}
+
+// One CTA of 256 threads per row; thread t holds chunks (c * 256 + t) of 8
+// values (c < CH) in registers between the two steps.  The fp64 partial sums
+// are combined warp by warp, then over the 8 warps in a fixed order.
+template <int CH>
+__global__ void __launch_bounds__(256) rmsnorm_f16_kernel(const uint16_t* __restrict__ Y, int ld_y, int K,
+                                                          double eps, uint16_t* __restrict__ X) {
+    __shared__ double red[8];
+    __shared__ double row_inv;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const uint16_t* yr = Y + (size_t)blockIdx.x * ld_y;
+    uint16_t* xr = X + (size_t)blockIdx.x * K;
+    uint4 v[CH];
+    float hi = 0.f, lo = 0.f;
+#pragma unroll
+    for (int c = 0; c < CH; ++c) {
+        const int k = (c * 256 + tid) * 8;
+        v[c] = k < K ? *reinterpret_cast<const uint4*>(yr + k) : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int c = 0; c < CH; ++c) add_squares(v[c], hi, lo);
+    double ss = double(hi) + double(lo);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-    const double inv = 1.0 / sqrt(ss / double(K) + eps);
-    uint16_t* xr = X + (size_t)m * K;
-    for (int k = lane * 8; k < K; k += 32 * 8) {
-        const uint4 v = *reinterpret_cast<const uint4*>(yr + k);
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-        uint32_t out[4];
+    if (lane == 0) red[warp] = ss;
+    __syncthreads();
+    if (tid == 0) {
+        double t = 0.0;
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[j]));
-            const uint32_t lo = __half_as_ushort(__double2half(double(f.x) * inv));
-            const uint32_t hi = __half_as_ushort(__double2half(double(f.y) * inv));
-            out[j] = lo | (hi << 16);
+        for (int w = 0; w < 8; ++w) t += red[w];
+        row_inv = 1.0 / sqrt(t / double(K) + eps);
+    }
+    __syncthreads();
+    const double inv = row_inv;
+    const float invf = float(inv);
+#pragma unroll
+    for (int c = 0; c < CH; ++c) {
+        if ((c * 256 + warp * 32) * 8 < K) {  // warp-uniform: the vote inside stays converged
+            const int k = (c * 256 + tid) * 8;
+            const uint4 o = scale_to_f16(v[c], inv, invf);
+            if (k < K) *reinterpret_cast<uint4*>(xr + k) = o;
         }
-        *reinterpret_cast<uint4*>(xr + k) = make_uint4(out[0], out[1], out[2], out[3]);
     }
 }
 
 }  // namespace
 
 void launch_rmsnorm_f16(const uint16_t* Y, int M, int ld_y, int K, double eps, uint16_t* X, cudaStream_t s) {
-    const int grid = (M + kRowsPerCta - 1) / kRowsPerCta;
-    rmsnorm_f16_kernel<<<grid, kRowsPerCta * 32, 0, s>>>(Y, M, ld_y, K, eps, X);
-    set_dispatch("rmsnorm_f16 rows=%d K=%d ld=%d grid=%d", M, K, ld_y, grid);
+    const int ch = (K + 2047) / 2048;  // 8-value chunks per thread
+    if (ch <= 1)
+        rmsnorm_f16_kernel<1><<<M, 256, 0, s>>>(Y, ld_y, K, eps, X);
+    else if (ch <= 2)
+        rmsnorm_f16_kernel<2><<<M, 256, 0, s>>>(Y, ld_y, K, eps, X);
+    else if (ch <= 4)
+        rmsnorm_f16_kernel<4><<<M, 256, 0, s>>>(Y, ld_y, K, eps, X);
+    else
+        rmsnorm_f16_kernel<8><<<M, 256, 0, s>>>(Y, ld_y, K, eps, X);
+    set_dispatch("rmsnorm_f16 rows=%d K=%d ld=%d chunks/thread=%d", M, K, ld_y, ch <= 2 ? ch : (ch <= 4 ? 4 : 8));
 }
 
 }  // namespace w4a4
