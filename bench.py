@@ -566,6 +566,92 @@ def run_stack(args, rank, world, local_rank):
     return 0
 
 
+# ------------------------------------------------------- config 3: small M
+DECODE_METRIC = "W4A4+LoRA linear packed-weight GB/s (K=N=4096, small M; min over M<=32)"
+
+
+def run_decode(args, rank, world, local_rank):
+    """Config 3: M in {1, 4, 16, 32, 76}, K = N = 4096.  Each timed GEMM call
+    reads a different replica of the packed weights (20 replicas > L2), so the
+    weights come from HBM; value = the lowest weight bandwidth over M <= 32."""
+    import torch
+    torch.cuda.set_device(local_rank)
+    from w4a4_quantized_gemm_gb300 import build as wbuild
+    wbuild.build()
+    import w4a4_quantized_gemm_gb300 as w4
+    from synthetic import SMALL_M_SWEEP
+
+    dev = torch.device("cuda", local_rank)
+    R = 20
+    results = {}
+    peaks = {}
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            peaks = json.load(f)
+    except (OSError, ValueError):
+        pass
+    hbm, hbm_src = (float(peaks["hbm_gbs"]), "measured") if "hbm_gbs" in peaks else (6800.0, "fallback")
+    base = make_linear_case(seed=0, **SMALL_M_SWEEP[-1])
+    W = torch.from_numpy(base.W).to(dev)
+    Ld = torch.from_numpy(base.L_down.view(np.float16).copy()).to(dev)
+    Lu = torch.from_numpy(base.L_up.view(np.float16).copy()).to(dev)
+    packed0 = torch.empty(w4.packed_weights_bytes(base.N, base.K, base.r), dtype=torch.uint8, device=dev)
+    w4.w4a4_pack_weights(W, Ld, Lu, packed0, base.r)
+    del W
+    packs = [packed0.clone() for _ in range(R)]
+    cs = torch.from_numpy(base.colscale.view(np.float16).copy()).to(dev)
+    b = torch.from_numpy(base.bias.view(np.float16).copy()).to(dev)
+    wbytes = metrics.weight_bytes(base.N, base.K)
+    for s_ in SMALL_M_SWEEP:
+        M = s_["M"]
+        X = torch.from_numpy(base.X[:M].view(np.float16).copy()).to(dev)
+        ws = torch.empty(w4.act_workspace_bytes(M, base.K, base.r), dtype=torch.uint8, device=dev)
+        Y = torch.empty((M, base.N), dtype=torch.float16, device=dev)
+        w4.w4a4_quantize_act(X, packs[0], ws, base.r)
+        w4.w4a4_linear(ws, packs[0], cs, b, Y, base.K, base.r)
+        disp = w4.w4a4_last_dispatch()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for p_ in packs:
+                w4.w4a4_linear(ws, p_, cs, b, Y, base.K, base.r, w4.KERNEL_AUTO, torch.cuda.current_stream())
+        gq = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gq):
+            for p_ in packs:
+                w4.w4a4_quantize_act(X, p_, ws, base.r, torch.cuda.current_stream())
+        torch.cuda.synchronize()
+        def tm(graph):
+            for _ in range(max(args.warmup, 3)):
+                graph.replay()
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            for _ in range(args.steps):
+                graph.replay()
+            e1.record()
+            torch.cuda.synchronize()
+            return e0.elapsed_time(e1) * 1e3 / (args.steps * R)
+        us = tm(g)
+        uq = tm(gq)
+        results[M] = {"gemm_us": us, "quantize_us": uq, "weight_gbs": wbytes / (us * 1e-6) / 1e9,
+                      "frac_hbm": wbytes / (us * 1e-6) / 1e9 / hbm, "dispatch": disp}
+    low = min(v["weight_gbs"] for m, v in results.items() if m <= 32)
+    m32 = results[32]
+    print(json.dumps({
+        "metric": DECODE_METRIC, "value": low, "unit": "GB/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": m32["gemm_us"] * 1e-3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "int4 codes (fp8 e4m3 operands), fp32 accumulate, fp16 out",
+        "data": "synthetic",
+        "config": {"workload": "small_m_sweep_K4096_N4096", "group": 64, "rank": 32, "replicas": R,
+                   "l2": f"{R} weight replicas, {R * wbytes / 2**20:.0f} MiB > L2", "per_M": results},
+        "gpu_launches": args.steps * R * len(results) * 2,
+        "roofline": {"bound": "hbm", "achieved": low, "peak": hbm, "unit": "GB/s", "frac": low / hbm,
+                     "traffic": None, "kernel": "w4a4_linear (small-M weight-streaming kernel)",
+                     "peak_source": f"{hbm_src} HBM copy bandwidth",
+                     "algorithmic_bytes_per_call": wbytes}}), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -577,13 +663,15 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--workload", choices=["layer", "stack"], default="layer")
+    ap.add_argument("--workload", choices=["layer", "stack", "decode"], default="layer")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
     rank = _env_int("RANK", 0)
     world = _env_int("WORLD_SIZE", 1)
     local_rank = _env_int("LOCAL_RANK", 0)
+    if args.workload == "decode" and args.impl == "ours":
+        return run_decode(args, rank, world, local_rank)
     if args.workload == "stack":
         if args.impl == "reference":
             return run_stack_reference(args, rank, world)

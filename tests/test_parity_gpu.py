@@ -219,3 +219,31 @@ def test_dispatch_is_logged():
     ws = quantize(c, t, packed)
     run_linear(c, t, packed, ws, w4.KERNEL_SMALLM)
     assert "gemm_smallm" in w4.w4a4_last_dispatch()
+
+
+# Small-M kernel with K split over a cluster: uneven group shares (G not a
+# multiple of the split), a ragged last column tile (warps without rows), and
+# more than one chunk of 8 groups per CTA.
+def _expected_split(M, N, K):
+    tok = 8 if M <= 8 else 16 if M <= 16 else 32 if M <= 32 else 64
+    tiles = -(-N // 128) * -(-M // tok)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    ks = 1
+    while ks < 8 and tiles * ks * 2 <= 2 * sms and ks * 2 <= K // 64:
+        ks *= 2
+    return ks
+
+
+@pytest.mark.parametrize("M,N,K,r", [(3, 400, 832, 32), (40, 144, 448, 16), (2, 48, 4480, 32), (1, 12800, 1280, 32),
+                                     (12, 1024, 4096, 64)])
+def test_smallm_split_k_cluster(M, N, K, r):
+    ks = _expected_split(M, N, K)
+    c = make_linear_case(M, K, N, r, seed=M + N + K)
+    t = to_dev(c)
+    packed = pack(c, t)
+    ws = quantize(c, t, packed)
+    Y = run_linear(c, t, packed, ws, w4.KERNEL_SMALLM)
+    assert f"split-K={ks} " in w4.w4a4_last_dispatch(), w4.w4a4_last_dispatch()
+    y = oracle.linear(c.X, c.W, c.L_down, c.L_up, c.colscale, c.bias)
+    check_tol(Y, y, f"smallm split {M}x{N}x{K} r={r}")
+    assert w4.w4a4_device_status() == 0

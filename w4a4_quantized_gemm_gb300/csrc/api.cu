@@ -60,6 +60,12 @@ w4a4_status sync_status(cudaStream_t s) {
     }
     return W4A4_OK;
 }
+// Reads and clears the status words of both GEMM kernels' bounded waits.
+w4a4_status device_status_words() {
+    const w4a4_status a = tc_read_and_clear_status();
+    const w4a4_status b = smallm_read_and_clear_status();
+    return a != W4A4_OK ? a : b;
+}
 }  // namespace
 
 void set_dispatch(const char* fmt, ...) {
@@ -276,7 +282,7 @@ w4a4_status w4a4_debug_group_partials(const void* act_ws, const void* packed, in
         st = launch_gemm_smallm(ws, pk, nullptr, nullptr, M, N, K, r, nullptr, P, stream);
     if (st != W4A4_OK) return st;
     if ((st = sync_status(stream)) != W4A4_OK) return st;
-    return tc_read_and_clear_status();
+    return device_status_words();
 }
 
 w4a4_status w4a4_device_status(void) {
@@ -284,7 +290,7 @@ w4a4_status w4a4_device_status(void) {
         cudaGetLastError();
         return W4A4_ERR_CUDA;
     }
-    return tc_read_and_clear_status();
+    return device_status_words();
 }
 
 }  // extern "C"

@@ -147,5 +147,6 @@ namespace w4a4 {
 void set_dispatch(const char* fmt, ...);
 w4a4_status launch_status();  // maps cudaGetLastError() to a status
 int device_sm_count();        // multiprocessors of the current device (cached)
-w4a4_status tc_read_and_clear_status();  // bounded-wait status of the tcgen05 kernel
+w4a4_status tc_read_and_clear_status();      // bounded-wait status of the tcgen05 kernel
+w4a4_status smallm_read_and_clear_status();  // bounded-wait status of the small-M kernel
 }  // namespace w4a4

@@ -140,10 +140,23 @@ __device__ __forceinline__ bool warp_wait_parity_cluster(uint32_t bar, uint32_t 
     }
     return __all_sync(0xffffffffu, ok);
 }
+// The two halves of a cluster barrier, for work placed between them.
+__device__ __forceinline__ void cluster_arrive_release() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait_acquire() {
+    asm volatile("barrier.cluster.wait.acquire.aligned;\n" ::: "memory");
+}
 // Every thread of every CTA of the cluster: no CTA leaves before the others are
 // done with its shared memory.
 __device__ __forceinline__ void cluster_sync_all() {
     asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;\n" ::: "memory");
+}
+
+// Arrive on a CTA mbarrier once every cp.async this thread issued so far has
+// landed; the arrival counts toward the barrier's initial count (noinc).
+__device__ __forceinline__ void cp_async_mbar_arrive_noinc(uint32_t bar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];\n" ::"r"(bar) : "memory");
 }
 
 __device__ __forceinline__ void fence_proxy_async_smem() {
