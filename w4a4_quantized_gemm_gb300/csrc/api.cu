@@ -14,7 +14,7 @@ namespace w4a4 {
 namespace {
 thread_local char t_dispatch[256] = "none";
 int g_small_m_threshold = -1;  // -1: read W4A4_SMALL_M on first use
-constexpr int kDefaultSmallM = 64;  // M <= this -> weight-streaming kernel, else tcgen05 tiles
+constexpr int kDefaultSmallM = 32;  // M <= this -> weight-streaming kernel, else tcgen05 tiles (measured crossover: 32..48)
 std::mutex g_mu;
 int g_sm_count[64] = {0};
 

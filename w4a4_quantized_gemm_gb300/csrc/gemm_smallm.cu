@@ -44,6 +44,7 @@ constexpr int kWarps = 8;
 constexpr int kTileN = kWarps * 16;  // weight rows per CTA
 constexpr int kMaxKS = 8;
 constexpr uint64_t kWaitNs = 2000000000ull;
+constexpr uint32_t kSuspendNs = 20000;  // upper bound of one suspension in a wait
 
 // Status word of this kernel's bounded waits (W4A4_ERR_TIMEOUT once one gave up).
 __device__ int g_smallm_status = 0;
@@ -186,18 +187,26 @@ __global__ void __launch_bounds__(kWarps * 32) gemm_smallm_kernel(
         }
     }
 
-    float acc[NT8][4];
+    // fp32 accumulators as packed pairs: (row a | row b) x (token 2q, 2q + 1) of each 8-token block
+    uint64_t acc_a[NT8], acc_b[NT8];
 #pragma unroll
-    for (int t = 0; t < NT8; ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.f;
+    for (int t = 0; t < NT8; ++t) acc_a[t] = acc_b[t] = 0ull;
+    const uint64_t m8 = f2_pack(-8.f, -8.f);
 
     // this lane's weight bytes (rows warp*16 + gid and + 8, bytes 8q..8q+7) and scales in a slot
     const uint8_t* smw = smraw + PLN.wq + (warp * 16 + gid) * 32 + 8 * q;
     const uint16_t* smsw = reinterpret_cast<const uint16_t*>(smraw + PLN.sw) + warp * 16 + gid;
+    // ldmatrix row address of this lane within a slot's code planes, token block 0: matrix
+    // lane / 8 = (plane, logical 16-byte chunk), row lane % 8 (the chunk's physical place
+    // follows the 32-byte swizzle of the token's row; token blocks start at multiples of 8)
+    const uint32_t lm_lane = uint32_t((lane >> 4) * (TOK * 32) + (lane & 7) * 32 +
+                                      ((((lane >> 3) & 1) ^ ((lane >> 2) & 1)) * 16));
     for (int c = 0; c < n_chunks; ++c) {
         const int b = c & 1, ng = min(half, n_groups - c * half);
         for (int j = 0; j < ng; ++j) {
             const int slot = b * half + j;
-            const bool ok = warp_wait_parity(full0 + 8u * slot, uint32_t(c >> 1) & 1u, abort, kWaitNs);
+            const bool ok = warp_wait_parity_suspend(full0 + 8u * slot, uint32_t(c >> 1) & 1u, abort, kWaitNs,
+                                                     kSuspendNs);
             if (!ok) {
                 if (lane == 0) {
                     *abort = 1;
@@ -210,6 +219,7 @@ __global__ void __launch_bounds__(kWarps * 32) gemm_smallm_kernel(
             const uint2 wb = *reinterpret_cast<const uint2*>(smw + slot * (kTileN * 32) + 8 * 32);
             const float swa = __half2float(__ushort_as_half(smsw[slot * kTileN]));
             const float swb = __half2float(__ushort_as_half(smsw[slot * kTileN + 8]));
+            const uint64_t swa2 = f2_pack(swa, swa), swb2 = f2_pack(swb, swb);
             uint32_t a0[4], a1[4];  // k-halves 0 and 1
             a0[0] = expand4(wa.x);
             a0[2] = expand4(wa.x >> 16);
@@ -219,40 +229,34 @@ __global__ void __launch_bounds__(kWarps * 32) gemm_smallm_kernel(
             a1[2] = expand4(wa.y >> 16);
             a1[1] = expand4(wb.y);
             a1[3] = expand4(wb.y >> 16);
-            const uint8_t* aq = smraw + PLN.aq + slot * (2 * TOK * 32);
-            const float2* as = reinterpret_cast<const float2*>(smraw + PLN.as + slot * (TOK * 8));
 #pragma unroll
             for (int t = 0; t < NT8; ++t) {
-                const int row = t * 8 + gid;
-                const int sw = swz32(row, 0) * 16;  // row % 8 == (rt0 + row) % 8
-                const uint8_t* r0 = aq + row * 32;
-                const uint8_t* r1 = aq + TOK * 32 + row * 32;
-                const uint32_t b00 = *reinterpret_cast<const uint32_t*>(r0 + sw + 4 * q);
-                const uint32_t b01 = *reinterpret_cast<const uint32_t*>(r0 + (sw ^ 16) + 4 * q);
-                const uint32_t b10 = *reinterpret_cast<const uint32_t*>(r1 + sw + 4 * q);
-                const uint32_t b11 = *reinterpret_cast<const uint32_t*>(r1 + (sw ^ 16) + 4 * q);
+                uint32_t bf[4];  // (plane 0 | plane 1) x (k 0-15 | k 16-31) of tokens t*8 .. t*8+7
+                ldsm_x4(bf, sbase + PLN.aq + uint32_t(slot * (2 * TOK * 32) + t * 256) + lm_lane);
+                // (sA, SA) of tokens t*8 + 2q and + 1
+                const float4 s =
+                    *reinterpret_cast<const float4*>(smraw + PLN.as + slot * (TOK * 8) + (t * 8 + 2 * q) * 8);
                 float d[4] = {0.f, 0.f, 0.f, 0.f};
-                mma_e4m3_16832(d, a0, b00, b01);
-                mma_e4m3_16832(d, a1, b10, b11);
-                const float2 s0 = as[t * 8 + 2 * q], s1 = as[t * 8 + 2 * q + 1];
+                mma_e4m3_16832(d, a0, bf[0], bf[1]);
+                mma_e4m3_16832(d, a1, bf[2], bf[3]);
                 if constexpr (DUMP) {
                     const int g = g_begin + c * half + j;
                     const int m0 = tok0 + t * 8 + 2 * q;
                     const int na_ = n0 + gid, nb_ = n0 + gid + 8;
                     if (m0 < M) {
-                        P[((size_t)m0 * N + na_) * G + g] = int32_t(d[0] - 8.f * s0.y);
-                        P[((size_t)m0 * N + nb_) * G + g] = int32_t(d[2] - 8.f * s0.y);
+                        P[((size_t)m0 * N + na_) * G + g] = int32_t(d[0] - 8.f * s.y);
+                        P[((size_t)m0 * N + nb_) * G + g] = int32_t(d[2] - 8.f * s.y);
                     }
                     if (m0 + 1 < M) {
-                        P[((size_t)(m0 + 1) * N + na_) * G + g] = int32_t(d[1] - 8.f * s1.y);
-                        P[((size_t)(m0 + 1) * N + nb_) * G + g] = int32_t(d[3] - 8.f * s1.y);
+                        P[((size_t)(m0 + 1) * N + na_) * G + g] = int32_t(d[1] - 8.f * s.w);
+                        P[((size_t)(m0 + 1) * N + nb_) * G + g] = int32_t(d[3] - 8.f * s.w);
                     }
                 } else {
-                    const float c0 = (-8.f * s0.y) * s0.x, c1 = (-8.f * s1.y) * s1.x;
-                    acc[t][0] = fmaf(swa, fmaf(s0.x, d[0], c0), acc[t][0]);
-                    acc[t][1] = fmaf(swa, fmaf(s1.x, d[1], c1), acc[t][1]);
-                    acc[t][2] = fmaf(swb, fmaf(s0.x, d[2], c0), acc[t][2]);
-                    acc[t][3] = fmaf(swb, fmaf(s1.x, d[3], c1), acc[t][3]);
+                    // acc += sW * (sA * D + (-8 SA) sA), pairwise over the two tokens
+                    const uint64_t sA2 = f2_pack(s.x, s.z);
+                    const uint64_t cc = fmul2_b64(fmul2_b64(f2_pack(s.y, s.w), m8), sA2);
+                    acc_a[t] = ffma2_b64(swa2, ffma2_b64(sA2, f2_pack(d[0], d[1]), cc), acc_a[t]);
+                    acc_b[t] = ffma2_b64(swb2, ffma2_b64(sA2, f2_pack(d[2], d[3]), cc), acc_b[t]);
                 }
             }
         }
@@ -271,13 +275,19 @@ __global__ void __launch_bounds__(kWarps * 32) gemm_smallm_kernel(
             for (int c = max(0, requested - 2); c < requested; ++c) {
                 const int ng = min(half, n_groups - c * half);
                 for (int j = 0; j < ng; ++j)
-                    wait_parity(full0 + 8u * ((c & 1) * half + j), uint32_t(c >> 1) & 1u, &never_abort, kWaitNs);
+                    wait_parity_suspend(full0 + 8u * ((c & 1) * half + j), uint32_t(c >> 1) & 1u, &never_abort, kWaitNs, kSuspendNs);
             }
-            if (!DUMP) wait_parity(aux_full, 0u, &never_abort, kWaitNs);
+            if (!DUMP) wait_parity_suspend(aux_full, 0u, &never_abort, kWaitNs, kSuspendNs);
         }
     }
     if constexpr (DUMP) return;
 
+    float acc[NT8][4];
+#pragma unroll
+    for (int t = 0; t < NT8; ++t) {
+        const float2 pa = f2_unpack(acc_a[t]), pb = f2_unpack(acc_b[t]);
+        acc[t][0] = pa.x, acc[t][1] = pa.y, acc[t][2] = pb.x, acc[t][3] = pb.y;
+    }
     if (KS > 1) {
         cluster_wait_acquire();  // every rank's barriers are initialised
         const int orank = warp % KS, ow = warp / KS;  // owner rank, owned-warp index there
@@ -290,7 +300,7 @@ __global__ void __launch_bounds__(kWarps * 32) gemm_smallm_kernel(
             for (int t = 0; t < NT8; ++t)
                 st_async_v4(dst + uint32_t(t) * 16u, make_float4(acc[t][0], acc[t][1], acc[t][2], acc[t][3]), rbar);
         } else {
-            const bool ok = warp_wait_parity(red_full, 0u, abort, kWaitNs);
+            const bool ok = warp_wait_parity_suspend(red_full, 0u, abort, kWaitNs, kSuspendNs);
             if (!ok) {
                 if (lane == 0) {
                     *abort = 1;
@@ -320,7 +330,7 @@ __global__ void __launch_bounds__(kWarps * 32) gemm_smallm_kernel(
     uint16_t* ys = reinterpret_cast<uint16_t*>(smraw + PLN.wq);
     constexpr int LDY = kTileN + 8;
     if (owner && warp_active && !*abort) {
-        const bool ok = r == 0 || warp_wait_parity(aux_full, 0u, abort, kWaitNs);
+        const bool ok = r == 0 || warp_wait_parity_suspend(aux_full, 0u, abort, kWaitNs, kSuspendNs);
         if (!ok && lane == 0) {
             *abort = 1;
             atomicExch(&g_smallm_status, int(W4A4_ERR_TIMEOUT));
@@ -366,7 +376,7 @@ __global__ void __launch_bounds__(kWarps * 32) gemm_smallm_kernel(
                 *reinterpret_cast<uint4*>(Y + (size_t)m * N + n) = *reinterpret_cast<const uint4*>(&ys[t * LDY + ch * 8]);
         }
     }
-    if (r > 0 && threadIdx.x == 0 && !wait_parity(aux_full, 0u, &never_abort, kWaitNs))
+    if (r > 0 && threadIdx.x == 0 && !wait_parity_suspend(aux_full, 0u, &never_abort, kWaitNs, kSuspendNs))
         atomicExch(&g_smallm_status, int(W4A4_ERR_TIMEOUT));  // (the LoRA copies land before the CTA leaves)
     if (KS > 1) cluster_wait_acquire();  // no rank leaves while a peer may still address its shared memory
 }

@@ -67,6 +67,27 @@ __device__ __forceinline__ bool wait_parity(uint32_t bar, uint32_t parity, volat
     }
 }
 
+// Same contract, but a warp whose phase is not complete is suspended in the
+// barrier unit -- woken when the phase completes, or after `hint_ns` -- instead
+// of polling: no issue slots are spent while waiting, and no sleep is added
+// after the completion.  The clock and the abort flag are read after every
+// suspension.
+__device__ __forceinline__ bool wait_parity_suspend(uint32_t bar, uint32_t parity, volatile int* abort,
+                                                    uint64_t limit_ns, uint32_t hint_ns) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (;;) {
+        if (mbar_try_wait_sleep(bar, parity, hint_ns)) return true;
+        if (*abort) return false;
+        if (globaltimer_ns() - t0 > limit_ns) return false;
+    }
+}
+__device__ __forceinline__ bool warp_wait_parity_suspend(uint32_t bar, uint32_t parity, volatile int* abort,
+                                                         uint64_t limit_ns, uint32_t hint_ns) {
+    const bool ok = wait_parity_suspend(bar, parity, abort, limit_ns, hint_ns);
+    return __all_sync(0xffffffffu, ok);
+}
+
 // Warp-wide wait: every lane polls the same barrier (no divergent branch around
 // a blocking instruction) and the lanes agree on the outcome.  The phase cannot
 // complete twice before this warp itself arrives somewhere, so all lanes see
@@ -327,6 +348,23 @@ __device__ __forceinline__ uint64_t ffma2_b64(uint64_t a, uint64_t b, uint64_t c
     uint64_t d;
     asm("fma.rn.f32x2 %0, %1, %2, %3;\n" : "=l"(d) : "l"(a), "l"(b), "l"(c));
     return d;
+}
+
+// d = a * b on both halves.
+__device__ __forceinline__ uint64_t fmul2_b64(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;\n" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
+// Four 8x8 b16 matrices from shared memory (row addresses from lanes 8i..8i+7
+// for matrix i); lane l receives the 32-bit word (row l / 4, column pair l % 4)
+// of each.
+__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], uint32_t saddr) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(saddr)
+                 : "memory");
 }
 
 // Packed fp32 pair FMA (sm_100 family): d = a * b + c elementwise.
