@@ -1,6 +1,11 @@
 """Profiling driver: one W4A4 linear of the M=700 decoder layer, called in a loop.
 
     python -m w4a4_quantized_gemm_gb300.profile_linear <qkv|o|gate_up|down|prefill_up|prefill_down|m1|m32> [iters]
+    python -m w4a4_quantized_gemm_gb300.profile_linear norm_gate_up [iters]
+
+The last form runs the stack's RMSNorm glue alone: the gate_up output
+[700, 6144] normalised over its first 3072 columns into the down linear's
+input, on replicas of the buffers.
 
 Each iteration runs the layer's two kernels (quantize + LoRA down, then GEMM +
 LoRA up + affine) on one of R replicas of the inputs, so that consecutive
@@ -38,6 +43,18 @@ def main() -> int:
 
     name = sys.argv[1] if len(sys.argv) > 1 else "qkv"
     iters = int(sys.argv[2]) if len(sys.argv) > 2 else 30
+    if name == "norm_gate_up":
+        dev = torch.device("cuda", 0)
+        g = torch.Generator(device="cpu").manual_seed(0)
+        Y0 = (torch.randn(700, 6144, generator=g) * 3).half().to(dev)
+        R = 24
+        Ys = [Y0.clone() for _ in range(R)]
+        Xs = [torch.empty((700, 3072), dtype=torch.float16, device=dev) for _ in range(R)]
+        for i in range(iters):
+            w4.w4a4_rmsnorm_f16(Ys[i % R], 3072, Xs[i % R])
+        torch.cuda.synchronize()
+        print(f"{name}: M=700 ld=6144 K=3072 replicas={R} iters={iters} dispatch={w4.w4a4_last_dispatch()}")
+        return 0
     s = SHAPES[name]
     M, K, N, r = s["M"], s["K"], s["N"], s["r"]
     c = make_linear_case(M=M, K=K, N=N, r=r, seed=0)
