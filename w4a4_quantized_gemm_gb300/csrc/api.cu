@@ -81,6 +81,17 @@ w4a4_status launch_status() {
     return e == cudaSuccess ? W4A4_OK : W4A4_ERR_CUDA;
 }
 
+unsigned add_pdl_attr(cudaLaunchAttribute* attrs, unsigned n) {
+    static const bool on = [] {
+        const char* e = std::getenv("W4A4_PDL");
+        return !(e && e[0] == '0');
+    }();
+    if (!on) return n;
+    attrs[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attrs[n].val.programmaticStreamSerializationAllowed = 1;
+    return n + 1;
+}
+
 int device_sm_count() {
     int dev = 0;
     cudaGetDevice(&dev);

@@ -132,6 +132,17 @@ __device__ __forceinline__ uint2 ldg_nc_v2(const void* p) {
     asm volatile("ld.global.nc.v2.u32 {%0,%1}, [%2];\n" : "=r"(v.x), "=r"(v.y) : "l"(p));
     return v;
 }
+// Programmatic dependent launch.  pdl_wait: block until the grids this one
+// depends on have completed and their writes are visible (a no-op when the
+// launch has no such dependency); every kernel calls it before its first
+// access to global memory, so no read or write can race with the previous
+// kernel in the stream.  pdl_launch_dependents: allow the next grid to be
+// scheduled now, so that its launch overlaps this grid's work.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+}
+
 __device__ __forceinline__ uint4 ldg_nc_v4(const void* p) {
     uint4 v;
     asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];\n"
@@ -147,6 +158,10 @@ namespace w4a4 {
 void set_dispatch(const char* fmt, ...);
 w4a4_status launch_status();  // maps cudaGetLastError() to a status
 int device_sm_count();        // multiprocessors of the current device (cached)
+// Appends the programmatic-stream-serialisation attribute (the launch may
+// overlap the previous kernel in the stream, which its pdl_wait orders) unless
+// W4A4_PDL=0 is set in the environment; returns the new attribute count.
+unsigned add_pdl_attr(cudaLaunchAttribute* attrs, unsigned n);
 w4a4_status tc_read_and_clear_status();      // bounded-wait status of the tcgen05 kernel
 w4a4_status smallm_read_and_clear_status();  // bounded-wait status of the small-M kernel
 }  // namespace w4a4

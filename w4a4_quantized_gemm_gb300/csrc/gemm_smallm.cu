@@ -83,6 +83,8 @@ __global__ void __launch_bounds__(kWarps * 32) gemm_smallm_kernel(
     constexpr int NT = kWarps * 32;
     extern __shared__ __align__(128) uint8_t smraw[];
     __shared__ int abort_flag, never_abort;
+    pdl_wait();
+    pdl_launch_dependents();
     const SmallMPlan PLN = smallm_plan(TOK, r);
     const uint32_t sbase = smem_u32(smraw);
     const uint32_t full0 = sbase + PLN.bar;  // full[s] = full0 + 8 s
@@ -409,13 +411,13 @@ w4a4_status launch_nt(const uint8_t* ws, const uint8_t* packed, const uint16_t* 
     const int KS = P ? 1 : smallm_split(M, N, K, NT8 * 8);
     dim3 grid(unsigned(((N + kTileN - 1) / kTileN) * KS), unsigned((M + NT8 * 8 - 1) / (NT8 * 8)));
     cudaLaunchConfig_t cfg{};
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = unsigned(KS);
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = add_pdl_attr(attr, 1);
     cfg.gridDim = grid;
     cfg.blockDim = dim3(kWarps * 32);
     cfg.dynamicSmemBytes = smallm_plan(NT8 * 8, r).total;

@@ -120,6 +120,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                    const uint16_t* __restrict__ colscale, const uint16_t* __restrict__ bias, int M, int N, int K,
                    int r, uint16_t* __restrict__ Y, int32_t* __restrict__ P, int KS) {
     extern __shared__ uint8_t smem_raw[];
+    pdl_wait();
+    pdl_launch_dependents();
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t* gbase = smem_raw + (base - raw);
@@ -620,14 +622,25 @@ w4a4_status launch_impl(const uint8_t* ws, const uint8_t* packed, const uint16_t
     const uint32_t smem = smem_map(S, rp, SPLIT).total;
     if (!SPLIT) {
         const int grid = tiles < device_sm_count() ? tiles : device_sm_count();
-        kern<<<grid, NUM_THREADS, smem, s>>>(ws, packed, cs, bias, M, N, K, r, Y, P, 1);
+        cudaLaunchConfig_t cfg{};
+        cudaLaunchAttribute attr[1];
+        cfg.attrs = attr;
+        cfg.numAttrs = add_pdl_attr(attr, 0);
+        cfg.gridDim = dim3(unsigned(grid));
+        cfg.blockDim = dim3(NUM_THREADS);
+        cfg.dynamicSmemBytes = smem;
+        cfg.stream = s;
+        if (cudaLaunchKernelEx(&cfg, kern, ws, packed, cs, bias, M, N, K, r, Y, P, 1) != cudaSuccess) {
+            cudaGetLastError();
+            return W4A4_ERR_CUDA;
+        }
         set_dispatch("gemm_tc tcgen05.f8f6f4 tile=%dx%d groups/job=%d stages=%d tiles=%d grid=%d%s", BM, BN, GPJ, S,
                      tiles, grid, DUMP ? " (partials dump)" : "");
         return launch_status();
     }
     // clusters of KS CTAs, as many as can be resident at once (persistent over tiles)
     cudaLaunchConfig_t cfg{};
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = unsigned(KS);
     attr[0].val.clusterDim.y = 1;
@@ -645,6 +658,7 @@ w4a4_status launch_impl(const uint8_t* ws, const uint8_t* packed, const uint16_t
     }
     const int clusters = tiles < active ? tiles : active;
     cfg.gridDim = dim3(unsigned(clusters * KS));
+    cfg.numAttrs = add_pdl_attr(attr, 1);
     if (cudaLaunchKernelEx(&cfg, kern, ws, packed, cs, bias, M, N, K, r, Y, P, KS) != cudaSuccess) {
         cudaGetLastError();
         return W4A4_ERR_CUDA;

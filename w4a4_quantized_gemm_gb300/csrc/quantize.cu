@@ -52,6 +52,8 @@ __global__ void __launch_bounds__(kWarps * 32) quantize_act_kernel(const uint16_
                                                                    const uint2* __restrict__ Ldp, int M,
                                                                    int K, uint8_t* __restrict__ ws) {
     extern __shared__ __align__(16) uint8_t qsm[];
+    pdl_wait();
+    pdl_launch_dependents();
     uint16_t(*xs)[kRows * kXsStride] = reinterpret_cast<uint16_t(*)[kRows * kXsStride]>(qsm);
     float* red = reinterpret_cast<float*>(qsm + kWarps * kRows * kXsStride * 2);
 
@@ -254,8 +256,11 @@ __global__ void unpack_act_kernel(const uint8_t* __restrict__ ws, int M, int K, 
 template <int R>
 w4a4_status launch_q(const uint16_t* X, const uint8_t* packed, int M, int K, uint8_t* ws, cudaStream_t s) {
     const int G = K / kGroup;
-    // split K over a (small) cluster so that each warp quantises about two groups
-    int CK = (G + 2 * kWarps - 1) / (2 * kWarps);
+    // split K over a (small) cluster: one group per warp where that takes at most
+    // two CTAs, else about two groups per warp (larger clusters cost more in
+    // their reduction than they gain)
+    int CK = (G + kWarps - 1) / kWarps;
+    if (CK > 2) CK = (G + 2 * kWarps - 1) / (2 * kWarps);
     if (CK > kMaxCluster) CK = kMaxCluster;
     if (CK < 1) CK = 1;
     const int row_blocks = (M + kRows - 1) / kRows;
@@ -274,13 +279,13 @@ w4a4_status launch_q(const uint16_t* X, const uint8_t* packed, int M, int K, uin
     }
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = unsigned(CK);
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = add_pdl_attr(attr, 1);
     const cudaError_t e = cudaLaunchKernelEx(&cfg, quantize_act_kernel<R>, X, reinterpret_cast<const uint2*>(packed),
                                              M, K, ws);
     set_dispatch("quantize_act rows/cluster=%d cluster=%d grid=%d rank=%d", kRows, CK, row_blocks * CK, R);

@@ -88,6 +88,8 @@ __global__ void __launch_bounds__(256) rmsnorm_f16_kernel(const uint16_t* __rest
                                                           double eps, uint16_t* __restrict__ X) {
     __shared__ double red[8];
     __shared__ double row_inv;
+    pdl_wait();
+    pdl_launch_dependents();
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const uint16_t* yr = Y + (size_t)blockIdx.x * ld_y;
     uint16_t* xr = X + (size_t)blockIdx.x * K;
@@ -128,14 +130,21 @@ __global__ void __launch_bounds__(256) rmsnorm_f16_kernel(const uint16_t* __rest
 
 void launch_rmsnorm_f16(const uint16_t* Y, int M, int ld_y, int K, double eps, uint16_t* X, cudaStream_t s) {
     const int ch = (K + 2047) / 2048;  // 8-value chunks per thread
+    cudaLaunchConfig_t cfg{};
+    cudaLaunchAttribute attr[1];
+    cfg.attrs = attr;
+    cfg.numAttrs = add_pdl_attr(attr, 0);
+    cfg.gridDim = dim3(unsigned(M));
+    cfg.blockDim = dim3(256);
+    cfg.stream = s;
     if (ch <= 1)
-        rmsnorm_f16_kernel<1><<<M, 256, 0, s>>>(Y, ld_y, K, eps, X);
+        cudaLaunchKernelEx(&cfg, rmsnorm_f16_kernel<1>, Y, ld_y, K, eps, X);
     else if (ch <= 2)
-        rmsnorm_f16_kernel<2><<<M, 256, 0, s>>>(Y, ld_y, K, eps, X);
+        cudaLaunchKernelEx(&cfg, rmsnorm_f16_kernel<2>, Y, ld_y, K, eps, X);
     else if (ch <= 4)
-        rmsnorm_f16_kernel<4><<<M, 256, 0, s>>>(Y, ld_y, K, eps, X);
+        cudaLaunchKernelEx(&cfg, rmsnorm_f16_kernel<4>, Y, ld_y, K, eps, X);
     else
-        rmsnorm_f16_kernel<8><<<M, 256, 0, s>>>(Y, ld_y, K, eps, X);
+        cudaLaunchKernelEx(&cfg, rmsnorm_f16_kernel<8>, Y, ld_y, K, eps, X);
     set_dispatch("rmsnorm_f16 rows=%d K=%d ld=%d chunks/thread=%d", M, K, ld_y, ch <= 2 ? ch : (ch <= 4 ? 4 : 8));
 }
 
