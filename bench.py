@@ -419,7 +419,8 @@ def stack_config(extra=None):
     from synthetic import STACK_LAYERS, STACK_LINEARS
     cfg = {"workload": STACK_WORKLOAD, "M": 700, "group": 64, "rank": 32, "layers": STACK_LAYERS,
            "linears_per_layer": {n: [k, nn] for n, k, nn in STACK_LINEARS},
-           "glue": "fp32/fp64 RMSNorm (unit gain, eps 1e-6) of the columns the next linear reads"}
+           "glue": "RMSNorm (unit gain, eps 1e-6, fp64-defined) of the columns the next linear reads, fused into "
+                   "the next linear's activation kernel; the last output normalised by the glue kernel"}
     if extra:
         cfg.update(extra)
     return cfg
@@ -493,13 +494,17 @@ def run_stack(args, rank, world, local_rank):
         for i, L in enumerate(stack.layers):
             w4.w4a4_linear(L["ws"], L["packed"], L["cs"], L["b"], L["Y"], L["K"], L["r"], w4.KERNEL_AUTO, st)
 
-    def quant_only(st):
-        for L in stack.layers:
-            w4.w4a4_quantize_act(L["X"], L["packed"], L["ws"], L["r"], st)
+    def quant_only(st):  # the activation step of every linear (with the RMSNorm where it is fused)
+        for i, L in enumerate(stack.layers):
+            if stack.reads_previous_output(i):
+                w4.w4a4_quantize_act_rmsnorm(stack.layers[i - 1]["Y"], L["K"], L["packed"], L["ws"], L["r"], st)
+            else:
+                w4.w4a4_quantize_act(L["X"], L["packed"], L["ws"], L["r"], st)
 
-    def glue_only(st):
+    def glue_only(st):  # the separate RMSNorm launches that remain
         for i in range(len(stack.layers)):
-            stack.run_glue(i, st)
+            if stack.has_glue(i):
+                stack.run_glue(i, st)
 
     stack.forward()
     torch.cuda.synchronize()

@@ -171,6 +171,16 @@ w4a4_status w4a4_linear_noalloc(const uint16_t* X, const void* packed, size_t pa
 #define W4A4_RMSNORM_EPS 1e-6
 w4a4_status w4a4_rmsnorm_f16(const uint16_t* Y, int M, int ld_y, int K, uint16_t* X, cudaStream_t stream);
 
+/* The glue and the next linear's activation step in one kernel: for each row
+ * m < M of Y (fp16, row stride ld_y elements), the first K columns are
+ * normalised exactly as w4a4_rmsnorm_f16 would write them (the same fp16
+ * bits) and then quantised and LoRA-down-projected exactly as
+ * w4a4_quantize_act would on those values.  The normalised fp16 values are
+ * not written out.  Arguments and limits as for w4a4_quantize_act (with X
+ * replaced by Y), plus ld_y >= K and ld_y % 8 == 0. */
+w4a4_status w4a4_quantize_act_rmsnorm(const uint16_t* Y, int ld_y, const void* packed, int M, int K, int r,
+                                      void* act_ws, size_t act_ws_bytes, cudaStream_t stream);
+
 /* ---- debug / validation entry points (small shapes; they synchronise `stream`)
  * Unpack the packed weights: codes int8 [N, K], scales fp16 [N, K/64],
  * L_down fp16 [K, r], L_up fp16 [r, N] (the last two may be NULL). */

@@ -86,6 +86,15 @@ def test_argument_checks_precede_any_launch(L):
     assert L.w4a4_rmsnorm_f16(_vp(0x10002), 64, 1024, 1024, A, None) == 3
     assert L.w4a4_rmsnorm_f16(A, 0, 1024, 1024, A, None) == 0     # M == 0: no-op
     assert L.w4a4_rmsnorm_f16(A, 4, 16392, 16392, A, None) == 2   # K > 16384
+    big = 1 << 40
+    assert L.w4a4_quantize_act_rmsnorm(A, 1000, A, 64, 1024, 32, A, big, None) == 1  # ld_y < K
+    assert L.w4a4_quantize_act_rmsnorm(A, 1028, A, 64, 1024, 32, A, big, None) == 2  # ld_y % 8 != 0
+    assert L.w4a4_quantize_act_rmsnorm(A, 1024, A, 64, 1000, 32, A, big, None) == 2  # K % 64 != 0
+    assert L.w4a4_quantize_act_rmsnorm(A, 1024, A, 64, 1024, 24, A, big, None) == 2  # r % 16 != 0
+    assert L.w4a4_quantize_act_rmsnorm(A, 1024, None, 64, 1024, 32, A, big, None) == 1  # r > 0 needs L_down
+    assert L.w4a4_quantize_act_rmsnorm(_vp(0x10008), 1024, A, 64, 1024, 32, A, big, None) == 3
+    assert L.w4a4_quantize_act_rmsnorm(A, 1024, A, 64, 1024, 32, A, 16, None) == 4  # workspace too small
+    assert L.w4a4_quantize_act_rmsnorm(A, 1024, A, 0, 1024, 32, A, big, None) == 0  # M == 0: no-op
 
 
 @pytest.mark.skipif(torch.cuda.is_available(), reason="valid shapes would launch on a GPU box")

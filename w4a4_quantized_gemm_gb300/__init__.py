@@ -48,6 +48,7 @@ SIGNATURES = {
     "w4a4_linear_select": (I, [P, Z, P, Z, P, P, I, I, I, I, P, I, P]),
     "w4a4_linear_noalloc": (I, [P, P, Z, P, P, I, I, I, I, P, P]),
     "w4a4_rmsnorm_f16": (I, [P, I, I, I, P, P]),
+    "w4a4_quantize_act_rmsnorm": (I, [P, I, P, I, I, I, P, Z, P]),
     "w4a4_debug_unpack_weights": (I, [P, I, I, I, P, P, P, P, P]),
     "w4a4_debug_unpack_act": (I, [P, I, I, I, P, P, P, P, P]),
     "w4a4_debug_group_partials": (I, [P, P, I, I, I, I, I, P, P]),
@@ -130,6 +131,14 @@ def w4a4_quantize_act(X, packed, act_ws, r: int, stream=None):
     M, K = X.shape
     _check(lib().w4a4_quantize_act(_ptr(X), _ptr(packed), M, K, r, _ptr(act_ws), _nbytes(act_ws),
                                    _stream(stream)), "w4a4_quantize_act")
+
+
+def w4a4_quantize_act_rmsnorm(Y, K: int, packed, act_ws, r: int, stream=None):
+    """RMSNorm of the first K columns of each row of Y [M, ld], then the
+    activation step of the next linear on the normalised values."""
+    M, ld = Y.shape
+    _check(lib().w4a4_quantize_act_rmsnorm(_ptr(Y), ld, _ptr(packed), M, K, r, _ptr(act_ws), _nbytes(act_ws),
+                                           _stream(stream)), "w4a4_quantize_act_rmsnorm")
 
 
 def w4a4_linear(act_ws, packed, colscale, bias, Y, K: int, r: int, kernel: int = KERNEL_AUTO, stream=None):

@@ -199,6 +199,21 @@ w4a4_status w4a4_quantize_act(const uint16_t* X, const void* packed, int M, int 
                                stream);
 }
 
+w4a4_status w4a4_quantize_act_rmsnorm(const uint16_t* Y, int ld_y, const void* packed, int M, int K, int r,
+                                      void* act_ws, size_t act_ws_bytes, cudaStream_t stream) {
+    if (M < 0 || ld_y < K) return W4A4_ERR_INVALID_ARG;
+    w4a4_status st = check_kn(16, K, r);
+    if (st != W4A4_OK) return st;
+    if (ld_y % 8 != 0) return W4A4_ERR_UNSUPPORTED_SHAPE;
+    if (M == 0) return W4A4_OK;
+    if (!Y || !act_ws || (r > 0 && !packed)) return W4A4_ERR_INVALID_ARG;
+    if (!aligned16(Y) || !aligned16(act_ws) || (packed && !aligned16(packed))) return W4A4_ERR_MISALIGNED;
+    if (act_ws_bytes < act_layout(M, K, r).total) return W4A4_ERR_WORKSPACE;
+    if ((st = check_device()) != W4A4_OK) return st;
+    return launch_quantize_act_rmsnorm(Y, ld_y, static_cast<const uint8_t*>(packed), M, K, r,
+                                       static_cast<uint8_t*>(act_ws), stream);
+}
+
 static int pick_kernel(int M, int kernel) {
     if (kernel == W4A4_KERNEL_TC || kernel == W4A4_KERNEL_SMALLM) return kernel;
     return M <= w4a4_small_m_threshold() ? W4A4_KERNEL_SMALLM : W4A4_KERNEL_TC;

@@ -17,9 +17,18 @@
 //    recomputed with the IEEE division, so codes equal rint(fl(x / scale)).
 //    The check is branch-free per element; the warp takes the slow path only
 //    when one of its lanes flagged such an element.
+//  * Fused variant (NORM): the input is the previous linear's output, and the
+//    RMSNorm between the two linears ("W4A4 CUDA Kernel for Voice Clone", 3.9)
+//    is applied on the way in: every CTA first sums the squares of its 16 rows
+//    over all K columns (the rows are L2-resident after the producing GEMM;
+//    every CTA of a cluster sums in the same order, so all agree on the
+//    inverse RMS without exchanging it), then each group's values are
+//    normalised to fp16 -- the same bits as the glue kernel writes -- before
+//    they are quantised and fed to the LoRA down-projection.
 #include <cooperative_groups.h>
 
 #include "kernels.h"
+#include "norm.cuh"
 
 namespace cg = cooperative_groups;
 
@@ -47,11 +56,12 @@ __device__ __forceinline__ uint32_t cvt_e4m3x2(float lo, float hi) {
     return r;
 }
 
-template <int R>  // LoRA rank, multiple of 16 (0 = no LoRA branch)
-__global__ void __launch_bounds__(kWarps * 32) quantize_act_kernel(const uint16_t* __restrict__ X,
+template <int R, bool NORM>  // LoRA rank, multiple of 16 (0 = no LoRA branch); RMSNorm on the way in
+__global__ void __launch_bounds__(kWarps * 32) quantize_act_kernel(const uint16_t* __restrict__ X, int ld_x,
                                                                    const uint2* __restrict__ Ldp, int M,
                                                                    int K, uint8_t* __restrict__ ws) {
     extern __shared__ __align__(16) uint8_t qsm[];
+    __shared__ double ssq[kWarps][kRows], row_inv[kRows];
     pdl_wait();
     pdl_launch_dependents();
     uint16_t(*xs)[kRows * kXsStride] = reinterpret_cast<uint16_t(*)[kRows * kXsStride]>(qsm);
@@ -79,7 +89,35 @@ __global__ void __launch_bounds__(kWarps * 32) quantize_act_kernel(const uint16_
     for (int t = 0; t < (NT > 0 ? NT : 1); ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.f;
 
     uint16_t* xw = xs[warp];
-    const uint16_t* xrow = X + (size_t)m * K + qhalf * 32;
+    const uint16_t* xrow = X + (size_t)m * ld_x + qhalf * 32;
+    double inv = 1.0;
+    float inva = 1.f, invb = 0.f;
+    if constexpr (NORM) {
+        // sum of squares of row qrow over all K columns (this lane's half of each
+        // of the warp's groups, then the lane pair, then the 8 warps in order)
+        float hi = 0.f, lo = 0.f;
+        for (int g0 = warp; g0 < G; g0 += kWarps) {
+            uint4 v[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                v[i] = valid ? ldg_nc_v4(xrow + (size_t)g0 * kGroup + 8 * i) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) add_squares(v[i], hi, lo);
+        }
+        double ss = double(hi) + double(lo);
+        ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+        if (qhalf == 0) ssq[warp][qrow] = ss;
+        __syncthreads();
+        if (threadIdx.x < kRows) {
+            double t = 0.0;
+#pragma unroll
+            for (int w = 0; w < kWarps; ++w) t += ssq[w][threadIdx.x];
+            row_inv[threadIdx.x] = 1.0 / sqrt(t / double(K) + W4A4_RMSNORM_EPS);
+        }
+        __syncthreads();
+        inv = row_inv[qrow];
+        split_inv(inv, inva, invb);
+    }
     int g = g_begin + warp;
     uint4 xv[4];
 #pragma unroll
@@ -104,6 +142,10 @@ __global__ void __launch_bounds__(kWarps * 32) quantize_act_kernel(const uint16_
 #pragma unroll
         for (int i = 0; i < 4; ++i)
             nv[i] = (valid && gn < g_end) ? ldg_nc_v4(xrow + (size_t)gn * kGroup + 8 * i) : make_uint4(0, 0, 0, 0);
+        if constexpr (NORM) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) xv[i] = scale_to_f16(xv[i], inv, inva, invb);
+        }
         float x[32];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
@@ -253,8 +295,9 @@ __global__ void unpack_act_kernel(const uint8_t* __restrict__ ws, int M, int K, 
     }
 }
 
-template <int R>
-w4a4_status launch_q(const uint16_t* X, const uint8_t* packed, int M, int K, uint8_t* ws, cudaStream_t s) {
+template <int R, bool NORM>
+w4a4_status launch_q(const uint16_t* X, int ld_x, const uint8_t* packed, int M, int K, uint8_t* ws,
+                     cudaStream_t s) {
     const int G = K / kGroup;
     // split K over a (small) cluster: one group per warp where that takes at most
     // two CTAs, else about two groups per warp (larger clusters cost more in
@@ -272,7 +315,7 @@ w4a4_status launch_q(const uint16_t* X, const uint8_t* packed, int M, int K, uin
     cudaGetDevice(&dev);
     constexpr int smem = q_smem_bytes(R);
     if (dev >= 0 && dev < 64 && !attr_done[dev]) {
-        if (cudaFuncSetAttribute(quantize_act_kernel<R>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+        if (cudaFuncSetAttribute(quantize_act_kernel<R, NORM>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
             cudaSuccess)
             return W4A4_ERR_CUDA;
         attr_done[dev] = 1;
@@ -286,9 +329,10 @@ w4a4_status launch_q(const uint16_t* X, const uint8_t* packed, int M, int K, uin
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = add_pdl_attr(attr, 1);
-    const cudaError_t e = cudaLaunchKernelEx(&cfg, quantize_act_kernel<R>, X, reinterpret_cast<const uint2*>(packed),
-                                             M, K, ws);
-    set_dispatch("quantize_act rows/cluster=%d cluster=%d grid=%d rank=%d", kRows, CK, row_blocks * CK, R);
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, quantize_act_kernel<R, NORM>, X, ld_x,
+                                             reinterpret_cast<const uint2*>(packed), M, K, ws);
+    set_dispatch("quantize_act%s rows/cluster=%d cluster=%d grid=%d rank=%d", NORM ? " (RMSNorm fused)" : "", kRows, CK,
+                 row_blocks * CK, R);
     if (e != cudaSuccess) {
         cudaGetLastError();
         return W4A4_ERR_CUDA;
@@ -296,22 +340,33 @@ w4a4_status launch_q(const uint16_t* X, const uint8_t* packed, int M, int K, uin
     return launch_status();
 }
 
+template <bool NORM>
+w4a4_status launch_qr(const uint16_t* X, int ld_x, const uint8_t* packed, int M, int K, int r, uint8_t* ws,
+                      cudaStream_t s) {
+    switch (r) {
+        case 0: return launch_q<0, NORM>(X, ld_x, packed, M, K, ws, s);
+        case 16: return launch_q<16, NORM>(X, ld_x, packed, M, K, ws, s);
+        case 32: return launch_q<32, NORM>(X, ld_x, packed, M, K, ws, s);
+        case 48: return launch_q<48, NORM>(X, ld_x, packed, M, K, ws, s);
+        case 64: return launch_q<64, NORM>(X, ld_x, packed, M, K, ws, s);
+        case 80: return launch_q<80, NORM>(X, ld_x, packed, M, K, ws, s);
+        case 96: return launch_q<96, NORM>(X, ld_x, packed, M, K, ws, s);
+        case 112: return launch_q<112, NORM>(X, ld_x, packed, M, K, ws, s);
+        case 128: return launch_q<128, NORM>(X, ld_x, packed, M, K, ws, s);
+        default: return W4A4_ERR_UNSUPPORTED_SHAPE;
+    }
+}
+
 }  // namespace
 
 w4a4_status launch_quantize_act(const uint16_t* X, const uint8_t* packed, int M, int K, int r, uint8_t* ws,
                                 cudaStream_t s) {
-    switch (r) {
-        case 0: return launch_q<0>(X, packed, M, K, ws, s);
-        case 16: return launch_q<16>(X, packed, M, K, ws, s);
-        case 32: return launch_q<32>(X, packed, M, K, ws, s);
-        case 48: return launch_q<48>(X, packed, M, K, ws, s);
-        case 64: return launch_q<64>(X, packed, M, K, ws, s);
-        case 80: return launch_q<80>(X, packed, M, K, ws, s);
-        case 96: return launch_q<96>(X, packed, M, K, ws, s);
-        case 112: return launch_q<112>(X, packed, M, K, ws, s);
-        case 128: return launch_q<128>(X, packed, M, K, ws, s);
-        default: return W4A4_ERR_UNSUPPORTED_SHAPE;
-    }
+    return launch_qr<false>(X, K, packed, M, K, r, ws, s);
+}
+
+w4a4_status launch_quantize_act_rmsnorm(const uint16_t* Y, int ld_y, const uint8_t* packed, int M, int K, int r,
+                                        uint8_t* ws, cudaStream_t s) {
+    return launch_qr<true>(Y, ld_y, packed, M, K, r, ws, s);
 }
 
 void launch_unpack_act(const uint8_t* ws, int M, int K, int r, int8_t* codes, float* sA, float* SA, float* lora,

@@ -15,70 +15,19 @@
 //  * the sum is an error-free two-term fp32 accumulation (hi + lo, Knuth's
 //    two-sum), combined in fp64 per row: its error is ~2^-44 relative,
 //    far below what could move an fp16 result;
-//  * the product is formed in fp32 (within 2^-23 relative of the fp64 one);
-//    only where that lands within 2 fp32 ulps of a midpoint between two fp16
-//    numbers (or in the fp16 subnormal range) is it redone in fp64, so the
-//    rounding to fp16 is the one the fp64 product gets.
+//  * the product is formed in fp32; where it lands within 2 fp32 ulps of a
+//    midpoint between two fp16 numbers, an exact fp32 residual decides the
+//    side (norm.cuh), and only the fp16-subnormal results (and products within
+//    2^-44 of a midpoint) are redone in fp64, so the rounding to fp16 is the
+//    one the fp64 product gets.
 //
 // One CTA per row: each thread reads its 16-byte chunks once (coalesced), keeps
 // them in registers, and writes the normalised values.
 #include "kernels.h"
+#include "norm.cuh"
 
 namespace w4a4 {
 namespace {
-
-
-// Two-term (Knuth two-sum) accumulation of the exact fp32 squares of 8 fp16 values.
-__device__ __forceinline__ void add_squares(const uint4 v, float& hi, float& lo) {
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[j]));
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const float q = h ? __fmul_rn(f.y, f.y) : __fmul_rn(f.x, f.x);  // exact
-            const float s = __fadd_rn(hi, q);                                 // s + e == hi + q exactly
-            const float bp = __fsub_rn(s, hi);
-            const float e = __fadd_rn(__fsub_rn(hi, __fsub_rn(s, bp)), __fsub_rn(q, bp));
-            hi = s;
-            lo = __fadd_rn(lo, e);
-        }
-    }
-}
-
-// fp16(y * inv) for 8 values, rounded as the fp64 product would be.  The fp32
-// product is within one fp32 ulp of the fp64 one (inv rounded to fp32, then
-// the product rounded), so where it lies more than 2 ulps from a midpoint
-// between fp16 numbers both round alike; the few others are redone in fp64.
-__device__ __forceinline__ uint4 scale_to_f16(const uint4 v, double inv, float invf) {
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-    float y[8], t[8];
-    uint32_t flags = 0;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[j]));
-        y[2 * j] = f.x;
-        y[2 * j + 1] = f.y;
-    }
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        t[i] = __fmul_rn(y[i], invf);
-        // the 13 fp32 mantissa bits below fp16 precision: 0x1000 is a midpoint
-        const int low = int(__float_as_uint(t[i]) & 0x1FFFu) - 0x1000;
-        const bool near = (fabsf(t[i]) < 6.103515625e-05f && t[i] != 0.f) || (low >= -2 && low <= 2);
-        flags |= uint32_t(near) << i;
-    }
-    uint16_t h[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) h[i] = __half_as_ushort(__float2half_rn(t[i]));
-    if (__any_sync(0xffffffffu, flags != 0)) {
-#pragma unroll
-        for (int i = 0; i < 8; ++i)
-            if (flags & (1u << i)) h[i] = __half_as_ushort(__double2half(double(y[i]) * inv));
-    }
-    return make_uint4(uint32_t(h[0]) | (uint32_t(h[1]) << 16), uint32_t(h[2]) | (uint32_t(h[3]) << 16),
-                      uint32_t(h[4]) | (uint32_t(h[5]) << 16), uint32_t(h[6]) | (uint32_t(h[7]) << 16));
-}
 
 // One CTA of 256 threads per row; thread t holds chunks (c * 256 + t) of 8
 // values (c < CH) in registers between the two steps.  The fp64 partial sums
@@ -115,12 +64,13 @@ __global__ void __launch_bounds__(256) rmsnorm_f16_kernel(const uint16_t* __rest
     }
     __syncthreads();
     const double inv = row_inv;
-    const float invf = float(inv);
+    float inva, invb;
+    split_inv(inv, inva, invb);
 #pragma unroll
     for (int c = 0; c < CH; ++c) {
         if ((c * 256 + warp * 32) * 8 < K) {  // warp-uniform: the vote inside stays converged
             const int k = (c * 256 + tid) * 8;
-            const uint4 o = scale_to_f16(v[c], inv, invf);
+            const uint4 o = scale_to_f16(v[c], inv, inva, invb);
             if (k < K) *reinterpret_cast<uint4*>(xr + k) = o;
         }
     }
