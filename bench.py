@@ -641,6 +641,9 @@ def run_decode(args, rank, world, local_rank):
     cs = torch.from_numpy(base.colscale.view(np.float16).copy()).to(dev)
     b = torch.from_numpy(base.bias.view(np.float16).copy()).to(dev)
     wbytes = metrics.weight_bytes(base.N, base.K)
+    sampler = ClockSampler(local_rank)
+    sampler.__enter__()
+    e2e = None
     for s_ in SMALL_M_SWEEP:
         M = s_["M"]
         X = torch.from_numpy(base.X[:M].view(np.float16).copy()).to(dev)
@@ -674,6 +677,26 @@ def run_decode(args, rank, world, local_rank):
         uq = tm(gq)
         results[M] = {"gemm_us": us, "quantize_us": uq, "weight_gbs": wbytes / (us * 1e-6) / 1e9,
                       "frac_hbm": wbytes / (us * 1e-6) / 1e9 / hbm, "dispatch": disp}
+        if M == 32 and not args.no_e2e:
+            # end to end through the public API at the metric's binding M: pinned host X in, the two
+            # C-ABI calls per weight replica, Y back to pinned host, all in one graph
+            Xh = torch.empty((M, base.K), dtype=torch.float16).pin_memory()
+            Xh.copy_(X.cpu())
+            Yh = torch.empty((M, base.N), dtype=torch.float16).pin_memory()
+            ge = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(ge):
+                for p_ in packs:
+                    X.copy_(Xh, non_blocking=True)
+                    w4.w4a4_quantize_act(X, p_, ws, base.r, torch.cuda.current_stream())
+                    w4.w4a4_linear(ws, p_, cs, b, Y, base.K, base.r, w4.KERNEL_AUTO, torch.cuda.current_stream())
+                    Yh.copy_(Y, non_blocking=True)
+            torch.cuda.synchronize()
+            ue = tm(ge)
+            e2e = {"value": wbytes / (ue * 1e-6) / 1e9, "unit": "GB/s", "h2d_bytes_per_step": M * base.K * 2,
+                   "d2h_bytes_per_step": M * base.N * 2, "us_per_call": ue, "M": M,
+                   "how": "per call: H2D of X from pinned host, quantize + linear through the C-ABI, D2H of Y "
+                          "(CUDA graph over the weight replicas)"}
+    sampler.__exit__()
     low = min(v["weight_gbs"] for m, v in results.items() if m <= 32)
     m32 = results[32]
     print(json.dumps({
@@ -683,7 +706,7 @@ def run_decode(args, rank, world, local_rank):
         "data": "synthetic",
         "config": {"workload": "small_m_sweep_K4096_N4096", "group": 64, "rank": 32, "replicas": R,
                    "l2": f"{R} weight replicas, {R * wbytes / 2**20:.0f} MiB > L2", "per_M": results},
-        "gpu_launches": args.steps * R * len(results) * 2,
+        "gpu_launches": args.steps * R * len(results) * 2, "e2e": e2e, "clocks": sampler.summary(),
         "roofline": {"bound": "hbm", "achieved": low, "peak": hbm, "unit": "GB/s", "frac": low / hbm,
                      "traffic": None, "kernel": "w4a4_linear (small-M weight-streaming kernel)",
                      "peak_source": f"{hbm_src} HBM copy bandwidth",
