@@ -15,6 +15,8 @@ Status of the pins (tests/test_oracle_pins.py):
   * group_partials            -- pinned (brute force, all -8 = 4096, cancellation)
   * lora_down / linear        -- pinned (numpy fp64 matmul special cases:
                                  rank 0, zero weights, dequantised reference)
+  * w4a16                     -- pinned (one-hot rows, exact homogeneity, the W4A4
+                                 layer on exactly quantisable inputs, numpy matmul)
 """
 from __future__ import annotations
 
@@ -68,6 +70,7 @@ def _load():
         lib.oracle_lora_down.argtypes = [P, P, I, I, I, P]
         lib.oracle_linear_from_codes.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, P]
         lib.oracle_linear_sampled.argtypes = [P, P, P, P, P, P, I, I, I, I, P, P, I, P, P, P, P, P, P]
+        lib.oracle_w4a16_from_codes.argtypes = [P, P, P, P, P, P, P, I, I, I, I, P]
         _lib = lib
         return lib
 
@@ -199,6 +202,29 @@ def linear_sampled(X, W, L_down, L_up, colscale, bias, rows, cols) -> np.ndarray
     res = np.empty_like(out)
     res[order] = out
     return res
+
+
+def w4a16_from_codes(X, qW, sW, D, L_up, colscale, bias) -> np.ndarray:
+    """fp64 Y [M, N] of the W4A16 layer: fp16 X against the dequantised INT4 weights."""
+    X = _c(X, np.uint16)
+    qW = _c(qW, np.int8); sW = _c(sW, np.uint16)
+    M, K = X.shape
+    N = qW.shape[0]
+    D = _c(D, np.float64).reshape(M, -1)
+    r = D.shape[1]
+    Lup = _c(L_up, np.uint16).reshape(r, N) if r else np.zeros((0, N), np.uint16)
+    cs = _c(colscale, np.uint16)
+    b = np.zeros(N, np.uint16) if bias is None else _c(bias, np.uint16)
+    Y = np.empty((M, N), np.float64)
+    _load().oracle_w4a16_from_codes(_ptr(X), _ptr(qW), _ptr(sW), _ptr(D), _ptr(Lup), _ptr(cs), _ptr(b),
+                                    M, N, K, r, _ptr(Y))
+    return Y
+
+
+def w4a16_linear(X, W, L_down, L_up, colscale, bias) -> np.ndarray:
+    """fp64 Y [M, N] of the W4A16 layer from raw inputs (the same weight quantiser and LoRA)."""
+    qW, sW = quantize_weights(W)
+    return w4a16_from_codes(X, qW, sW, lora_down(X, L_down), L_up, colscale, bias)
 
 
 RMSNORM_EPS = 1e-6

@@ -252,3 +252,30 @@ void oracle_linear_sampled(const uint16_t* X, const float* W, const uint16_t* Ld
         out[i] = output_element(qa_buf, sa_buf, qw_buf, sw_buf, d_buf, Lup, n, N, K, r, cs[n], bias[n]);
     }
 }
+
+/* ---- W4A16: fp16 activations against the same INT4 weights -------------
+ * "INT4 Kernel Architecture, in depth", "W4A16 versus W4A4": the activations
+ * stay in fp16 and only the weights are 4-bit, dequantised per group:
+ *   Y[m,n] = colscale[n] * ( sum_k X[m,k] * qW[n,k] * sW[n,g(k)]
+ *                            + sum_j D[m,j] L_up[j,n] ) + bias[n]
+ * with the same weight quantiser, LoRA and column affine as the W4A4 layer.
+ * Every product X * q * s is exact in fp64 (11 + 4 + 11 significant bits). */
+void oracle_w4a16_from_codes(const uint16_t* X, const int8_t* qW, const uint16_t* sW, const double* D,
+                             const uint16_t* Lup, const uint16_t* cs, const uint16_t* bias, int64_t M,
+                             int64_t N, int64_t K, int64_t r, double* Y) {
+    int64_t G = K / OR_GROUP;
+    for (int64_t m = 0; m < M; ++m)
+        for (int64_t n = 0; n < N; ++n) {
+            double main_sum = 0.0;
+            for (int64_t g = 0; g < G; ++g) {
+                double s = (double)oracle_f16_to_f32(sW[n * G + g]);
+                for (int k = 0; k < OR_GROUP; ++k) {
+                    int64_t kk = g * OR_GROUP + k;
+                    main_sum += (double)oracle_f16_to_f32(X[m * K + kk]) * (double)qW[n * K + kk] * s;
+                }
+            }
+            double lora = 0.0;
+            for (int64_t j = 0; j < r; ++j) lora += D[m * r + j] * (double)oracle_f16_to_f32(Lup[j * N + n]);
+            Y[m * N + n] = (double)oracle_f16_to_f32(cs[n]) * (main_sum + lora) + (double)oracle_f16_to_f32(bias[n]);
+        }
+}

@@ -301,3 +301,67 @@ def test_rmsnorm_invariants():
     assert ulps.max() <= 1 and (ulps > 0).mean() < 0.01
     xf = X.view(np.float16).astype(np.float64)
     assert np.all(np.abs((xf ** 2).mean(axis=1) - 1.0) < 2e-3)
+
+
+# --------------------------------------------------------------------- W4A16
+# "INT4 Kernel Architecture, in depth", "W4A16 versus W4A4": fp16 activations
+# against the same dequantised INT4 weights.
+def test_w4a16_one_hot_rows_read_single_weights():
+    """Row m of X is e_{k_m}: y[m, n] = cs (qW[n, k] sW[n, k/64] + L_down[k] . L_up[:, n]) + bias
+    -- one weight (and one LoRA row) per output, so a transposed or mis-grouped
+    index shows up directly."""
+    K, N, r = 256, 40, 16
+    c = make_linear_case(6, K, N, r, seed=21)
+    ks = np.array([0, 5, 63, 64, 130, 255])
+    X = np.zeros((len(ks), K), np.float16)
+    X[np.arange(len(ks)), ks] = 1.0
+    y = oracle.w4a16_linear(X.view(np.uint16), c.W, c.L_down, c.L_up, c.colscale, c.bias)
+    qW, sW = oracle.quantize_weights(c.W)
+    Ld = c.L_down.view(np.float16).astype(np.float64)
+    Lu = c.L_up.view(np.float16).astype(np.float64)
+    cs = c.colscale.view(np.float16).astype(np.float64)
+    b = c.bias.view(np.float16).astype(np.float64)
+    for i, k in enumerate(ks):
+        w = qW[:, k].astype(np.float64) * sW.view(np.float16)[:, k // G].astype(np.float64)
+        np.testing.assert_allclose(y[i], cs * (w + Ld[k] @ Lu) + b, rtol=1e-14, atol=1e-14)
+
+
+def test_w4a16_exact_homogeneity():
+    """No LoRA, unit colscale, zero bias: scaling X by 2 scales y by 2 exactly."""
+    c = make_linear_case(10, 192, 24, 0, seed=22)
+    one = np.full(24, 0x3C00, np.uint16)
+    zero = np.zeros(24, np.uint16)
+    X2 = (c.X.view(np.float16) * np.float16(2)).view(np.uint16)
+    y1 = oracle.w4a16_linear(c.X, c.W, None, None, one, zero)
+    y2 = oracle.w4a16_linear(X2, c.W, None, None, one, zero)
+    assert np.array_equal(y2, 2 * y1)
+
+
+def test_w4a16_equals_w4a4_on_exactly_quantisable_inputs():
+    """Activations that the W4A4 quantiser reproduces exactly (codes in [-7, 7]
+    with a +-7 in every group, power-of-two scales) give the same layer through
+    the integer-product path and through the W4A16 path."""
+    M, K, N, r = 7, 256, 33, 16
+    c = make_linear_case(M, K, N, r, seed=23)
+    rng = np.random.default_rng(23)
+    q = rng.integers(-7, 8, size=(M, K))
+    q[:, ::G] = 7
+    s = 2.0 ** rng.integers(-6, 2, size=(M, K // G))
+    X = (q * np.repeat(s, G, axis=1)).astype(np.float16)
+    assert np.array_equal(X.astype(np.float64), q * np.repeat(s, G, axis=1))
+    qa, sa = oracle.quantize_act(X.view(np.uint16))
+    assert np.array_equal(qa, q) and np.array_equal(sa.astype(np.float64), s)
+    y4 = oracle.linear(X.view(np.uint16), c.W, c.L_down, c.L_up, c.colscale, c.bias)
+    y16 = oracle.w4a16_linear(X.view(np.uint16), c.W, c.L_down, c.L_up, c.colscale, c.bias)
+    np.testing.assert_allclose(y16, y4, rtol=1e-13, atol=1e-13)
+
+
+def test_w4a16_matches_numpy_dequantised_matmul():
+    c = make_linear_case(12, 320, 28, 32, seed=24)
+    y = oracle.w4a16_linear(c.X, c.W, c.L_down, c.L_up, c.colscale, c.bias)
+    qW, sW = oracle.quantize_weights(c.W)
+    wh = (qW.astype(np.float64).reshape(28, -1, G) * sW.view(np.float16).astype(np.float64)[..., None]).reshape(28, 320)
+    X = c.X.view(np.float16).astype(np.float64)
+    lora = X @ c.L_down.view(np.float16).astype(np.float64) @ c.L_up.view(np.float16).astype(np.float64)
+    exp = c.colscale.view(np.float16).astype(np.float64) * (X @ wh.T + lora) + c.bias.view(np.float16).astype(np.float64)
+    np.testing.assert_allclose(y, exp, rtol=1e-12, atol=1e-12)
