@@ -673,10 +673,17 @@ def run_decode(args, rank, world, local_rank):
             e1.record()
             torch.cuda.synchronize()
             return e0.elapsed_time(e1) * 1e3 / (args.steps * R)
+        gw = torch.cuda.CUDAGraph()  # the W4A16 linear on the same weights: fp16 X straight in, one kernel
+        with torch.cuda.graph(gw):
+            for p_ in packs:
+                w4.w4a16_linear(X, p_, cs, b, Y, base.r, torch.cuda.current_stream())
+        torch.cuda.synchronize()
         us = tm(g)
         uq = tm(gq)
+        uw = tm(gw)
         results[M] = {"gemm_us": us, "quantize_us": uq, "weight_gbs": wbytes / (us * 1e-6) / 1e9,
-                      "frac_hbm": wbytes / (us * 1e-6) / 1e9 / hbm, "dispatch": disp}
+                      "frac_hbm": wbytes / (us * 1e-6) / 1e9 / hbm, "dispatch": disp,
+                      "w4a16_linear_us": uw, "w4a16_weight_gbs": wbytes / (uw * 1e-6) / 1e9}
         if M == 32 and not args.no_e2e:
             # end to end through the public API at the metric's binding M: pinned host X in, the two
             # C-ABI calls per weight replica, Y back to pinned host, all in one graph

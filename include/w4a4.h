@@ -181,6 +181,17 @@ w4a4_status w4a4_rmsnorm_f16(const uint16_t* Y, int M, int ld_y, int K, uint16_t
 w4a4_status w4a4_quantize_act_rmsnorm(const uint16_t* Y, int ld_y, const void* packed, int M, int K, int r,
                                       void* act_ws, size_t act_ws_bytes, cudaStream_t stream);
 
+/* ---- W4A16 linear ([INT4] "W4A16 versus W4A4": fp16 activations, the
+ * weights dequantised in registers), for the decode regime.  Same packed
+ * weights, LoRA and affine as w4a4_linear, no activation quantisation:
+ *   Y[m,n] = fp16_rn( colscale[n] * ( sum_g sW[n,g] sum_{k in g} X[m,k] c[n,k]
+ *                                     + (X L_down)[m,:] . L_up[:,n] ) + bias[n] )
+ * with the products accumulated in fp32.  X fp16 [M, K] row-major (16-byte
+ * aligned); no workspace.  Any M >= 0 is accepted (the kernel streams the
+ * weights once per block of up to 64 rows, so it is meant for small M). */
+w4a4_status w4a16_linear(const uint16_t* X, const void* packed, size_t packed_bytes, const uint16_t* colscale,
+                         const uint16_t* bias, int M, int N, int K, int r, uint16_t* Y, cudaStream_t stream);
+
 /* ---- debug / validation entry points (small shapes; they synchronise `stream`)
  * Unpack the packed weights: codes int8 [N, K], scales fp16 [N, K/64],
  * L_down fp16 [K, r], L_up fp16 [r, N] (the last two may be NULL). */

@@ -49,6 +49,7 @@ SIGNATURES = {
     "w4a4_linear_noalloc": (I, [P, P, Z, P, P, I, I, I, I, P, P]),
     "w4a4_rmsnorm_f16": (I, [P, I, I, I, P, P]),
     "w4a4_quantize_act_rmsnorm": (I, [P, I, P, I, I, I, P, Z, P]),
+    "w4a16_linear": (I, [P, P, Z, P, P, I, I, I, I, P, P]),
     "w4a4_debug_unpack_weights": (I, [P, I, I, I, P, P, P, P, P]),
     "w4a4_debug_unpack_act": (I, [P, I, I, I, P, P, P, P, P]),
     "w4a4_debug_group_partials": (I, [P, P, I, I, I, I, I, P, P]),
@@ -131,6 +132,14 @@ def w4a4_quantize_act(X, packed, act_ws, r: int, stream=None):
     M, K = X.shape
     _check(lib().w4a4_quantize_act(_ptr(X), _ptr(packed), M, K, r, _ptr(act_ws), _nbytes(act_ws),
                                    _stream(stream)), "w4a4_quantize_act")
+
+
+def w4a16_linear(X, packed, colscale, bias, Y, r: int, stream=None):
+    """W4A16 linear: fp16 X [M, K] against the packed INT4 weights -> Y [M, N]."""
+    M, K = X.shape
+    N = Y.shape[1]
+    _check(lib().w4a16_linear(_ptr(X), _ptr(packed), _nbytes(packed), _ptr(colscale), _ptr(bias), M, N, K, r, _ptr(Y),
+                              _stream(stream)), "w4a16_linear")
 
 
 def w4a4_quantize_act_rmsnorm(Y, K: int, packed, act_ws, r: int, stream=None):

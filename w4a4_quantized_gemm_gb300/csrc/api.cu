@@ -64,7 +64,8 @@ w4a4_status sync_status(cudaStream_t s) {
 w4a4_status device_status_words() {
     const w4a4_status a = tc_read_and_clear_status();
     const w4a4_status b = smallm_read_and_clear_status();
-    return a != W4A4_OK ? a : b;
+    const w4a4_status c = w4a16_read_and_clear_status();
+    return a != W4A4_OK ? a : b != W4A4_OK ? b : c;
 }
 }  // namespace
 
@@ -253,6 +254,20 @@ w4a4_status w4a4_linear(const void* act_ws, size_t act_ws_bytes, const void* pac
                         cudaStream_t stream) {
     return w4a4_linear_select(act_ws, act_ws_bytes, packed, packed_bytes, colscale, bias, M, N, K, r, Y,
                               W4A4_KERNEL_AUTO, stream);
+}
+
+w4a4_status w4a16_linear(const uint16_t* X, const void* packed, size_t packed_bytes, const uint16_t* colscale,
+                         const uint16_t* bias, int M, int N, int K, int r, uint16_t* Y, cudaStream_t stream) {
+    if (M < 0) return W4A4_ERR_INVALID_ARG;
+    w4a4_status st = check_kn(N, K, r);
+    if (st != W4A4_OK) return st;
+    if (M == 0) return W4A4_OK;
+    if (!X || !packed || !colscale || !Y) return W4A4_ERR_INVALID_ARG;
+    if (!aligned16(X) || !aligned16(packed) || !aligned16(colscale) || (bias && !aligned16(bias)) || !aligned16(Y))
+        return W4A4_ERR_MISALIGNED;
+    if (packed_bytes < packed_layout(N, K, r).total) return W4A4_ERR_WORKSPACE;
+    if ((st = check_device()) != W4A4_OK) return st;
+    return launch_gemm_w4a16(X, static_cast<const uint8_t*>(packed), colscale, bias, M, N, K, r, Y, stream);
 }
 
 w4a4_status w4a4_rmsnorm_f16(const uint16_t* Y, int M, int ld_y, int K, uint16_t* X, cudaStream_t stream) {

@@ -350,6 +350,12 @@ __device__ __forceinline__ uint64_t ffma2_b64(uint64_t a, uint64_t b, uint64_t c
     return d;
 }
 
+// d = a + b on both halves.
+__device__ __forceinline__ uint64_t fadd2_b64(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;\n" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
 // d = a * b on both halves.
 __device__ __forceinline__ uint64_t fmul2_b64(uint64_t a, uint64_t b) {
     uint64_t d;
