@@ -89,9 +89,12 @@ typedef enum {
 
 /* Kernel selection for w4a4_linear_select / w4a4_debug_group_partials. */
 typedef enum {
-    W4A4_KERNEL_AUTO = 0,   /* by M: small-M kernel for M <= threshold, else tensor-core tiles */
+    W4A4_KERNEL_AUTO = 0,   /* by M: M <= 8 the warp-MMA small-M kernel, M <= threshold the tcgen05
+                               small-M kernel, else tensor-core tiles */
     W4A4_KERNEL_TC = 1,     /* tcgen05 (TMEM accumulators, bulk-copy pipeline) */
-    W4A4_KERNEL_SMALLM = 2  /* weight-streaming kernel (warp-level MMA, split over K) */
+    W4A4_KERNEL_SMALLM = 2, /* weight-streaming kernel (warp-level MMA, split over K) */
+    W4A4_KERNEL_SMALLM_TC = 3 /* weight-streaming kernel on tcgen05 (weights as the 128-row operand, tokens
+                                 as N; split over K); no partials dump (w4a4_debug_group_partials refuses it) */
 } w4a4_kernel;
 
 /* ---- size queries (bytes of caller-allocated device buffers) ---- */

@@ -16,7 +16,8 @@ from tests.helpers import check_tol, pack, quantize, run_linear, to_dev
 pytestmark = pytest.mark.gpu
 
 KERNELS = [w4.KERNEL_SMALLM, w4.KERNEL_TC]
-KNAMES = {w4.KERNEL_SMALLM: "smallm", w4.KERNEL_TC: "tc"}
+YKERNELS = KERNELS + [w4.KERNEL_SMALLM_TC]  # (the tcgen05 small-M kernel has no partials dump)
+KNAMES = {w4.KERNEL_SMALLM: "smallm", w4.KERNEL_TC: "tc", w4.KERNEL_SMALLM_TC: "smallm_tc"}
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -144,7 +145,7 @@ SHAPES = [(1, 16, 64, 0), (5, 32, 128, 16), (16, 256, 256, 32), (37, 144, 192, 3
           (129, 272, 320, 32), (200, 512, 512, 64), (300, 128, 1024, 128)]
 
 
-@pytest.mark.parametrize("kernel", KERNELS, ids=lambda k: KNAMES[k])
+@pytest.mark.parametrize("kernel", YKERNELS, ids=lambda k: KNAMES[k])
 @pytest.mark.parametrize("M,N,K,r", SHAPES)
 def test_linear_within_tolerance(kernel, M, N, K, r):
     c = make_linear_case(M, K, N, r, seed=M + 3 * N + K)
@@ -156,7 +157,7 @@ def test_linear_within_tolerance(kernel, M, N, K, r):
     check_tol(Y, y, f"{KNAMES[kernel]} {M}x{N}x{K} r={r}")
 
 
-@pytest.mark.parametrize("kernel", KERNELS, ids=lambda k: KNAMES[k])
+@pytest.mark.parametrize("kernel", YKERNELS, ids=lambda k: KNAMES[k])
 def test_zero_input_gives_bias_exactly(kernel):
     c = make_linear_case(20, 256, 64, 32, seed=5)
     c.X = np.zeros_like(c.X)
@@ -167,7 +168,7 @@ def test_zero_input_gives_bias_exactly(kernel):
     assert np.array_equal(Y, np.broadcast_to(c.bias, Y.shape))
 
 
-@pytest.mark.parametrize("kernel", KERNELS, ids=lambda k: KNAMES[k])
+@pytest.mark.parametrize("kernel", YKERNELS, ids=lambda k: KNAMES[k])
 def test_no_bias_and_determinism(kernel):
     c = make_linear_case(70, 256, 96, 32, seed=8)
     t = to_dev(c)
@@ -192,7 +193,7 @@ def test_m_zero_is_noop():
     w4.w4a4_linear(ws, packed, t["colscale"], t["bias"], Y, 128, 16)
 
 
-@pytest.mark.parametrize("kernel", KERNELS, ids=lambda k: KNAMES[k])
+@pytest.mark.parametrize("kernel", YKERNELS, ids=lambda k: KNAMES[k])
 def test_output_guard_regions_untouched(kernel):
     """Y written only inside [M, N]: canaries before/after the buffer and the
     columns of a wider row stride stay intact (stand-in for a memory checker)."""
@@ -246,4 +247,21 @@ def test_smallm_split_k_cluster(M, N, K, r):
     assert f"split-K={ks} " in w4.w4a4_last_dispatch(), w4.w4a4_last_dispatch()
     y = oracle.linear(c.X, c.W, c.L_down, c.L_up, c.colscale, c.bias)
     check_tol(Y, y, f"smallm split {M}x{N}x{K} r={r}")
+    assert w4.w4a4_device_status() == 0
+
+
+# The tcgen05 small-M kernel on the split shapes above, every token-block size
+# (16, 32, 64), ragged column tiles, ranks 0..128, more rows than one block.
+@pytest.mark.parametrize("M,N,K,r", [(3, 400, 832, 32), (40, 144, 448, 16), (2, 48, 4480, 32), (1, 12800, 1280, 32),
+                                     (12, 1024, 4096, 64), (32, 4096, 4096, 32), (64, 1024, 1024, 128),
+                                     (70, 96, 256, 32), (17, 272, 320, 0)])
+def test_smallm_tc_matches_oracle(M, N, K, r):
+    c = make_linear_case(M, K, N, r, seed=M + 2 * N + K)
+    t = to_dev(c)
+    packed = pack(c, t)
+    ws = quantize(c, t, packed)
+    Y = run_linear(c, t, packed, ws, w4.KERNEL_SMALLM_TC)
+    assert "gemm_smallm_tc" in w4.w4a4_last_dispatch(), w4.w4a4_last_dispatch()
+    y = oracle.linear(c.X, c.W, c.L_down, c.L_up, c.colscale, c.bias)
+    check_tol(Y, y, f"smallm_tc {M}x{N}x{K} r={r}")
     assert w4.w4a4_device_status() == 0

@@ -14,6 +14,7 @@ namespace w4a4 {
 namespace {
 thread_local char t_dispatch[256] = "none";
 int g_small_m_threshold = -1;  // -1: read W4A4_SMALL_M on first use
+constexpr int kWarpMmaMaxM = 8;     // M <= this -> the warp-MMA weight-streaming kernel
 constexpr int kDefaultSmallM = 32;  // M <= this -> weight-streaming kernel, else tcgen05 tiles (measured crossover: 32..48)
 std::mutex g_mu;
 int g_sm_count[64] = {0};
@@ -65,7 +66,8 @@ w4a4_status device_status_words() {
     const w4a4_status a = tc_read_and_clear_status();
     const w4a4_status b = smallm_read_and_clear_status();
     const w4a4_status c = w4a16_read_and_clear_status();
-    return a != W4A4_OK ? a : b != W4A4_OK ? b : c;
+    const w4a4_status d = smtc_read_and_clear_status();
+    return a != W4A4_OK ? a : b != W4A4_OK ? b : c != W4A4_OK ? c : d;
 }
 }  // namespace
 
@@ -215,9 +217,13 @@ w4a4_status w4a4_quantize_act_rmsnorm(const uint16_t* Y, int ld_y, const void* p
                                        static_cast<uint8_t*>(act_ws), stream);
 }
 
+// AUTO: up to 8 rows the warp-MMA weight-streaming kernel, up to the small-M
+// threshold the tcgen05 weight-streaming kernel, above it the tcgen05 tiles
+// (measured crossovers on the decoder-layer and K = N = 4096 shapes).
 static int pick_kernel(int M, int kernel) {
-    if (kernel == W4A4_KERNEL_TC || kernel == W4A4_KERNEL_SMALLM) return kernel;
-    return M <= w4a4_small_m_threshold() ? W4A4_KERNEL_SMALLM : W4A4_KERNEL_TC;
+    if (kernel == W4A4_KERNEL_TC || kernel == W4A4_KERNEL_SMALLM || kernel == W4A4_KERNEL_SMALLM_TC) return kernel;
+    if (M > w4a4_small_m_threshold()) return W4A4_KERNEL_TC;
+    return M <= kWarpMmaMaxM ? W4A4_KERNEL_SMALLM : W4A4_KERNEL_SMALLM_TC;
 }
 
 static w4a4_status linear_checks(const void* act_ws, size_t act_ws_bytes, const void* packed, size_t packed_bytes,
@@ -239,13 +245,14 @@ static w4a4_status linear_checks(const void* act_ws, size_t act_ws_bytes, const 
 w4a4_status w4a4_linear_select(const void* act_ws, size_t act_ws_bytes, const void* packed, size_t packed_bytes,
                                const uint16_t* colscale, const uint16_t* bias, int M, int N, int K, int r,
                                uint16_t* Y, int kernel, cudaStream_t stream) {
-    if (kernel < W4A4_KERNEL_AUTO || kernel > W4A4_KERNEL_SMALLM) return W4A4_ERR_INVALID_ARG;
+    if (kernel < W4A4_KERNEL_AUTO || kernel > W4A4_KERNEL_SMALLM_TC) return W4A4_ERR_INVALID_ARG;
     w4a4_status st = linear_checks(act_ws, act_ws_bytes, packed, packed_bytes, colscale, bias, M, N, K, r, Y);
     if (st != W4A4_OK || M == 0) return st;
     const uint8_t* ws = static_cast<const uint8_t*>(act_ws);
     const uint8_t* pk = static_cast<const uint8_t*>(packed);
-    if (pick_kernel(M, kernel) == W4A4_KERNEL_TC)
-        return launch_gemm_tc(ws, pk, colscale, bias, M, N, K, r, Y, nullptr, stream);
+    const int k = pick_kernel(M, kernel);
+    if (k == W4A4_KERNEL_TC) return launch_gemm_tc(ws, pk, colscale, bias, M, N, K, r, Y, nullptr, stream);
+    if (k == W4A4_KERNEL_SMALLM_TC) return launch_gemm_smallm_tc(ws, pk, colscale, bias, M, N, K, r, Y, stream);
     return launch_gemm_smallm(ws, pk, colscale, bias, M, N, K, r, Y, nullptr, stream);
 }
 
@@ -313,6 +320,7 @@ w4a4_status w4a4_debug_group_partials(const void* act_ws, const void* packed, in
     if (st != W4A4_OK) return st;
     if (M == 0) return W4A4_OK;
     if (!act_ws || !packed || !P) return W4A4_ERR_INVALID_ARG;
+    if (kernel == W4A4_KERNEL_SMALLM_TC) return W4A4_ERR_UNSUPPORTED_SHAPE;  // (no partials dump)
     if (!aligned16(act_ws) || !aligned16(packed)) return W4A4_ERR_MISALIGNED;
     if ((st = check_device()) != W4A4_OK) return st;
     const uint8_t* ws = static_cast<const uint8_t*>(act_ws);

@@ -165,4 +165,5 @@ unsigned add_pdl_attr(cudaLaunchAttribute* attrs, unsigned n);
 w4a4_status tc_read_and_clear_status();      // bounded-wait status of the tcgen05 kernel
 w4a4_status smallm_read_and_clear_status();  // bounded-wait status of the small-M kernel
 w4a4_status w4a16_read_and_clear_status();   // bounded-wait status of the W4A16 kernel
+w4a4_status smtc_read_and_clear_status();    // bounded-wait status of the tcgen05 small-M kernel
 }  // namespace w4a4

@@ -32,6 +32,8 @@ w4a4_status launch_gemm_tc(const uint8_t* ws, const uint8_t* packed, const uint1
 // rmsnorm.cu (stack glue between linears)
 w4a4_status launch_quantize_act_rmsnorm(const uint16_t* Y, int ld_y, const uint8_t* packed, int M, int K, int r,
                                         uint8_t* ws, cudaStream_t s);
+w4a4_status launch_gemm_smallm_tc(const uint8_t* ws, const uint8_t* packed, const uint16_t* colscale,
+                                  const uint16_t* bias, int M, int N, int K, int r, uint16_t* Y, cudaStream_t s);
 w4a4_status launch_gemm_w4a16(const uint16_t* X, const uint8_t* packed, const uint16_t* colscale,
                               const uint16_t* bias, int M, int N, int K, int r, uint16_t* Y, cudaStream_t s);
 void launch_rmsnorm_f16(const uint16_t* Y, int M, int ld_y, int K, double eps, uint16_t* X, cudaStream_t s);
