@@ -17,6 +17,10 @@ Status of the pins (tests/test_oracle_pins.py):
                                  rank 0, zero weights, dequantised reference)
   * w4a16                     -- pinned (one-hot rows, exact homogeneity, the W4A4
                                  layer on exactly quantisable inputs, numpy matmul)
+  * quantize_weights_asym /   -- pinned (exactly representable groups: codes, scale,
+    w4a16_asym                   zero and values recovered; code range and the
+                                 half-step bound; the layer on such weights equals
+                                 a numpy fp64 matmul; one-hot rows)
 """
 from __future__ import annotations
 
@@ -71,6 +75,8 @@ def _load():
         lib.oracle_linear_from_codes.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, P]
         lib.oracle_linear_sampled.argtypes = [P, P, P, P, P, P, I, I, I, I, P, P, I, P, P, P, P, P, P]
         lib.oracle_w4a16_from_codes.argtypes = [P, P, P, P, P, P, P, I, I, I, I, P]
+        lib.oracle_quantize_weights_asym.argtypes = [P, I, I, P, P, P]
+        lib.oracle_w4a16_asym_from_codes.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, P]
         _lib = lib
         return lib
 
@@ -225,6 +231,44 @@ def w4a16_linear(X, W, L_down, L_up, colscale, bias) -> np.ndarray:
     """fp64 Y [M, N] of the W4A16 layer from raw inputs (the same weight quantiser and LoRA)."""
     qW, sW = quantize_weights(W)
     return w4a16_from_codes(X, qW, sW, lora_down(X, L_down), L_up, colscale, bias)
+
+
+GROUP_ASYM = 128
+
+
+def quantize_weights_asym(W: np.ndarray):
+    """W fp32 [N, K] -> (codes uint8 [N, K] in 0..15, scale fp16 bits [N, K/128],
+    zero fp16 bits [N, K/128]): asymmetric 4-bit with a zero point per group of 128."""
+    W = _c(W, np.float32)
+    N, K = W.shape
+    q = np.empty((N, K), np.uint8)
+    s = np.empty((N, K // GROUP_ASYM), np.uint16)
+    z = np.empty((N, K // GROUP_ASYM), np.uint16)
+    _load().oracle_quantize_weights_asym(_ptr(W), N, K, _ptr(q), _ptr(s), _ptr(z))
+    return q, s, z
+
+
+def w4a16_asym_from_codes(X, q, scale, zero, D, L_up, colscale, bias) -> np.ndarray:
+    """fp64 Y [M, N]: fp16 X against (q - zero) * scale, plus the LoRA and the column affine."""
+    X = _c(X, np.uint16)
+    q = _c(q, np.uint8); scale = _c(scale, np.uint16); zero = _c(zero, np.uint16)
+    M, K = X.shape
+    N = q.shape[0]
+    D = _c(D, np.float64).reshape(M, -1)
+    r = D.shape[1]
+    Lup = _c(L_up, np.uint16).reshape(r, N) if r else np.zeros((0, N), np.uint16)
+    cs = _c(colscale, np.uint16)
+    b = np.zeros(N, np.uint16) if bias is None else _c(bias, np.uint16)
+    Y = np.empty((M, N), np.float64)
+    _load().oracle_w4a16_asym_from_codes(_ptr(X), _ptr(q), _ptr(scale), _ptr(zero), _ptr(D), _ptr(Lup), _ptr(cs),
+                                         _ptr(b), M, N, K, r, _ptr(Y))
+    return Y
+
+
+def w4a16_asym_linear(X, W, L_down, L_up, colscale, bias) -> np.ndarray:
+    """fp64 Y [M, N] of the W4A16 layer with asymmetric group-128 weights, from raw inputs."""
+    q, s, z = quantize_weights_asym(W)
+    return w4a16_asym_from_codes(X, q, s, z, lora_down(X, L_down), L_up, colscale, bias)
 
 
 RMSNORM_EPS = 1e-6

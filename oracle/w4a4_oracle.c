@@ -279,3 +279,64 @@ void oracle_w4a16_from_codes(const uint16_t* X, const int8_t* qW, const uint16_t
             Y[m * N + n] = (double)oracle_f16_to_f32(cs[n]) * (main_sum + lora) + (double)oracle_f16_to_f32(bias[n]);
         }
 }
+
+/* ---- asymmetric 4-bit weights with a zero point, groups of 128 ---------
+ * "INT4 Kernel Architecture, in depth", "How the weights are stored": one fp16
+ * scale and one zero point per group of 128 input channels of an output row,
+ * codes 0..15, value = (q - zero) * scale.  Per row n and group g, in IEEE
+ * binary32 with round-to-nearest-even:
+ *   lo = min w, hi = max w;  scale = max(hi - lo, 1e-8) / 15;
+ *   zero = rint(-lo / scale);  q = clamp(rint(w / scale + zero), 0, 15);
+ * then scale is stored rounded to fp16 and zero as fp16 (exact: an integer).
+ * W fp32 [N, K]; q uint8 [N, K]; scale, zero fp16 bits [N, K/128].          */
+#define OR_GROUP_ASYM 128
+void oracle_quantize_weights_asym(const float* W, int64_t N, int64_t K, uint8_t* q, uint16_t* scale,
+                                  uint16_t* zero) {
+    int64_t G = K / OR_GROUP_ASYM;
+    for (int64_t n = 0; n < N; ++n)
+        for (int64_t g = 0; g < G; ++g) {
+            const float* w = W + n * K + g * OR_GROUP_ASYM;
+            float lo = w[0], hi = w[0];
+            for (int k = 1; k < OR_GROUP_ASYM; ++k) {
+                if (w[k] < lo) lo = w[k];
+                if (w[k] > hi) hi = w[k];
+            }
+            float range = hi - lo;
+            if (range < 1e-8f) range = 1e-8f;
+            const float s = range / 15.0f;
+            const float z = rintf(-lo / s);
+            for (int k = 0; k < OR_GROUP_ASYM; ++k) {
+                float v = rintf(w[k] / s + z);
+                if (v < 0.0f) v = 0.0f;
+                if (v > 15.0f) v = 15.0f;
+                q[n * K + g * OR_GROUP_ASYM + k] = (uint8_t)v;
+            }
+            scale[n * G + g] = oracle_f32_to_f16(s);
+            zero[n * G + g] = oracle_f32_to_f16(z);
+        }
+}
+
+/* W4A16 layer with those weights: fp16 X against (q - zero) * scale,
+ *   Y[m,n] = colscale[n] * ( sum_k X[m,k] (q[n,k] - zero[n,g(k)]) scale[n,g(k)]
+ *                            + sum_j D[m,j] L_up[j,n] ) + bias[n]
+ * in fp64 (each product exact: 11 + 12 + 11 significant bits).              */
+void oracle_w4a16_asym_from_codes(const uint16_t* X, const uint8_t* q, const uint16_t* scale, const uint16_t* zero,
+                                  const double* D, const uint16_t* Lup, const uint16_t* cs, const uint16_t* bias,
+                                  int64_t M, int64_t N, int64_t K, int64_t r, double* Y) {
+    int64_t G = K / OR_GROUP_ASYM;
+    for (int64_t m = 0; m < M; ++m)
+        for (int64_t n = 0; n < N; ++n) {
+            double main_sum = 0.0;
+            for (int64_t g = 0; g < G; ++g) {
+                double s = (double)oracle_f16_to_f32(scale[n * G + g]);
+                double z = (double)oracle_f16_to_f32(zero[n * G + g]);
+                for (int k = 0; k < OR_GROUP_ASYM; ++k) {
+                    int64_t kk = g * OR_GROUP_ASYM + k;
+                    main_sum += (double)oracle_f16_to_f32(X[m * K + kk]) * ((double)q[n * K + kk] - z) * s;
+                }
+            }
+            double lora = 0.0;
+            for (int64_t j = 0; j < r; ++j) lora += D[m * r + j] * (double)oracle_f16_to_f32(Lup[j * N + n]);
+            Y[m * N + n] = (double)oracle_f16_to_f32(cs[n]) * (main_sum + lora) + (double)oracle_f16_to_f32(bias[n]);
+        }
+}

@@ -365,3 +365,90 @@ def test_w4a16_matches_numpy_dequantised_matmul():
     lora = X @ c.L_down.view(np.float16).astype(np.float64) @ c.L_up.view(np.float16).astype(np.float64)
     exp = c.colscale.view(np.float16).astype(np.float64) * (X @ wh.T + lora) + c.bias.view(np.float16).astype(np.float64)
     np.testing.assert_allclose(y, exp, rtol=1e-12, atol=1e-12)
+
+
+# ---- asymmetric group-128 weights with a zero point ("INT4 Kernel
+# Architecture, in depth", "How the weights are stored")
+GA = 128
+
+
+def _exact_asym_weights(rng, N, K):
+    """Groups of integer multiples of s = 2^-e spanning exactly [-z s, (15 - z) s]:
+    scale, zero point and codes are then exact, and dequantisation gives W back."""
+    G = K // GA
+    e = rng.integers(5, 9, size=(N, G))
+    z = rng.integers(0, 16, size=(N, G))
+    s = np.ldexp(1.0, -e)
+    q = rng.integers(0, 16, size=(N, G, GA))
+    q[:, :, 0], q[:, :, 1] = 0, 15  # both ends present: hi - lo = 15 s
+    W = ((q - z[:, :, None]) * s[:, :, None]).reshape(N, K).astype(np.float32)
+    return W, q.reshape(N, K), s, z
+
+
+def test_asym_exact_groups_recover_codes_scale_zero_and_values():
+    rng = np.random.default_rng(31)
+    W, q, s, z = _exact_asym_weights(rng, 24, 512)
+    qo, so, zo = oracle.quantize_weights_asym(W)
+    assert np.array_equal(qo, q)
+    assert np.array_equal(so.view(np.float16).astype(np.float64), s)
+    assert np.array_equal(zo.view(np.float16).astype(np.float64), z)
+    deq = (qo.reshape(24, -1, GA) - z[:, :, None]) * s[:, :, None]
+    assert np.array_equal(deq.reshape(24, 512), W.astype(np.float64))
+
+
+def test_asym_codes_range_and_half_step_bound():
+    """Random groups (mixed signs, all-positive, all-negative): codes in 0..15,
+    the group's minimum takes code 0, its maximum 14 or 15, and every value is
+    within half a step of (q - zero) scale for the binary32 scale and zero."""
+    rng = np.random.default_rng(32)
+    N, K = 12, 1024
+    W = rng.normal(0, 0.02, (N, K)).astype(np.float32)
+    W[3] = np.abs(W[3]) + 1.0   # all positive: negative zero point
+    W[4] = -np.abs(W[4]) - 0.5  # all negative: zero point above 15
+    q, _, _ = oracle.quantize_weights_asym(W)
+    assert q.min() >= 0 and q.max() <= 15
+    g = W.reshape(N, -1, GA)
+    qg = q.reshape(N, -1, GA)
+    lo, hi = g.min(axis=2), g.max(axis=2)
+    s32 = (np.maximum(hi - lo, np.float32(1e-8)) / np.float32(15)).astype(np.float32)
+    z32 = np.rint(-lo / s32).astype(np.float32)
+    n_i, g_i = np.indices(lo.shape)
+    assert np.all(qg[n_i, g_i, g.argmin(axis=2)] == 0)
+    assert np.all(np.isin(qg[n_i, g_i, g.argmax(axis=2)], (14, 15)))
+    err = np.abs(g.astype(np.float64) - (qg - z32[:, :, None].astype(np.float64)) * s32[:, :, None])
+    assert np.all(err <= 0.5001 * s32[:, :, None])
+
+
+def test_w4a16_asym_on_exact_weights_equals_numpy_matmul():
+    """With exactly representable weights the layer is the textbook
+    colscale * (X W^T + X L_down L_up) + bias, in fp64 (numpy)."""
+    rng = np.random.default_rng(33)
+    M, N, K, r = 7, 40, 384, 16
+    W, _, _, _ = _exact_asym_weights(rng, N, K)
+    c = make_linear_case(M, K, N, r, seed=34)
+    y = oracle.w4a16_asym_linear(c.X, W, c.L_down, c.L_up, c.colscale, c.bias)
+    X = c.X.view(np.float16).astype(np.float64)
+    Ld = c.L_down.view(np.float16).astype(np.float64)
+    Lu = c.L_up.view(np.float16).astype(np.float64)
+    ref = c.colscale.view(np.float16).astype(np.float64) * (X @ W.astype(np.float64).T + (X @ Ld) @ Lu) \
+        + c.bias.view(np.float16).astype(np.float64)
+    np.testing.assert_allclose(y, ref, rtol=1e-12, atol=1e-12)
+
+
+def test_w4a16_asym_one_hot_rows_read_single_weights():
+    """Row i of X is e_k: y = cs ((q[n,k] - zero[n,k/128]) scale[n,k/128] + L_down[k] . L_up[:, n]) + bias."""
+    K, N, r = 512, 24, 16
+    c = make_linear_case(4, K, N, r, seed=35)
+    ks = np.array([0, 127, 128, 300, 511])
+    X = np.zeros((len(ks), K), np.float16)
+    X[np.arange(len(ks)), ks] = 1.0
+    y = oracle.w4a16_asym_linear(X.view(np.uint16), c.W, c.L_down, c.L_up, c.colscale, c.bias)
+    q, s, z = oracle.quantize_weights_asym(c.W)
+    sf, zf = s.view(np.float16).astype(np.float64), z.view(np.float16).astype(np.float64)
+    Ld = c.L_down.view(np.float16).astype(np.float64)
+    Lu = c.L_up.view(np.float16).astype(np.float64)
+    cs = c.colscale.view(np.float16).astype(np.float64)
+    b = c.bias.view(np.float16).astype(np.float64)
+    for i, k in enumerate(ks):
+        w = (q[:, k] - zf[:, k // GA]) * sf[:, k // GA]
+        np.testing.assert_allclose(y[i], cs * (w + Ld[k] @ Lu) + b, rtol=1e-14, atol=1e-14)
