@@ -1,6 +1,6 @@
 """Profiling driver: one W4A4 linear of the M=700 decoder layer, called in a loop.
 
-    python -m w4a4_quantized_gemm_gb300.profile_linear <qkv|o|gate_up|down|prefill_up|prefill_down|m1|m32> [iters]
+    python -m w4a4_quantized_gemm_gb300.profile_linear <qkv|o|gate_up|down|prefill_up|prefill_down|m1|m16|m32> [iters]
     python -m w4a4_quantized_gemm_gb300.profile_linear norm_gate_up [iters]
 
 The last form runs the stack's RMSNorm glue alone: the gate_up output
@@ -30,6 +30,7 @@ SHAPES.update({
     "prefill_up": dict(M=8192, K=4096, N=14336, r=32),
     "prefill_down": dict(M=8192, K=14336, N=4096, r=32),
     "m1": dict(M=1, K=4096, N=4096, r=32),
+    "m16": dict(M=16, K=4096, N=4096, r=32),
     "m32": dict(M=32, K=4096, N=4096, r=32),
 })
 
