@@ -287,7 +287,8 @@ void oracle_w4a16_from_codes(const uint16_t* X, const int8_t* qW, const uint16_t
  * binary32 with round-to-nearest-even:
  *   lo = min w, hi = max w;  scale = max(hi - lo, 1e-8) / 15;
  *   zero = rint(-lo / scale);  q = clamp(rint(w / scale + zero), 0, 15);
- * then scale is stored rounded to fp16 and zero as fp16 (exact: an integer).
+ * then scale is stored rounded to fp16 and zero as fp16 (exact: an integer;
+ * a zero point of 0 is stored as +0, whichever sign the rounding gave).
  * W fp32 [N, K]; q uint8 [N, K]; scale, zero fp16 bits [N, K/128].          */
 #define OR_GROUP_ASYM 128
 void oracle_quantize_weights_asym(const float* W, int64_t N, int64_t K, uint8_t* q, uint16_t* scale,
@@ -304,7 +305,7 @@ void oracle_quantize_weights_asym(const float* W, int64_t N, int64_t K, uint8_t*
             float range = hi - lo;
             if (range < 1e-8f) range = 1e-8f;
             const float s = range / 15.0f;
-            const float z = rintf(-lo / s);
+            const float z = rintf(-lo / s) + 0.0f; /* an integer; +0 rather than -0 when it is zero */
             for (int k = 0; k < OR_GROUP_ASYM; ++k) {
                 float v = rintf(w[k] / s + z);
                 if (v < 0.0f) v = 0.0f;

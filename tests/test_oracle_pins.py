@@ -452,3 +452,14 @@ def test_w4a16_asym_one_hot_rows_read_single_weights():
     for i, k in enumerate(ks):
         w = (q[:, k] - zf[:, k // GA]) * sf[:, k // GA]
         np.testing.assert_allclose(y[i], cs * (w + Ld[k] @ Lu) + b, rtol=1e-14, atol=1e-14)
+
+
+def test_asym_zero_point_of_zero_is_positive_zero():
+    """A group whose minimum is 0 (either sign) gets zero point +0 (fp16 bits 0x0000)."""
+    W = np.abs(np.random.default_rng(36).normal(0, 0.02, (2, 256))).astype(np.float32)
+    W[0, 5] = 0.0
+    W[1, 7] = -0.0
+    W[:, 128:] += 0.05  # second group: minimum well above 0, negative zero point
+    _, _, z = oracle.quantize_weights_asym(W)
+    assert z[0, 0] == 0 and z[1, 0] == 0
+    assert np.all(z[:, 1].view(np.float16) < 0)
