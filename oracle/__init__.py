@@ -21,6 +21,9 @@ Status of the pins (tests/test_oracle_pins.py):
     w4a16_asym                   zero and values recovered; code range and the
                                  half-step bound; the layer on such weights equals
                                  a numpy fp64 matmul; one-hot rows)
+  * silu_mul                  -- pinned (closed forms: silu(0) = 0, silu(ln 3) =
+                                 (3/4) ln 3, silu(v) -> v and -> 0 in the tails;
+                                 the gate/up column split on crafted rows)
 """
 from __future__ import annotations
 
@@ -76,6 +79,7 @@ def _load():
         lib.oracle_linear_sampled.argtypes = [P, P, P, P, P, P, I, I, I, I, P, P, I, P, P, P, P, P, P]
         lib.oracle_w4a16_from_codes.argtypes = [P, P, P, P, P, P, P, I, I, I, I, P]
         lib.oracle_quantize_weights_asym.argtypes = [P, I, I, P, P, P]
+        lib.oracle_silu_mul.argtypes = [P, I, I, P]
         lib.oracle_w4a16_asym_from_codes.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, P]
         _lib = lib
         return lib
@@ -269,6 +273,29 @@ def w4a16_asym_linear(X, W, L_down, L_up, colscale, bias) -> np.ndarray:
     """fp64 Y [M, N] of the W4A16 layer with asymmetric group-128 weights, from raw inputs."""
     q, s, z = quantize_weights_asym(W)
     return w4a16_asym_from_codes(X, q, s, z, lora_down(X, L_down), L_up, colscale, bias)
+
+
+def silu_mul(Y: np.ndarray) -> np.ndarray:
+    """fp64 H [M, I] = silu(Y[:, :I]) * Y[:, I:] for a fused gate|up output Y fp64 [M, 2I]."""
+    Y = _c(Y, np.float64)
+    M, N2 = Y.shape
+    H = np.empty((M, N2 // 2), np.float64)
+    _load().oracle_silu_mul(_ptr(Y), M, N2 // 2, _ptr(H))
+    return H
+
+
+def silu_mul_linear(X, W, L_down, L_up, colscale, bias) -> np.ndarray:
+    """fp64 H [M, N/2]: the W4A4 layer on a fused gate|up weight W [N, K] (gate rows
+    first), then silu(gate) * up."""
+    return silu_mul(linear(X, W, L_down, L_up, colscale, bias))
+
+
+def silu_mul_linear_sampled(X, W, L_down, L_up, colscale, bias, rows, cols) -> np.ndarray:
+    """fp64 H[rows[i], cols[i]] from raw inputs (the gate and up outputs of each pair sampled)."""
+    rows = np.asarray(rows, np.int64); cols = np.asarray(cols, np.int64)
+    I = np.asarray(W).shape[0] // 2
+    y = linear_sampled(X, W, L_down, L_up, colscale, bias, np.r_[rows, rows], np.r_[cols, cols + I])
+    return silu_mul(np.stack([y[: rows.size], y[rows.size:]], axis=1)).ravel()
 
 
 RMSNORM_EPS = 1e-6

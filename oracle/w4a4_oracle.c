@@ -341,3 +341,17 @@ void oracle_w4a16_asym_from_codes(const uint16_t* X, const uint8_t* q, const uin
             Y[m * N + n] = (double)oracle_f16_to_f32(cs[n]) * (main_sum + lora) + (double)oracle_f16_to_f32(bias[n]);
         }
 }
+
+/* ---- SiLU(gate) * up on a fused gate|up output ----------------------------
+ * "W4A4 CUDA Kernel for Voice Clone", 1 (the decoder layer's MLP: gate_proj
+ * and up_proj, then SiLU(gate) x up into down_proj).  Y fp64 [M, 2I] holds the
+ * gate outputs in columns 0..I-1 and the up outputs in I..2I-1;
+ *   H[m, j] = silu(Y[m, j]) * Y[m, I + j],   silu(v) = v / (1 + exp(-v)),
+ * in fp64.                                                                  */
+void oracle_silu_mul(const double* Y, int64_t M, int64_t I, double* H) {
+    for (int64_t m = 0; m < M; ++m)
+        for (int64_t j = 0; j < I; ++j) {
+            double g = Y[m * 2 * I + j], u = Y[m * 2 * I + I + j];
+            H[m * I + j] = g / (1.0 + exp(-g)) * u;
+        }
+}

@@ -463,3 +463,28 @@ def test_asym_zero_point_of_zero_is_positive_zero():
     _, _, z = oracle.quantize_weights_asym(W)
     assert z[0, 0] == 0 and z[1, 0] == 0
     assert np.all(z[:, 1].view(np.float16) < 0)
+
+
+# ---- SiLU(gate) * up on a fused gate|up output
+def test_silu_mul_closed_forms_and_column_split():
+    ln3 = np.log(3.0)
+    Y = np.array([[0.0, ln3, 40.0, -40.0, 5.0, 2.0, 1.0, 1.0],
+                  [1.0, 1.0, 1.0, 1.0, 0.0, ln3, 3.0, -2.0]])
+    H = oracle.silu_mul(Y)
+    assert H.shape == (2, 4)
+    # row 0: gates (0, ln 3, 40, -40) times ups (5, 2, 1, 1)
+    assert H[0, 0] == 0.0
+    assert abs(H[0, 1] - 2 * 0.75 * ln3) < 1e-15
+    assert abs(H[0, 2] - 40.0) < 1e-15             # silu(v) -> v for large v
+    assert 0 > H[0, 3] > -40 * np.exp(-39.9)        # -> 0 from below for large -v
+    # row 1: gates all 1 -> silu(1) = 1 / (1 + e^-1), times ups (0, ln 3, 3, -2)
+    s1 = 1.0 / (1.0 + np.exp(-1.0))
+    np.testing.assert_allclose(H[1], s1 * np.array([0.0, ln3, 3.0, -2.0]), rtol=1e-15)
+
+
+def test_silu_mul_sampled_matches_full():
+    c = make_linear_case(9, 128, 64, 16, seed=37)
+    H = oracle.silu_mul_linear(c.X, c.W, c.L_down, c.L_up, c.colscale, c.bias)
+    rows, cols = np.array([0, 3, 8, 8]), np.array([0, 31, 5, 31])
+    Hs = oracle.silu_mul_linear_sampled(c.X, c.W, c.L_down, c.L_up, c.colscale, c.bias, rows, cols)
+    assert np.array_equal(Hs, H[rows, cols])
