@@ -283,14 +283,14 @@ def run_ours(args, rank, world, local_rank):
 
     def timed(graphs, steps):
         for i in range(args.warmup):
-            graphs[i % R].replay()
+            graphs[i % len(graphs)].replay()
         torch.cuda.synchronize()
         if world > 1:
             dist.barrier()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record()
         for i in range(steps):
-            graphs[i % R].replay()
+            graphs[i % len(graphs)].replay()
         e1.record()
         torch.cuda.synchronize()
         return e0.elapsed_time(e1)
@@ -310,23 +310,31 @@ def run_ours(args, rank, world, local_rank):
     ms_per_step = ms / args.steps
     value = world * layer_ops() / (ms_per_step * 1e-3) / 1e12
 
-    # per-kernel durations: graphs holding only one kernel kind per linear
-    def one_kernel(name, kind):
-        def fn(rep, st):
-            d = L[name]
-            c = d["c"]
-            if kind == "q":
-                w4.w4a4_quantize_act(d["X"][rep], d["packed"][rep], d["ws"][rep], c.r, st)
-            else:
-                w4.w4a4_linear(d["ws"][rep], d["packed"][rep], d["cs"][rep], d["b"][rep], d["Y"][rep], c.K, c.r,
-                               w4.KERNEL_AUTO, st)
-        return fn
+    # per-kernel durations.  Per step: one graph per replica holding the step's
+    # four GEMMs (or four activation kernels), the same buffers as the step.
+    # Per linear: one graph holding that linear's kernel over all R replicas
+    # (per launch = graph time / R; the replicas of one linear may sit in L2).
+    def launch(name, kind, rep, st):
+        d = L[name]
+        c = d["c"]
+        if kind == "q":
+            w4.w4a4_quantize_act(d["X"][rep], d["packed"][rep], d["ws"][rep], c.r, st)
+        else:
+            w4.w4a4_linear(d["ws"][rep], d["packed"][rep], d["cs"][rep], d["b"][rep], d["Y"][rep], c.K, c.r,
+                           w4.KERNEL_AUTO, st)
+
+    def kind_step(kind):
+        return lambda rep, st: [launch(n, kind, rep, st) for n in names]
+
+    def one_linear(name, kind):
+        return lambda rep, st: [launch(name, kind, j, st) for j in range(R)]
 
     reps = max(args.steps, 2 * R)
-    q_us = {n: 1e3 * timed(capture(one_kernel(n, "q")), reps) / reps for n in names}
-    g_us = {n: 1e3 * timed(capture(one_kernel(n, "g")), reps) / reps for n in names}
-    gemm_s = sum(g_us.values()) * 1e-6
-    q_s = sum(q_us.values()) * 1e-6
+    q_s = timed(capture(kind_step("q")), reps) / reps * 1e-3
+    gemm_s = timed(capture(kind_step("g")), reps) / reps * 1e-3
+    lin_reps = max(4, reps // R)
+    q_us = {n: 1e3 * timed(capture(one_linear(n, "q"))[:1], lin_reps) / (lin_reps * R) for n in names}
+    g_us = {n: 1e3 * timed(capture(one_linear(n, "g"))[:1], lin_reps) / (lin_reps * R) for n in names}
     peaks = {}
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:

@@ -58,8 +58,17 @@
  *       SA = sum of the group's 64 codes (exact integer in fp32).
  *   next align256            La  [MT][r/16][128][32 bytes]: lora_act = X L_down
  *       rounded to fp16, row m, column j in plane j/16, same 32-byte swizzle.
+ *   next align256            flags [160][16] uint32: stream-K ready flags of the
+ *       tcgen05 GEMM, cleared by w4a4_quantize_act, left cleared by w4a4_linear.
+ *   next align256            (M >= 33 only, optional) stream-K hand-over area,
+ *       [160 CTAs][16 warps][8][32][4] fp32: partial sums of output tiles that
+ *       the GEMM splits between CTAs; written and read by w4a4_linear.
  *   Rows >= roundup(M, 16) of the workspace are never written and never
- *   influence Y.  total = w4a4_act_workspace_bytes(M, K, r)
+ *   influence Y.  w4a4_act_workspace_min_bytes(M, K, r) is the size up to and
+ *   including the flags (what every call needs); w4a4_act_workspace_bytes adds
+ *   the hand-over area.  A workspace without it runs the GEMM on its other
+ *   schedules.  Because w4a4_linear writes the flags and the hand-over area,
+ *   two calls that may overlap on the GPU must not share a workspace.
  */
 #ifndef W4A4_H_
 #define W4A4_H_
@@ -100,6 +109,7 @@ typedef enum {
 /* ---- size queries (bytes of caller-allocated device buffers) ---- */
 size_t w4a4_packed_weights_bytes(int N, int K, int r);
 size_t w4a4_act_workspace_bytes(int M, int K, int r);
+size_t w4a4_act_workspace_min_bytes(int M, int K, int r);
 
 /* ---- offline weight packing ([VC] 2.1-2.3, 3.10; [INT4] "How the weights are stored")
  * W      fp32 [N, K] row-major (nn.Linear out x in).
@@ -135,6 +145,27 @@ w4a4_status w4a4_quantize_act(const uint16_t* X, const void* packed, int M, int 
 w4a4_status w4a4_linear(const void* act_ws, size_t act_ws_bytes, const void* packed,
                         size_t packed_bytes, const uint16_t* colscale, const uint16_t* bias,
                         int M, int N, int K, int r, uint16_t* Y, cudaStream_t stream);
+
+/* ---- fused gate|up linear with the SiLU(gate) * up epilogue ([VC] 1: the
+ * decoder MLP's SiLU(gate_proj x) * up_proj x feeding down_proj).
+ * w4a4_pack_weights_gate_up packs W fp32 [N, K] whose rows 0..N/2-1 are the
+ * gate rows and N/2..N-1 the up rows (N % 32 == 0), like w4a4_pack_weights but
+ * with the rows (and the columns of L_up [r, N]) in the order the epilogue
+ * pairs them: packed row p of 128-row tile t = p / 128, 32-row slice
+ * s = (p % 128) / 32, w = p % 32 holds original row j = 64 t + 16 s + w % 16
+ * for w < 16 (a gate) and N/2 + j otherwise (its up).  Same buffer size; the
+ * debug unpack returns the rows in that packed order.
+ * w4a4_linear_silu_mul computes, with acc as in w4a4_linear (original row
+ * indices for colscale and bias, fp16 [N]):
+ *   g = colscale[j] acc[m, j] + bias[j],  u = colscale[N/2+j] acc[m, N/2+j] + bias[N/2+j]
+ *   H[m, j] = fp16_rn( g / (1 + exp(-g)) * u ),  H fp16 [M, N/2] row-major,
+ * in fp32 from the accumulators (no fp16 rounding of g and u).  It runs the
+ * tcgen05 tile kernel for every M.  Workspace as for w4a4_linear. */
+w4a4_status w4a4_pack_weights_gate_up(const float* W, const uint16_t* L_down, const uint16_t* L_up, int N, int K,
+                                      int r, void* packed, size_t packed_bytes, cudaStream_t stream);
+w4a4_status w4a4_linear_silu_mul(const void* act_ws, size_t act_ws_bytes, const void* packed, size_t packed_bytes,
+                                 const uint16_t* colscale, const uint16_t* bias, int M, int N, int K, int r,
+                                 uint16_t* H, cudaStream_t stream);
 
 /* Same as w4a4_linear with an explicit kernel choice (tests, measurements). */
 w4a4_status w4a4_linear_select(const void* act_ws, size_t act_ws_bytes, const void* packed,
@@ -195,6 +226,29 @@ w4a4_status w4a4_quantize_act_rmsnorm(const uint16_t* Y, int ld_y, const void* p
 w4a4_status w4a16_linear(const uint16_t* X, const void* packed, size_t packed_bytes, const uint16_t* colscale,
                          const uint16_t* bias, int M, int N, int K, int r, uint16_t* Y, cudaStream_t stream);
 
+/* ---- asymmetric group-128 weights ([INT4] "How the weights are stored": one
+ * fp16 scale and one zero point per group of 128 input channels, codes 0..15,
+ * value (q - zero) * scale).  K % 128 == 0.  Per row n and group g, in IEEE
+ * binary32 (round to nearest even):
+ *   scale = max(max w - min w, 1e-8) / 15;  zero = rint(-min w / scale) (+0 if 0);
+ *   q = clamp(rint(w / scale + zero), 0, 15);
+ * stored: fp16(scale), fp16(zero).  Same buffer size and sections as
+ * w4a4_pack_weights (packed_weights_bytes): the codes as plain nibbles q in
+ * the same record layout, the scale plane holding fp16(scale) in the slot of
+ * the group's first 64 channels and fp16(zero) in the slot of its second
+ * (w4a4_debug_unpack_weights then returns q - 8 and those two columns).  The
+ * buffer is read by w4a16_linear_asym only.  Synchronises `stream`; returns
+ * W4A4_ERR_INVALID_ARG, with the buffer written, when a zero point lies
+ * outside [-1024, 1023] (groups far from zero relative to their range). */
+w4a4_status w4a16_pack_weights_asym(const float* W, const uint16_t* L_down, const uint16_t* L_up, int N, int K,
+                                    int r, void* packed, size_t packed_bytes, cudaStream_t stream);
+/* W4A16 linear on those weights:
+ *   Y[m,n] = fp16_rn( colscale[n] * ( sum_k X[m,k] (q[n,k] - zero[n,g]) scale[n,g]
+ *                                     + (X L_down)[m,:] . L_up[:,n] ) + bias[n] )
+ * with the products accumulated in fp32; arguments as for w4a16_linear. */
+w4a4_status w4a16_linear_asym(const uint16_t* X, const void* packed, size_t packed_bytes, const uint16_t* colscale,
+                              const uint16_t* bias, int M, int N, int K, int r, uint16_t* Y, cudaStream_t stream);
+
 /* ---- debug / validation entry points (small shapes; they synchronise `stream`)
  * Unpack the packed weights: codes int8 [N, K], scales fp16 [N, K/64],
  * L_down fp16 [K, r], L_up fp16 [r, N] (the last two may be NULL). */
@@ -218,6 +272,13 @@ w4a4_status w4a4_device_status(void);
 const char* w4a4_status_string(int status);
 const char* w4a4_last_dispatch(void);       /* kernel and launch shape of this thread's last call */
 int w4a4_small_m_threshold(void);
+/* Whether the tcgen05 GEMM may split tiles between CTAs (stream-K schedule,
+ * used when the workspace holds the hand-over area and the schedule's cost
+ * model favours it).  Off by default (measured slower than the round-robin and
+ * split-K schedules on the decoder-layer shapes); W4A4_STREAM_K=1 turns it on
+ * at load. */
+int w4a4_stream_k(void);
+void w4a4_set_stream_k(int on);
 void w4a4_set_small_m_threshold(int m);     /* M <= threshold -> small-M kernel */
 int w4a4_layout_version(void);
 

@@ -23,7 +23,7 @@ def L():
 def declared_functions():
     src = open(HEADER).read()
     src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
-    return sorted(set(re.findall(r"\b(w4a4_[a-z0-9_]+)\s*\(", src)))
+    return sorted(set(re.findall(r"\b(w4a(?:4|16)_[a-z0-9_]+)\s*\(", src)))
 
 
 def test_header_declares_expected_entry_points():
@@ -46,8 +46,11 @@ def test_size_queries(L):
     exp = al(exp + 32 * 4096 * 2)
     assert w4.packed_weights_bytes(4096, 1024, 32) == exp
     MT = (700 + 127) // 128
-    ws = al(al(al(MT * G * 2 * 128 * 32) + MT * G * 128 * 8) + MT * 2 * 128 * 32)
-    assert w4.act_workspace_bytes(700, 1024, 32) == ws
+    ws = al(al(al(al(MT * G * 2 * 128 * 32) + MT * G * 128 * 8) + MT * 2 * 128 * 32) + 160 * 16 * 4)
+    assert w4.act_workspace_min_bytes(700, 1024, 32) == ws
+    # the tcgen05 GEMM's stream-K hand-over area: 160 CTAs x 16 warps x 4 KB, from M = 33 on
+    assert w4.act_workspace_bytes(700, 1024, 32) == ws + 160 * 16 * 4096
+    assert w4.act_workspace_bytes(32, 1024, 32) == w4.act_workspace_min_bytes(32, 1024, 32)
     assert L.w4a4_packed_weights_bytes(4096, 1000, 32) == 0   # K % 64
     assert L.w4a4_packed_weights_bytes(4100, 1024, 32) == 0   # N % 16
     assert L.w4a4_packed_weights_bytes(4096, 1024, 24) == 0   # r % 16

@@ -265,3 +265,44 @@ def test_smallm_tc_matches_oracle(M, N, K, r):
     y = oracle.linear(c.X, c.W, c.L_down, c.L_up, c.colscale, c.bias)
     check_tol(Y, y, f"smallm_tc {M}x{N}x{K} r={r}")
     assert w4.w4a4_device_status() == 0
+
+
+# The tcgen05 GEMM's stream-K schedule: every CTA takes an equal run of jobs,
+# tiles cut between CTAs are finished by the CTA holding their first job.
+# Shapes: the layer's qkv and o linears (tiles cut in two and three), a tile cut
+# between 32 CTAs (one job each), rank 128 (3-stage variant), a ragged M tail.
+@pytest.mark.parametrize("M,N,K,r", [(700, 4096, 1024, 32), (700, 1024, 2048, 32), (129, 256, 4096, 32),
+                                     (300, 512, 640, 128), (200, 144, 1024, 16)])
+def test_stream_k_matches_oracle(M, N, K, r):
+    was = w4.w4a4_stream_k()
+    w4.w4a4_set_stream_k(True)
+    try:
+        _stream_k_case(M, N, K, r)
+    finally:
+        w4.w4a4_set_stream_k(was)
+
+
+def _stream_k_case(M, N, K, r):
+    c = make_linear_case(M, K, N, r, seed=M + 5 * N + K)
+    t = to_dev(c)
+    packed = pack(c, t)
+    ws = quantize(c, t, packed)
+    Y = run_linear(c, t, packed, ws, w4.KERNEL_TC)
+    assert "stream-K" in w4.w4a4_last_dispatch(), w4.w4a4_last_dispatch()
+    assert w4.w4a4_device_status() == 0
+    # oracle on sampled rows (every column) for the large shapes
+    rows = np.arange(M) if M * N * K <= 200 * 2 ** 20 else np.unique(np.r_[0, 1, 127, 128, M - 1, np.arange(5, M, 97)])
+    rr, cc = np.repeat(rows, N), np.tile(np.arange(N), rows.size)
+    y = oracle.linear_sampled(c.X, c.W, c.L_down, c.L_up, c.colscale, c.bias, rr, cc).reshape(rows.size, N)
+    check_tol(Y.cpu()[rows], y, f"stream-K {M}x{N}x{K} r={r}")
+    # a second call on the same workspace finds the flags cleared: the same bits
+    Y2 = run_linear(c, t, packed, ws, w4.KERNEL_TC)
+    assert torch.equal(Y, Y2)
+    # without the hand-over area the GEMM takes another schedule, within tolerance too
+    ws_min = ws[: w4.act_workspace_min_bytes(M, K, r)]
+    Y3 = torch.full((M, N), float("nan"), dtype=torch.float16, device="cuda")
+    w4.w4a4_linear(ws_min, packed, t["colscale"], t["bias"], Y3, K, r, w4.KERNEL_TC)
+    torch.cuda.synchronize()
+    assert "stream-K" not in w4.w4a4_last_dispatch(), w4.w4a4_last_dispatch()
+    check_tol(Y3.cpu()[rows], y, f"round-robin {M}x{N}x{K} r={r}")
+    assert w4.w4a4_device_status() == 0

@@ -77,3 +77,59 @@ def test_w4a16_output_guard_regions_untouched():
     b = buf.cpu().numpy()
     assert np.all(b[:guard] == 0x5A5A) and np.all(b[guard + M * N:] == 0x5A5A)
     check_tol(Y, oracle.w4a16_linear(c.X, c.W, c.L_down, c.L_up, c.colscale, c.bias), "w4a16 guarded")
+
+
+# ---- asymmetric group-128 weights with a zero point ("INT4 Kernel Architecture,
+# in depth", "How the weights are stored")
+def _pack_asym(c, t):
+    packed = torch.empty(w4.packed_weights_bytes(c.N, c.K, c.r), dtype=torch.uint8, device="cuda")
+    w4.w4a16_pack_weights_asym(t["W"], t["L_down"], t["L_up"], packed, c.r)
+    return packed
+
+
+@pytest.mark.parametrize("N,K,r", [(16, 128, 0), (48, 384, 16), (4096, 1024, 32)])
+def test_pack_asym_bitexact(N, K, r):
+    """Codes, fp16 scales and fp16 zero points equal the oracle's bit for bit."""
+    c = make_linear_case(1, K, N, r, seed=N + 7 * K)
+    c.W[3 % N] = np.abs(c.W[3 % N]) + 0.05   # an all-positive row: negative zero points
+    t = to_dev(c)
+    packed = _pack_asym(c, t)
+    codes, planes, Ld, Lu = w4.w4a4_debug_unpack_weights(packed, N, K, r)
+    q, s, z = oracle.quantize_weights_asym(c.W)
+    assert np.array_equal(codes.cpu().numpy().astype(np.int16) + 8, q.astype(np.int16))
+    pl = planes.cpu().numpy().view(np.uint16)
+    assert np.array_equal(pl[:, 0::2], s)
+    assert np.array_equal(pl[:, 1::2], z)
+    if r:
+        assert np.array_equal(Ld.cpu().numpy().view(np.uint16), c.L_down)
+        assert np.array_equal(Lu.cpu().numpy().view(np.uint16), c.L_up)
+
+
+@pytest.mark.parametrize("M,N,K,r", [(1, 256, 1024, 32), (5, 48, 256, 16), (16, 400, 896, 32), (33, 144, 384, 0),
+                                     (64, 1024, 1024, 128), (1, 4096, 4096, 32), (32, 4096, 4096, 32)])
+def test_w4a16_asym_matches_oracle(M, N, K, r):
+    c = make_linear_case(M, K, N, r, seed=41 + M + N + K)
+    c.W[1] = np.abs(c.W[1]) + 0.05
+    t = to_dev(c)
+    packed = _pack_asym(c, t)
+    Y = torch.empty((M, N), dtype=torch.float16, device="cuda")
+    w4.w4a16_linear_asym(t["X"], packed, t["colscale"], t["bias"], Y, r)
+    torch.cuda.synchronize()
+    assert "asymmetric" in w4.w4a4_last_dispatch(), w4.w4a4_last_dispatch()
+    assert w4.w4a4_device_status() == 0
+    y = oracle.w4a16_asym_linear(c.X, c.W, c.L_down, c.L_up, c.colscale, c.bias)
+    check_tol(Y, y, f"w4a16 asym {M}x{N}x{K} r={r}")
+
+
+def test_asym_rejects_k_not_multiple_of_128_and_far_zero_points():
+    c = make_linear_case(2, 192, 32, 16, seed=3)
+    t = to_dev(c)
+    packed = torch.empty(w4.packed_weights_bytes(32, 192, 16), dtype=torch.uint8, device="cuda")
+    with pytest.raises(w4.W4A4Error):
+        w4.w4a16_pack_weights_asym(t["W"], t["L_down"], t["L_up"], packed, 16)
+    c = make_linear_case(2, 256, 32, 16, seed=4)
+    c.W[0] = 10.0 + np.linspace(0, 1e-3, 256, dtype=np.float32)  # zero point about -1.5e5
+    t = to_dev(c)
+    packed = torch.empty(w4.packed_weights_bytes(32, 256, 16), dtype=torch.uint8, device="cuda")
+    with pytest.raises(w4.W4A4Error):
+        w4.w4a16_pack_weights_asym(t["W"], t["L_down"], t["L_up"], packed, 16)

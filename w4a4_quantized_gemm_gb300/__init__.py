@@ -41,6 +41,7 @@ P, I, Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
 SIGNATURES = {
     "w4a4_packed_weights_bytes": (Z, [I, I, I]),
     "w4a4_act_workspace_bytes": (Z, [I, I, I]),
+    "w4a4_act_workspace_min_bytes": (Z, [I, I, I]),
     "w4a4_pack_weights": (I, [P, P, P, I, I, I, P, Z, P]),
     "w4a4_pack_weight_codes": (I, [P, P, P, P, I, I, I, P, Z, P]),
     "w4a4_quantize_act": (I, [P, P, I, I, I, P, Z, P]),
@@ -50,6 +51,10 @@ SIGNATURES = {
     "w4a4_rmsnorm_f16": (I, [P, I, I, I, P, P]),
     "w4a4_quantize_act_rmsnorm": (I, [P, I, P, I, I, I, P, Z, P]),
     "w4a16_linear": (I, [P, P, Z, P, P, I, I, I, I, P, P]),
+    "w4a16_pack_weights_asym": (I, [P, P, P, I, I, I, P, Z, P]),
+    "w4a4_pack_weights_gate_up": (I, [P, P, P, I, I, I, P, Z, P]),
+    "w4a4_linear_silu_mul": (I, [P, Z, P, Z, P, P, I, I, I, I, P, P]),
+    "w4a16_linear_asym": (I, [P, P, Z, P, P, I, I, I, I, P, P]),
     "w4a4_debug_unpack_weights": (I, [P, I, I, I, P, P, P, P, P]),
     "w4a4_debug_unpack_act": (I, [P, I, I, I, P, P, P, P, P]),
     "w4a4_debug_group_partials": (I, [P, P, I, I, I, I, I, P, P]),
@@ -57,6 +62,8 @@ SIGNATURES = {
     "w4a4_status_string": (ctypes.c_char_p, [I]),
     "w4a4_last_dispatch": (ctypes.c_char_p, []),
     "w4a4_small_m_threshold": (I, []),
+    "w4a4_stream_k": (I, []),
+    "w4a4_set_stream_k": (None, [I]),
     "w4a4_set_small_m_threshold": (None, [I]),
     "w4a4_layout_version": (I, []),
 }
@@ -115,6 +122,14 @@ def act_workspace_bytes(M: int, K: int, r: int) -> int:
     return n
 
 
+def act_workspace_min_bytes(M: int, K: int, r: int) -> int:
+    """Bytes every call needs (without the GEMM's optional stream-K hand-over area)."""
+    n = lib().w4a4_act_workspace_min_bytes(M, K, r)
+    if n == 0 and M > 0:
+        raise W4A4Error(2, "w4a4_act_workspace_min_bytes")
+    return n
+
+
 # ------------------------------------------------------------------ entry points
 def w4a4_pack_weights(W, L_down, L_up, packed, r: int, stream=None):
     N, K = W.shape
@@ -140,6 +155,35 @@ def w4a16_linear(X, packed, colscale, bias, Y, r: int, stream=None):
     N = Y.shape[1]
     _check(lib().w4a16_linear(_ptr(X), _ptr(packed), _nbytes(packed), _ptr(colscale), _ptr(bias), M, N, K, r, _ptr(Y),
                               _stream(stream)), "w4a16_linear")
+
+
+def w4a4_pack_weights_gate_up(W, L_down, L_up, packed, r: int, stream=None):
+    """Fused gate|up weights W [N, K] (gate rows first) packed for w4a4_linear_silu_mul."""
+    N, K = W.shape
+    _check(lib().w4a4_pack_weights_gate_up(_ptr(W), _ptr(L_down), _ptr(L_up), N, K, r, _ptr(packed),
+                                           _nbytes(packed), _stream(stream)), "w4a4_pack_weights_gate_up")
+
+
+def w4a4_linear_silu_mul(act_ws, packed, colscale, bias, H, K: int, r: int, stream=None):
+    """H [M, N/2] = silu(gate) * up of the fused gate|up W4A4 linear (colscale, bias [N])."""
+    M, I = H.shape
+    _check(lib().w4a4_linear_silu_mul(_ptr(act_ws), _nbytes(act_ws), _ptr(packed), _nbytes(packed), _ptr(colscale),
+                                      _ptr(bias), M, 2 * I, K, r, _ptr(H), _stream(stream)), "w4a4_linear_silu_mul")
+
+
+def w4a16_pack_weights_asym(W, L_down, L_up, packed, r: int, stream=None):
+    """Asymmetric group-128 INT4 weights (fp16 scale + zero point per group) into `packed`."""
+    N, K = W.shape
+    _check(lib().w4a16_pack_weights_asym(_ptr(W), _ptr(L_down), _ptr(L_up), N, K, r, _ptr(packed), _nbytes(packed),
+                                         _stream(stream)), "w4a16_pack_weights_asym")
+
+
+def w4a16_linear_asym(X, packed, colscale, bias, Y, r: int, stream=None):
+    """W4A16 linear on weights packed by w4a16_pack_weights_asym."""
+    M, K = X.shape
+    N = Y.shape[1]
+    _check(lib().w4a16_linear_asym(_ptr(X), _ptr(packed), _nbytes(packed), _ptr(colscale), _ptr(bias), M, N, K, r,
+                                   _ptr(Y), _stream(stream)), "w4a16_linear_asym")
 
 
 def w4a4_quantize_act_rmsnorm(Y, K: int, packed, act_ws, r: int, stream=None):
@@ -219,6 +263,14 @@ def w4a4_small_m_threshold() -> int:
 
 def w4a4_set_small_m_threshold(m: int):
     lib().w4a4_set_small_m_threshold(int(m))
+
+
+def w4a4_stream_k() -> bool:
+    return bool(lib().w4a4_stream_k())
+
+
+def w4a4_set_stream_k(on: bool):
+    lib().w4a4_set_stream_k(1 if on else 0)
 
 
 # ------------------------------------------------------------- layer helper

@@ -2,6 +2,7 @@
 // kernel dispatch by M, status mapping and the dispatch log ("INT4 Kernel
 // Architecture, in depth", "Failure modes": no silent fallback, log which
 // kernel each layer uses).
+#include <atomic>
 #include <cstdarg>
 #include <cstdio>
 #include <cstdlib>
@@ -15,6 +16,7 @@ namespace {
 thread_local char t_dispatch[256] = "none";
 int g_small_m_threshold = -1;  // -1: read W4A4_SMALL_M on first use
 constexpr int kWarpMmaMaxM = 8;     // M <= this -> the warp-MMA weight-streaming kernel
+constexpr int kStreamKDefault = 0;  // stream-K measured slower than split-K / round-robin on every layer shape
 constexpr int kDefaultSmallM = 32;  // M <= this -> weight-streaming kernel, else tcgen05 tiles (measured crossover: 32..48)
 std::mutex g_mu;
 int g_sm_count[64] = {0};
@@ -95,6 +97,19 @@ unsigned add_pdl_attr(cudaLaunchAttribute* attrs, unsigned n) {
     return n + 1;
 }
 
+// Stream-K schedule of the tcgen05 GEMM: W4A4_STREAM_K=1 / 0 sets the initial
+// state, w4a4_set_stream_k changes it.
+static std::atomic<int> g_stream_k{-1};
+bool tc_stream_k_enabled() {
+    int v = g_stream_k.load();
+    if (v < 0) {
+        const char* e = std::getenv("W4A4_STREAM_K");
+        v = (e && e[0] == '1') ? 1 : (e && e[0] == '0') ? 0 : kStreamKDefault;
+        g_stream_k.store(v);
+    }
+    return v != 0;
+}
+
 int device_sm_count() {
     int dev = 0;
     cudaGetDevice(&dev);
@@ -120,6 +135,11 @@ size_t w4a4_packed_weights_bytes(int N, int K, int r) {
 }
 
 size_t w4a4_act_workspace_bytes(int M, int K, int r) {
+    if (M < 0 || check_kn(16, K, r) != W4A4_OK) return 0;
+    return act_layout(M, K, r).full;
+}
+
+size_t w4a4_act_workspace_min_bytes(int M, int K, int r) {
     if (M < 0 || check_kn(16, K, r) != W4A4_OK) return 0;
     return act_layout(M, K, r).total;
 }
@@ -156,9 +176,13 @@ void w4a4_set_small_m_threshold(int m) {
     g_small_m_threshold = m < 0 ? 0 : m;
 }
 
+int w4a4_stream_k(void) { return tc_stream_k_enabled() ? 1 : 0; }
+
+void w4a4_set_stream_k(int on) { g_stream_k.store(on ? 1 : 0); }
+
 static w4a4_status pack_common(const float* W, const int8_t* codes, const uint16_t* scales, const uint16_t* L_down,
                                const uint16_t* L_up, int N, int K, int r, void* packed, size_t packed_bytes,
-                               cudaStream_t stream) {
+                               cudaStream_t stream, int silu_I = 0) {
     w4a4_status st = check_kn(N, K, r);
     if (st != W4A4_OK) return st;
     if (!packed || (!W && !(codes && scales))) return W4A4_ERR_INVALID_ARG;
@@ -168,10 +192,10 @@ static w4a4_status pack_common(const float* W, const int8_t* codes, const uint16
     if (packed_bytes < packed_layout(N, K, r).total) return W4A4_ERR_WORKSPACE;
     if ((st = check_device()) != W4A4_OK) return st;
     uint8_t* out = static_cast<uint8_t*>(packed);
-    launch_pack_weights(W, codes, scales, N, K, r, out, stream);
+    launch_pack_weights(W, codes, scales, N, K, r, silu_I, out, stream);
     if ((st = launch_status()) != W4A4_OK) return st;
-    launch_pack_lora(L_down, L_up, N, K, r, out, stream);
-    set_dispatch("pack_weights N=%d K=%d r=%d", N, K, r);
+    launch_pack_lora(L_down, L_up, N, K, r, silu_I, out, stream);
+    set_dispatch("pack_weights%s N=%d K=%d r=%d", silu_I ? " (gate|up order)" : "", N, K, r);
     return launch_status();
 }
 
@@ -179,6 +203,13 @@ w4a4_status w4a4_pack_weights(const float* W, const uint16_t* L_down, const uint
                               void* packed, size_t packed_bytes, cudaStream_t stream) {
     if (!W) return W4A4_ERR_INVALID_ARG;
     return pack_common(W, nullptr, nullptr, L_down, L_up, N, K, r, packed, packed_bytes, stream);
+}
+
+w4a4_status w4a4_pack_weights_gate_up(const float* W, const uint16_t* L_down, const uint16_t* L_up, int N, int K,
+                                      int r, void* packed, size_t packed_bytes, cudaStream_t stream) {
+    if (!W) return W4A4_ERR_INVALID_ARG;
+    if (N % 32 != 0) return W4A4_ERR_UNSUPPORTED_SHAPE;
+    return pack_common(W, nullptr, nullptr, L_down, L_up, N, K, r, packed, packed_bytes, stream, N / 2);
 }
 
 w4a4_status w4a4_pack_weight_codes(const int8_t* codes, const uint16_t* scales, const uint16_t* L_down,
@@ -251,8 +282,12 @@ w4a4_status w4a4_linear_select(const void* act_ws, size_t act_ws_bytes, const vo
     const uint8_t* ws = static_cast<const uint8_t*>(act_ws);
     const uint8_t* pk = static_cast<const uint8_t*>(packed);
     const int k = pick_kernel(M, kernel);
-    if (k == W4A4_KERNEL_TC) return launch_gemm_tc(ws, pk, colscale, bias, M, N, K, r, Y, nullptr, stream);
-    if (k == W4A4_KERNEL_SMALLM_TC) return launch_gemm_smallm_tc(ws, pk, colscale, bias, M, N, K, r, Y, stream);
+    if (k == W4A4_KERNEL_TC) {
+        const ActLayout AL = act_layout(M, K, r);
+        const bool sk_room = AL.full > AL.total && act_ws_bytes >= AL.full;
+        return launch_gemm_tc(ws, pk, colscale, bias, M, N, K, r, Y, nullptr, sk_room, 0, stream);
+    }
+    if (k == W4A4_KERNEL_SMALLM_TC) return launch_gemm_smallm_tc(ws, pk, colscale, bias, M, N, K, r, Y, 0, stream);
     return launch_gemm_smallm(ws, pk, colscale, bias, M, N, K, r, Y, nullptr, stream);
 }
 
@@ -261,6 +296,21 @@ w4a4_status w4a4_linear(const void* act_ws, size_t act_ws_bytes, const void* pac
                         cudaStream_t stream) {
     return w4a4_linear_select(act_ws, act_ws_bytes, packed, packed_bytes, colscale, bias, M, N, K, r, Y,
                               W4A4_KERNEL_AUTO, stream);
+}
+
+w4a4_status w4a4_linear_silu_mul(const void* act_ws, size_t act_ws_bytes, const void* packed, size_t packed_bytes,
+                                 const uint16_t* colscale, const uint16_t* bias, int M, int N, int K, int r,
+                                 uint16_t* H, cudaStream_t stream) {
+    if (N % 32 != 0) return W4A4_ERR_UNSUPPORTED_SHAPE;
+    w4a4_status st = linear_checks(act_ws, act_ws_bytes, packed, packed_bytes, colscale, bias, M, N, K, r, H);
+    if (st != W4A4_OK || M == 0) return st;
+    const uint8_t* ws = static_cast<const uint8_t*>(act_ws);
+    const uint8_t* pk = static_cast<const uint8_t*>(packed);
+    // up to the small-M threshold the tcgen05 weight-streaming kernel, above it the tiles
+    if (M <= w4a4_small_m_threshold()) return launch_gemm_smallm_tc(ws, pk, colscale, bias, M, N, K, r, H, N / 2, stream);
+    const ActLayout AL = act_layout(M, K, r);
+    const bool sk_room = AL.full > AL.total && act_ws_bytes >= AL.full;
+    return launch_gemm_tc(ws, pk, colscale, bias, M, N, K, r, H, nullptr, sk_room, N / 2, stream);
 }
 
 w4a4_status w4a16_linear(const uint16_t* X, const void* packed, size_t packed_bytes, const uint16_t* colscale,
@@ -274,7 +324,39 @@ w4a4_status w4a16_linear(const uint16_t* X, const void* packed, size_t packed_by
         return W4A4_ERR_MISALIGNED;
     if (packed_bytes < packed_layout(N, K, r).total) return W4A4_ERR_WORKSPACE;
     if ((st = check_device()) != W4A4_OK) return st;
-    return launch_gemm_w4a16(X, static_cast<const uint8_t*>(packed), colscale, bias, M, N, K, r, Y, stream);
+    return launch_gemm_w4a16(X, static_cast<const uint8_t*>(packed), colscale, bias, M, N, K, r, Y, false, stream);
+}
+
+w4a4_status w4a16_pack_weights_asym(const float* W, const uint16_t* L_down, const uint16_t* L_up, int N, int K,
+                                    int r, void* packed, size_t packed_bytes, cudaStream_t stream) {
+    w4a4_status st = check_kn(N, K, r);
+    if (st != W4A4_OK) return st;
+    if (K % 128 != 0) return W4A4_ERR_UNSUPPORTED_SHAPE;
+    if (!packed || !W || (r > 0 && (!L_down || !L_up))) return W4A4_ERR_INVALID_ARG;
+    if (!aligned16(packed) || !aligned16(W) || (L_down && !aligned16(L_down)) || (L_up && !aligned16(L_up)))
+        return W4A4_ERR_MISALIGNED;
+    if (packed_bytes < packed_layout(N, K, r).total) return W4A4_ERR_WORKSPACE;
+    if ((st = check_device()) != W4A4_OK) return st;
+    uint8_t* out = static_cast<uint8_t*>(packed);
+    launch_pack_lora(L_down, L_up, N, K, r, 0, out, stream);
+    if ((st = launch_status()) != W4A4_OK) return st;
+    set_dispatch("pack_weights_asym N=%d K=%d r=%d group=128", N, K, r);
+    return launch_pack_weights_asym(W, N, K, r, out, stream);
+}
+
+w4a4_status w4a16_linear_asym(const uint16_t* X, const void* packed, size_t packed_bytes, const uint16_t* colscale,
+                              const uint16_t* bias, int M, int N, int K, int r, uint16_t* Y, cudaStream_t stream) {
+    if (M < 0) return W4A4_ERR_INVALID_ARG;
+    w4a4_status st = check_kn(N, K, r);
+    if (st != W4A4_OK) return st;
+    if (K % 128 != 0) return W4A4_ERR_UNSUPPORTED_SHAPE;
+    if (M == 0) return W4A4_OK;
+    if (!X || !packed || !colscale || !Y) return W4A4_ERR_INVALID_ARG;
+    if (!aligned16(X) || !aligned16(packed) || !aligned16(colscale) || (bias && !aligned16(bias)) || !aligned16(Y))
+        return W4A4_ERR_MISALIGNED;
+    if (packed_bytes < packed_layout(N, K, r).total) return W4A4_ERR_WORKSPACE;
+    if ((st = check_device()) != W4A4_OK) return st;
+    return launch_gemm_w4a16(X, static_cast<const uint8_t*>(packed), colscale, bias, M, N, K, r, Y, true, stream);
 }
 
 w4a4_status w4a4_rmsnorm_f16(const uint16_t* Y, int M, int ld_y, int K, uint16_t* X, cudaStream_t stream) {
@@ -326,7 +408,7 @@ w4a4_status w4a4_debug_group_partials(const void* act_ws, const void* packed, in
     const uint8_t* ws = static_cast<const uint8_t*>(act_ws);
     const uint8_t* pk = static_cast<const uint8_t*>(packed);
     if (pick_kernel(M, kernel) == W4A4_KERNEL_TC)
-        st = launch_gemm_tc(ws, pk, nullptr, nullptr, M, N, K, r, nullptr, P, stream);
+        st = launch_gemm_tc(ws, pk, nullptr, nullptr, M, N, K, r, nullptr, P, false, 0, stream);
     else
         st = launch_gemm_smallm(ws, pk, nullptr, nullptr, M, N, K, r, nullptr, P, stream);
     if (st != W4A4_OK) return st;

@@ -32,8 +32,17 @@ __host__ __device__ inline PackedLayout packed_layout(int N, int K, int r) {
 }
 
 // Activation workspace sections (byte offsets).
+// Stream-K hand-over area of the tcgen05 GEMM: one 64 KB slot of fp32 partial
+// sums per CTA (16 epilogue warps x 4 KB) and one ready counter per (CTA, warp)
+// (32 once every lane of the warp has released its part).
+constexpr int kStreamKSlots = 160;      // CTAs of a stream-K launch at most
+constexpr int kStreamKWarps = 16;
+constexpr size_t kStreamKSlotBytes = size_t(kStreamKWarps) * 32 * 32 * 4;
+constexpr int kStreamKMinM = 33;        // the area is sized in for M >= this
+
 struct ActLayout {
-    size_t qA, sS, La, total;
+    size_t qA, sS, La, flags, total;  // total: what every call needs
+    size_t part, full;                // optional stream-K partial slots; full: with them
     int MT;
 };
 __host__ __device__ inline ActLayout act_layout(int M, int K, int r) {
@@ -43,8 +52,22 @@ __host__ __device__ inline ActLayout act_layout(int M, int K, int r) {
     L.qA = 0;
     L.sS = align256(size_t(L.MT) * G * 2 * kTileM * 32);
     L.La = align256(L.sS + size_t(L.MT) * G * kTileM * 8);
-    L.total = align256(L.La + size_t(L.MT) * size_t(r / 16) * kTileM * 32);
+    L.flags = align256(L.La + size_t(L.MT) * size_t(r / 16) * kTileM * 32);
+    L.total = align256(L.flags + size_t(kStreamKSlots) * kStreamKWarps * 4);
+    L.part = L.total;
+    L.full = M >= kStreamKMinM ? L.part + size_t(kStreamKSlots) * kStreamKSlotBytes : L.total;
     return L;
+}
+
+// Fused gate|up weights packed for the SiLU(gate) * up epilogue (I gate rows,
+// then I up rows; I % 16 == 0): in every 128-row tile t, each 32-row slice s
+// holds 16 gate rows and then the 16 up rows of the same outputs, so that one
+// epilogue thread finds both factors of an output among its 32 columns.
+// Original row of packed row p: j = 64 t + 16 s + p % 16, gate j or up I + j.
+__host__ __device__ inline int gate_up_row(int p, int I) {
+    const int t = p >> 7, s = (p >> 5) & 3, w = p & 31;
+    const int j = 64 * t + 16 * s + (w & 15);
+    return w < 16 ? j : I + j;
 }
 
 // Physical 16-byte chunk of logical chunk c (0/1) in 32-byte row `row` of a
@@ -162,6 +185,7 @@ int device_sm_count();        // multiprocessors of the current device (cached)
 // overlap the previous kernel in the stream, which its pdl_wait orders) unless
 // W4A4_PDL=0 is set in the environment; returns the new attribute count.
 unsigned add_pdl_attr(cudaLaunchAttribute* attrs, unsigned n);
+bool tc_stream_k_enabled();
 w4a4_status tc_read_and_clear_status();      // bounded-wait status of the tcgen05 kernel
 w4a4_status smallm_read_and_clear_status();  // bounded-wait status of the small-M kernel
 w4a4_status w4a16_read_and_clear_status();   // bounded-wait status of the W4A16 kernel

@@ -83,8 +83,6 @@ __global__ void __launch_bounds__(kWarps * 32) gemm_smallm_kernel(
     constexpr int NT = kWarps * 32;
     extern __shared__ __align__(128) uint8_t smraw[];
     __shared__ int abort_flag, never_abort;
-    pdl_wait();
-    pdl_launch_dependents();
     const SmallMPlan PLN = smallm_plan(TOK, r);
     const uint32_t sbase = smem_u32(smraw);
     const uint32_t full0 = sbase + PLN.bar;  // full[s] = full0 + 8 s
@@ -157,6 +155,17 @@ __global__ void __launch_bounds__(kWarps * 32) gemm_smallm_kernel(
     }
     __syncthreads();  // barriers initialised for this CTA's threads
     if (KS > 1 && !DUMP) cluster_arrive_release();  // ... and, once every rank has arrived, for the peers
+    // The setup above touches only shared memory and overlaps the previous kernel;
+    // so does warming L2 with this CTA's share of the weight records and scales
+    // (a prefetch only fills the cache; every copy proper comes after the wait).
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < n_groups; ++i) {
+            prefetch_l2(qW + ((size_t)(g_begin + i) * N + nbase) * 32, uint32_t(rows_valid) * 32);
+            prefetch_l2(sWg + ((size_t)(g_begin + i) * N + nbase) * 2, uint32_t(rows_valid) * 2);
+        }
+    }
+    pdl_wait();
+    pdl_launch_dependents();
     if (!DUMP) {
         // LoRA planes first (their barrier then completes with them alone): the
         // token block's activations, and the up-projection rows of the warps this rank owns

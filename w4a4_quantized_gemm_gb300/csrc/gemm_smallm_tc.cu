@@ -78,14 +78,12 @@ __host__ __device__ inline TcPlan tc_plan(int tokn, int r, int ks) {
 template <int TOKN>
 __global__ void __launch_bounds__(kThreads, 1) gemm_smallm_tc_kernel(
     const uint8_t* __restrict__ ws, const uint8_t* __restrict__ packed, const uint16_t* __restrict__ colscale,
-    const uint16_t* __restrict__ bias, int M, int N, int K, int r, uint16_t* __restrict__ Y, int KS) {
+    const uint16_t* __restrict__ bias, int M, int N, int K, int r, uint16_t* __restrict__ Y, int KS, int silu_I) {
     constexpr int BLK = TOKN / 4;  // 4-token blocks
     constexpr int kS = stages_for(TOKN);
     extern __shared__ uint8_t smdyn[];
     __shared__ uint32_t tmem_slot;
     __shared__ int abort_flag, never_abort;
-    pdl_wait();
-    pdl_launch_dependents();
     const TcPlan PLN = tc_plan(TOKN, r, KS);
     // the tensor core's operands want 1024-byte aligned planes: align the dynamic region by hand
     const uint32_t raw = smem_u32(smdyn);
@@ -142,6 +140,17 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_smallm_tc_kernel(
     tc_fence_after();
     const uint32_t tmem = tmem_slot;
     if (KS > 1) cluster_arrive_release();
+    // The setup above touches only this CTA's shared and tensor memory and overlaps
+    // the previous kernel; so does warming L2 with this CTA's share of the weight
+    // records and scales (a prefetch only fills the cache; the copies come after the wait).
+    if (warp == WARP_PROD && lane == 0) {
+        for (int i = 0; i < n_groups; ++i) {
+            prefetch_l2(packed + PL.qW + ((size_t)(g_begin + i) * N + nbase) * 32, uint32_t(rows_valid) * 32);
+            prefetch_l2(packed + PL.sW + ((size_t)(g_begin + i) * N + nbase) * 2, uint32_t(rows_valid) * 2);
+        }
+    }
+    pdl_wait();
+    pdl_launch_dependents();
     bool ok = true;
 
     if (warp == WARP_PROD) {
@@ -397,7 +406,30 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_smallm_tc_kernel(
     // ---- affine of the owned token blocks, staged as rows [token][128 + 8] over the weight planes
     uint16_t* ys = reinterpret_cast<uint16_t*>(smraw + PLN.wexp);
     constexpr int LDY = kRows + 8;
-    if (warp < 4 && !*abort) {
+    if (warp < 4 && !*abort && silu_I > 0) {
+        // fused gate|up weights (gate_up_row order): lanes 0..15 of warp w hold the gates
+        // of outputs j = 64 t + 16 w + lane, lanes 16..31 the matching ups; h = silu(g) u
+        // is staged as [token][64 + 8] at column 16 w + lane
+        const int j = (nbase >> 1) + 16 * warp + (lane & 15);
+        const bool gate = lane < 16, valid = j < silu_I;
+        const int src = gate ? j : silu_I + j;
+        const float cs = valid ? __half2float(__ushort_as_half(colscale[src])) : 0.f;
+        const float bs = (bias && valid) ? __half2float(__ushort_as_half(bias[src])) : 0.f;
+#pragma unroll
+        for (int b = 0; b < BLK; ++b) {
+            if (b % KS != kr) continue;
+            const float2 p0 = f2_unpack(acc[2 * b]), p1 = f2_unpack(acc[2 * b + 1]);
+            const float v[4] = {p0.x, p0.y, p1.x, p1.y};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float y = fmaf(cs, v[i], bs);
+                const float u = __shfl_down_sync(0xffffffffu, y, 16);
+                if (gate)  // silu(y) u, fast exponential and divide (relative error ~1e-6)
+                    ys[(4 * b + i) * LDY + 16 * warp + lane] =
+                        __half_as_ushort(__float2half_rn(__fdividef(y, 1.0f + __expf(-y)) * u));
+            }
+        }
+    } else if (warp < 4 && !*abort) {
         const int n = nbase + row;
         const float cs = n < N ? __half2float(__ushort_as_half(colscale[n])) : 0.f;
         const float bs = (bias && n < N) ? __half2float(__ushort_as_half(bias[n])) : 0.f;
@@ -412,7 +444,16 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_smallm_tc_kernel(
         }
     }
     __syncthreads();
-    if (!*abort) {
+    if (!*abort && silu_I > 0) {
+        for (int c = threadIdx.x; c < TOKN * (kRows / 16); c += kThreads) {
+            const int t = c / (kRows / 16), ch = c % (kRows / 16);
+            const int m = tok0 + t, j = (nbase >> 1) + ch * 8;
+            if ((t / 4) % KS != kr) continue;
+            if (m < M && j < silu_I)
+                *reinterpret_cast<uint4*>(Y + (size_t)m * silu_I + j) =
+                    *reinterpret_cast<const uint4*>(&ys[t * LDY + ch * 8]);
+        }
+    } else if (!*abort) {
         for (int c = threadIdx.x; c < TOKN * (kRows / 8); c += kThreads) {
             const int t = c / (kRows / 8), ch = c % (kRows / 8);
             const int m = tok0 + t, n = nbase + ch * 8;
@@ -437,7 +478,7 @@ int smtc_split(int M, int N, int K, int TOKN) {
 
 template <int TOKN>
 w4a4_status launch_t(const uint8_t* ws, const uint8_t* packed, const uint16_t* cs, const uint16_t* bias, int M,
-                     int N, int K, int r, uint16_t* Y, cudaStream_t s) {
+                     int N, int K, int r, uint16_t* Y, int silu_I, cudaStream_t s) {
     const int KS = smtc_split(M, N, K, TOKN);
     const TcPlan plan = tc_plan(TOKN, r, KS);
     const int smem_max = int(tc_plan(TOKN, W4A4_MAX_RANK, kMaxKS).total) + 1024;
@@ -463,13 +504,13 @@ w4a4_status launch_t(const uint8_t* ws, const uint8_t* packed, const uint16_t* c
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = plan.total + 1024;  // (the dynamic region is aligned up to 1024 bytes inside)
     cfg.stream = s;
-    if (cudaLaunchKernelEx(&cfg, gemm_smallm_tc_kernel<TOKN>, ws, packed, cs, bias, M, N, K, r, Y, KS) !=
+    if (cudaLaunchKernelEx(&cfg, gemm_smallm_tc_kernel<TOKN>, ws, packed, cs, bias, M, N, K, r, Y, KS, silu_I) !=
         cudaSuccess) {
         cudaGetLastError();
         return W4A4_ERR_CUDA;
     }
-    set_dispatch("gemm_smallm_tc tcgen05.f8f6f4 swap-AB N=%d split-K=%d (cluster) grid=%ux%u", TOKN, KS, grid.x,
-                 grid.y);
+    set_dispatch("gemm_smallm_tc tcgen05.f8f6f4 swap-AB N=%d split-K=%d (cluster) grid=%ux%u%s", TOKN, KS, grid.x,
+                 grid.y, silu_I ? " silu(gate)*up" : "");
     return launch_status();
 }
 
@@ -490,10 +531,11 @@ w4a4_status smtc_read_and_clear_status() {
 }
 
 w4a4_status launch_gemm_smallm_tc(const uint8_t* ws, const uint8_t* packed, const uint16_t* colscale,
-                                  const uint16_t* bias, int M, int N, int K, int r, uint16_t* Y, cudaStream_t s) {
-    if (M <= 16) return launch_t<16>(ws, packed, colscale, bias, M, N, K, r, Y, s);
-    if (M <= 32) return launch_t<32>(ws, packed, colscale, bias, M, N, K, r, Y, s);
-    return launch_t<64>(ws, packed, colscale, bias, M, N, K, r, Y, s);
+                                  const uint16_t* bias, int M, int N, int K, int r, uint16_t* Y, int silu_I,
+                                  cudaStream_t s) {
+    if (M <= 16) return launch_t<16>(ws, packed, colscale, bias, M, N, K, r, Y, silu_I, s);
+    if (M <= 32) return launch_t<32>(ws, packed, colscale, bias, M, N, K, r, Y, silu_I, s);
+    return launch_t<64>(ws, packed, colscale, bias, M, N, K, r, Y, silu_I, s);
 }
 
 }  // namespace w4a4

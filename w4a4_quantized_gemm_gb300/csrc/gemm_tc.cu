@@ -96,15 +96,17 @@ static_assert((2 - 1) * 2 * 4 * kRedBlock <= kRed && (3 - 1) * 2 * 4 * kRedBlock
                   (4 - 1) * 1 * 4 * kRedBlock <= kRed, "reduction buffer too small");
 
 struct Map {
-    uint32_t ST, SC, LA, LU, RED, BAR, SLOT, total;
+    uint32_t ST, SC, LA, LU, CB, RED, BAR, SLOT, total;
 };
+constexpr uint32_t kCB = 128;  // per epilogue warp: its 32 columns' colscale and bias (fp16)
 __host__ __device__ constexpr Map smem_map(int S, int rp, bool split) {
     Map m{};
     m.ST = 0;
     m.SC = m.ST + uint32_t(S) * kStage;
     m.LA = m.SC + SS * kScale;
     m.LU = m.LA + uint32_t(rp) * BM * 32;
-    m.RED = m.LU + uint32_t(rp) * BN * 32;
+    m.CB = m.LU + uint32_t(rp) * BN * 32;
+    m.RED = m.CB + NUM_EPI_WARPS * kCB;
     m.BAR = m.RED + (split ? kRed : 0u);
     m.SLOT = m.BAR + (3 * S + 2 * SS + 2 * NPB + 6) * 8;
     m.total = m.SLOT + 16 + 1024;  // + base alignment
@@ -114,14 +116,12 @@ static_assert(smem_map(4, 2, false).total <= 227 * 1024, "4 stages must fit at r
 static_assert(smem_map(3, 8, false).total <= 227 * 1024, "3 stages must fit at rank 128");
 static_assert(smem_map(3, 2, true).total <= 227 * 1024, "3 stages + the reduction buffer must fit at rank 32");
 
-template <int S, bool DUMP, bool SPLIT>
+template <int S, bool DUMP, bool SPLIT, bool SK>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_tc_kernel(const uint8_t* __restrict__ ws, const uint8_t* __restrict__ packed,
                    const uint16_t* __restrict__ colscale, const uint16_t* __restrict__ bias, int M, int N, int K,
-                   int r, uint16_t* __restrict__ Y, int32_t* __restrict__ P, int KS) {
+                   int r, uint16_t* __restrict__ Y, int32_t* __restrict__ P, int KS, int silu_I) {
     extern __shared__ uint8_t smem_raw[];
-    pdl_wait();
-    pdl_launch_dependents();
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t* gbase = smem_raw + (base - raw);
@@ -136,11 +136,35 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int cid = int(blockIdx.x) / KS, ncl = int(gridDim.x) / KS;
     const int j0 = kr * J / KS, j1 = (kr + 1) * J / KS;
     const int RPB = DUMP ? 0 : r / 16;  // LoRA operand planes held in shared memory
-    const int RP = kr == 0 ? RPB : 0;   // the LoRA term is added by rank 0 only
     const ActLayout AL = act_layout(M, K, r);
     const PackedLayout PL = packed_layout(N, K, r);
     const int MT = AL.MT, NT = (N + BN - 1) / BN;
     const int tiles = MT * NT;
+    // Work is walked as segments (tile t, jobs [a, b)).  Round-robin: CTA (or
+    // cluster) cid takes tiles cid, cid + ncl, ... with jobs [j0, j1).  Stream-K:
+    // the tiles x J jobs, tile-major, are cut into gridDim.x equal runs, CTA p
+    // taking run p; a tile cut between CTAs is finished by the CTA holding its
+    // first job, which adds the later CTAs' fp32 sums handed over in the workspace.
+    // (the host keeps tiles x J below 2^31)
+    const int units = tiles * J;
+    const int sk_ctas = int(gridDim.x);
+    auto sk_start = [&](int p) -> int { return int((long long)p * units / sk_ctas); };
+    const int u_begin = SK ? sk_start(int(blockIdx.x)) : cid;
+    const int u_end = SK ? sk_start(int(blockIdx.x) + 1) : tiles;
+    auto seg_at = [&](int u, int& t, int& a, int& b) {
+        if (SK) {
+            t = u / J;
+            a = u - t * J;
+            b = min(J, a + (u_end - u));
+        } else {
+            t = u;
+            a = j0;
+            b = j1;
+        }
+    };
+    auto seg_next = [&](int u, int a, int b) -> int { return SK ? u + (b - a) : u + ncl; };
+    // the LoRA term is added once per tile: by split rank 0, or by the segment holding job 0
+    auto lora_planes = [&](int a) -> int { return (SK ? a == 0 : kr == 0) ? RPB : 0; };
     const Map mp = smem_map(S, RPB, SPLIT);
 
     auto full = [&](int s) { return base + mp.BAR + 8u * s; };             // copies landed (producers + tx)
@@ -194,6 +218,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     volatile int no_abort = 0;
+    // Everything above touches only this CTA's shared and tensor memory, so it
+    // overlaps the previous kernel; so does warming L2 with the weight records of
+    // the first jobs (a prefetch only fills the cache, the copies proper come
+    // after the wait).  Global data the previous kernel may write is read after it.
+    if (warp == WARP_PRODUCER_W && lane == 0 && u_begin < u_end && !DUMP) {
+        int t0, a0, b0;
+        seg_at(u_begin, t0, a0, b0);
+        const int n0 = (t0 / MT) * BN, rows = min(BN, N - n0);
+        for (int g = a0 * GPJ; g < min(G, (a0 + S) * GPJ); ++g)
+            prefetch_l2(packed + PL.qW + (size_t(g) * N + n0) * 32, uint32_t(rows) * 32);
+    }
+    pdl_wait();
+    pdl_launch_dependents();
 
     auto fail = [&]() {
         atomicExch(&g_tc_status, int(W4A4_ERR_TIMEOUT));
@@ -211,7 +248,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const int role = warp == WARP_PRODUCER ? 0 : warp == WARP_PRODUCER_W ? 1 : 2;
         uint32_t it = 0, lp = 0, lora_issued = 0;
         bool ok = true;
-        for (int t = cid; t < tiles && ok; t += ncl) {
+        int t = 0, a = 0, b = 0;
+        for (int u = u_begin; u < u_end && ok; u = seg_next(u, a, b)) {
+            seg_at(u, t, a, b);
+            const int RP = lora_planes(a);
             const int mt = t % MT, n0 = (t / MT) * BN;
             const int rows = min(BN, N - n0);
             if (RP > 0 && role < 2) {
@@ -235,7 +275,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 lp ^= 1u;
                 lora_issued = 1;
             }
-            for (int jb = j0; jb < j1; ++jb) {
+            for (int jb = a; jb < b; ++jb) {
                 const int g0 = jb * GPJ, ng = min(GPJ, G - g0);
                 const int s = int(it % S);
                 const uint32_t ph = (it / S) & 1u;
@@ -278,11 +318,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         constexpr uint32_t IDESC = idesc_m128(BN);
         uint32_t it = 0, jc = 0, lp = 0;
         bool ok = true;
-        for (int t = cid; t < tiles && ok; t += ncl) {
+        int t = 0, a = 0, b = 0;
+        for (int u = u_begin; u < u_end && ok; u = seg_next(u, a, b)) {
+            seg_at(u, t, a, b);
+            const int RP = lora_planes(a);
             if (RP > 0) {
                 // the LoRA product takes a job buffer of its own (first 128 columns)
-                const uint32_t b = jc % NPB, tph = (jc / NPB) & 1u;
-                if (!warp_wait_parity(tempty(b), tph ^ 1u, abort_flag, WAIT_LIMIT_NS, BACKOFF_MMA) ||
+                const uint32_t bf = jc % NPB, tph = (jc / NPB) & 1u;
+                if (!warp_wait_parity(tempty(bf), tph ^ 1u, abort_flag, WAIT_LIMIT_NS, BACKOFF_MMA) ||
                     !warp_wait_parity(lfull, lp, abort_flag, WAIT_LIMIT_NS, BACKOFF_MMA)) {
                     ok = false;
                     break;
@@ -290,23 +333,23 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 tc_fence_after();
                 if (lane == 0) {
                     for (int p = 0; p < RP; ++p)
-                        mma_f16(tmem + b * (GPJ * BN), sdesc_sw32(base + mp.LA + uint32_t(p) * BM * 32),
+                        mma_f16(tmem + bf * (GPJ * BN), sdesc_sw32(base + mp.LA + uint32_t(p) * BM * 32),
                                 sdesc_sw32(base + mp.LU + uint32_t(p) * BN * 32), IDESC, p > 0 ? 1u : 0u);
-                    mma_commit(tfull(b));
+                    mma_commit(tfull(bf));
                     mma_commit(lempty);
                 }
                 __syncwarp();
                 ++jc;
                 lp ^= 1u;
             }
-            for (int jb = j0; jb < j1; ++jb) {
+            for (int jb = a; jb < b; ++jb) {
                 const int ng = min(GPJ, G - jb * GPJ);
                 const int s = int(it % S);
                 const uint32_t ph = (it / S) & 1u;
-                const uint32_t b = jc % NPB, tph = (jc / NPB) & 1u;
+                const uint32_t bf = jc % NPB, tph = (jc / NPB) & 1u;
                 if (!warp_wait_parity(full(s), ph, abort_flag, WAIT_LIMIT_NS, BACKOFF_MMA) ||
                     !warp_wait_parity(bready(s), ph, abort_flag, WAIT_LIMIT_NS, BACKOFF_MMA) ||
-                    !warp_wait_parity(tempty(b), tph ^ 1u, abort_flag, WAIT_LIMIT_NS, BACKOFF_MMA)) {
+                    !warp_wait_parity(tempty(bf), tph ^ 1u, abort_flag, WAIT_LIMIT_NS, BACKOFF_MMA)) {
                     ok = false;
                     break;
                 }
@@ -314,12 +357,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 if (lane == 0) {
                     const uint32_t sb = base + mp.ST + uint32_t(s) * kStage;
                     for (int j = 0; j < ng; ++j) {
-                        const uint32_t d = tmem + b * (GPJ * BN) + uint32_t(j) * BN;
+                        const uint32_t d = tmem + bf * (GPJ * BN) + uint32_t(j) * BN;
                         const uint32_t a0 = sb + ST_A + uint32_t(j) * kA, b0 = sb + ST_B + uint32_t(j) * kB;
                         mma_f8(d, sdesc_sw32(a0), sdesc_sw32(b0), IDESC, 0u);
                         mma_f8(d, sdesc_sw32(a0 + BM * 32), sdesc_sw32(b0 + BN * 32), IDESC, 1u);
                     }
-                    mma_commit(tfull(b));
+                    mma_commit(tfull(bf));
                     mma_commit(empty(s));
                 }
                 __syncwarp();
@@ -340,8 +383,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         static_assert(EXP_ROWS == 32, "one expansion row per lane");
         uint32_t it = 0;
         bool ok = true;
-        for (int t = cid; t < tiles && ok; t += ncl) {
-            for (int jb = j0; jb < j1; ++jb) {
+        int t = 0, a = 0, b = 0;
+        for (int u = u_begin; u < u_end && ok; u = seg_next(u, a, b)) {
+            seg_at(u, t, a, b);
+            for (int jb = a; jb < b; ++jb) {
                 const int ng = min(GPJ, G - jb * GPJ);
                 const int s = int(it % S), q = int(it % SS);
                 const uint32_t ph = (it / S) & 1u, sph = (it / SS) & 1u;
@@ -394,23 +439,48 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const uint32_t tl = tmem + (uint32_t(lq * 32) << 16) + uint32_t(c0);
         uint32_t it = 0, jc = 0, tc = 0;
         bool ok = true;
-        for (int t = cid; t < tiles && ok; t += ncl) {
+        int t = 0, a = 0, b = 0;
+        for (int u = u_begin; u < u_end && ok; u = seg_next(u, a, b)) {
+            seg_at(u, t, a, b);
+            const int RP = lora_planes(a);
             const int mt = t % MT, n0 = (t / MT) * BN;
             const int m = mt * BM + row;
             uint64_t acc[EPI_COLS / 2];  // running sums as packed column pairs
+            // this warp's colscale / bias for the tile's store, fetched while the jobs run:
+            // 16-byte chunks [cs 0..31 | bias 0..31], or with the SiLU epilogue
+            // [cs gate 0..15 | cs up | bias gate | bias up]
+            uint8_t* const cbw = gbase + mp.CB + uint32_t(warp) * kCB;
+            // (only warps that store this segment: not a stream-K hand-over, not a split-K sender)
+            const bool stores = !DUMP && !(SK && a > 0) && !(SPLIT && ((warp >> 2) % KS) != kr);
+            if (stores && lane < 8) {
+                const uint16_t* src = nullptr;
+                if (silu_I > 0) {
+                    const int hb = (n0 >> 1) + (c0 >> 1), which = lane >> 1;
+                    if (hb < silu_I)
+                        src = (which < 2 ? colscale : bias) + ((which & 1) ? silu_I : 0) + hb + (lane & 1) * 8;
+                    if (which >= 2 && !bias) src = nullptr;
+                } else {
+                    const int n = n0 + c0 + (lane & 3) * 8;
+                    if (n < N) src = lane < 4 ? colscale : bias;
+                    if (src) src += n;
+                }
+                if (src) cp_async16(cbw + lane * 16, src);
+                else *reinterpret_cast<uint4*>(cbw + lane * 16) = make_uint4(0, 0, 0, 0);
+            }
+            if (stores) cp_async_commit();
             if (RP > 0) {
-                const uint32_t b = jc % NPB, tph = (jc / NPB) & 1u;
-                if (!warp_wait_parity(tfull(b), tph, abort_flag, WAIT_LIMIT_NS, BACKOFF_EPI)) {
+                const uint32_t bf = jc % NPB, tph = (jc / NPB) & 1u;
+                if (!warp_wait_parity(tfull(bf), tph, abort_flag, WAIT_LIMIT_NS, BACKOFF_EPI)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
                 float l[EPI_COLS];
-                tmem_ld32(tl + b * (GPJ * BN), l);
+                tmem_ld32(tl + bf * (GPJ * BN), l);
                 tmem_wait_ld();
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(tempty(b));
+                if (lane == 0) mbar_arrive(tempty(bf));
 #pragma unroll
                 for (int c = 0; c < EPI_COLS / 2; ++c) acc[c] = f2_pack(l[2 * c], l[2 * c + 1]);
                 ++jc;
@@ -418,13 +488,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
                 for (int c = 0; c < EPI_COLS / 2; ++c) acc[c] = 0ull;
             }
-            for (int jb = j0; jb < j1; ++jb) {
+            for (int jb = a; jb < b; ++jb) {
                 const int g0 = jb * GPJ;
                 const bool two = g0 + 1 < G;
                 const int q = int(it % SS);
                 const uint32_t sph = (it / SS) & 1u;
-                const uint32_t b = jc % NPB, tph = (jc / NPB) & 1u;
-                if (!warp_wait_parity(tfull(b), tph, abort_flag, WAIT_LIMIT_NS, BACKOFF_EPI) ||
+                const uint32_t bf = jc % NPB, tph = (jc / NPB) & 1u;
+                if (!warp_wait_parity(tfull(bf), tph, abort_flag, WAIT_LIMIT_NS, BACKOFF_EPI) ||
                     !warp_wait_parity(sfull(q), sph, abort_flag, WAIT_LIMIT_NS, BACKOFF_EPI)) {
                     ok = false;
                     break;
@@ -437,7 +507,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 const float cm0 = (-8.f * sv0.y) * sv0.x, cm1 = (-8.f * sv1.y) * sv1.x;
                 const uint64_t sa0 = f2_pack(sv0.x, sv0.x), cc0 = f2_pack(cm0, cm0);
                 const uint64_t sa1 = f2_pack(sv1.x, sv1.x), cc1 = f2_pack(cm1, cm1);
-                const uint32_t tb = tl + b * (GPJ * BN);
+                const uint32_t tb = tl + bf * (GPJ * BN);
 #pragma unroll
                 for (int ch = 0; ch < EPI_COLS / 16; ++ch) {
                     float d0[16], d1[16];
@@ -447,7 +517,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     if (ch == EPI_COLS / 16 - 1) {
                         tc_fence_before();
                         __syncwarp();
-                        if (lane == 0) mbar_arrive(tempty(b));
+                        if (lane == 0) mbar_arrive(tempty(bf));
                     }
                     if constexpr (DUMP) {
                         if (m < M) {
@@ -491,6 +561,49 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 ++jc;
             }
             if (!ok) break;
+            if constexpr (SK) {
+                // this warp's slice of a CTA's hand-over slot: 8 x (32 lanes x 16 B), coalesced
+                uint8_t* const wsw = const_cast<uint8_t*>(ws);
+                uint32_t* const flags = reinterpret_cast<uint32_t*>(wsw + AL.flags);
+                auto slot_of = [&](int p) {
+                    return reinterpret_cast<float4*>(wsw + AL.part + (size_t(p) * kStreamKWarps + warp) * (32 * 32 * 4));
+                };
+                if (a > 0) {
+                    // a later part of a tile: hand the sums to the CTA that finishes it
+                    float4* dst = slot_of(int(blockIdx.x));
+#pragma unroll
+                    for (int c4 = 0; c4 < EPI_COLS / 4; ++c4) {
+                        const float2 lo = f2_unpack(acc[2 * c4]), hi = f2_unpack(acc[2 * c4 + 1]);
+                        __stcg(dst + c4 * 32 + lane, make_float4(lo.x, lo.y, hi.x, hi.y));
+                    }
+                    // every lane releases its own chunks; the warp's counter reaches 32 when all have landed
+                    red_add_release_gpu(flags + blockIdx.x * kStreamKWarps + warp, 1u);
+                    continue;
+                }
+                if (b < J) {
+                    // the tile's first part: add the later CTAs' sums in CTA order
+                    const int tile_end = (t + 1) * J;
+                    for (int p = int(blockIdx.x) + 1; p < sk_ctas && sk_start(p) < tile_end; ++p) {
+                        uint32_t* fl = flags + p * kStreamKWarps + warp;
+                        const bool got = __all_sync(0xffffffffu, wait_flag_gpu(fl, 32u, abort_flag, WAIT_LIMIT_NS));
+                        if (!got) {
+                            ok = false;
+                            break;
+                        }
+                        const float4* src = slot_of(p);
+#pragma unroll
+                        for (int c4 = 0; c4 < EPI_COLS / 4; ++c4) {
+                            const float4 v = __ldcg(src + c4 * 32 + lane);
+                            const float2 lo = f2_unpack(acc[2 * c4]), hi = f2_unpack(acc[2 * c4 + 1]);
+                            acc[2 * c4] = f2_pack(lo.x + v.x, lo.y + v.y);
+                            acc[2 * c4 + 1] = f2_pack(hi.x + v.z, hi.y + v.w);
+                        }
+                        __syncwarp();
+                        if (lane == 0) *fl = 0u;  // cleared for the next call on this workspace
+                    }
+                    if (!ok) break;
+                }
+            }
             if constexpr (SPLIT && !DUMP) {
                 const int sl = warp >> 2, owner = sl % KS;
                 if (owner != kr) {
@@ -549,14 +662,47 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
             ++tc;
             if constexpr (!DUMP) {
-                if (m < M) {
+                cp_async_wait<0>();  // this warp's colscale / bias chunks
+                __syncwarp();
+                if (m < M && silu_I > 0) {
+                    // fused gate|up weights: columns 0..15 of this warp's slice are gates, 16..31
+                    // the matching ups (gate_up_row); h = silu(gate) * up for 16 outputs
+                    const int hb = (n0 >> 1) + (c0 >> 1);
+                    if (hb < silu_I) {
+                        const uint4* cbv = reinterpret_cast<const uint4*>(cbw);
+                        uint4* dst = reinterpret_cast<uint4*>(Y + size_t(m) * silu_I + hb);
+#pragma unroll
+                        for (int q8 = 0; q8 < 2; ++q8) {
+                            const uint4 csg = cbv[q8], csu = cbv[2 + q8], bg = cbv[4 + q8], bu = cbv[6 + q8];
+                            const uint32_t w_cg[4] = {csg.x, csg.y, csg.z, csg.w}, w_cu[4] = {csu.x, csu.y, csu.z, csu.w};
+                            const uint32_t w_bg[4] = {bg.x, bg.y, bg.z, bg.w}, w_bu[4] = {bu.x, bu.y, bu.z, bu.w};
+                            uint32_t hw[4];
+#pragma unroll
+                            for (int j = 0; j < 4; ++j) {
+                                const float2 c2g = __half22float2(*reinterpret_cast<const __half2*>(&w_cg[j]));
+                                const float2 c2u = __half22float2(*reinterpret_cast<const __half2*>(&w_cu[j]));
+                                const float2 b2g = __half22float2(*reinterpret_cast<const __half2*>(&w_bg[j]));
+                                const float2 b2u = __half22float2(*reinterpret_cast<const __half2*>(&w_bu[j]));
+                                const float2 ag = f2_unpack(acc[q8 * 4 + j]), au = f2_unpack(acc[8 + q8 * 4 + j]);
+                                const float g0 = fmaf(c2g.x, ag.x, b2g.x), g1 = fmaf(c2g.y, ag.y, b2g.y);
+                                const float u0 = fmaf(c2u.x, au.x, b2u.x), u1 = fmaf(c2u.y, au.y, b2u.y);
+                                // silu(g) = g / (1 + e^-g) with the fast exponential and divide
+                                // (relative error ~1e-6; e^-g = inf gives -0)
+                                const __half2 h = __floats2half2_rn(__fdividef(g0, 1.0f + __expf(-g0)) * u0,
+                                                                    __fdividef(g1, 1.0f + __expf(-g1)) * u1);
+                                hw[j] = *reinterpret_cast<const uint32_t*>(&h);
+                            }
+                            dst[q8] = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+                        }
+                    }
+                } else if (m < M) {
+                    const uint4* cbv = reinterpret_cast<const uint4*>(cbw);
 #pragma unroll
                     for (int ch = 0; ch < EPI_COLS / 8; ++ch) {
                         const int n = n0 + c0 + ch * 8;
                         if (n < N) {
-                            const uint4 csv = __ldg(reinterpret_cast<const uint4*>(colscale + n));
-                            const uint4 bsv =
-                                bias ? __ldg(reinterpret_cast<const uint4*>(bias + n)) : make_uint4(0, 0, 0, 0);
+                            const uint4 csv = cbv[ch];
+                            const uint4 bsv = cbv[4 + ch];
                             const uint32_t cw[4] = {csv.x, csv.y, csv.z, csv.w};
                             const uint32_t bw[4] = {bsv.x, bsv.y, bsv.z, bsv.w};
                             uint32_t out[4];
@@ -577,6 +723,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
             }
         }
+        cp_async_wait<0>();  // (a segment left early) nothing lands in shared memory after this
         if (!ok) fail();
     }
 
@@ -588,21 +735,22 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 }
 
 // Registers per thread the kernel was compiled for (cached per instantiation).
-template <int S, bool DUMP, bool SPLIT>
+template <int S, bool DUMP, bool SPLIT, bool SK>
 int launch_regs() {
     static int regs = -1;
     if (regs < 0) {
         cudaFuncAttributes fa{};
-        if (cudaFuncGetAttributes(&fa, gemm_tc_kernel<S, DUMP, SPLIT>) != cudaSuccess) return 0;
+        if (cudaFuncGetAttributes(&fa, gemm_tc_kernel<S, DUMP, SPLIT, SK>) != cudaSuccess) return 0;
         regs = fa.numRegs;
     }
     return regs;
 }
 
-template <int S, bool DUMP, bool SPLIT>
+template <int S, bool DUMP, bool SPLIT, bool SK = false>
 w4a4_status launch_impl(const uint8_t* ws, const uint8_t* packed, const uint16_t* cs, const uint16_t* bias, int M,
-                        int N, int K, int r, uint16_t* Y, int32_t* P, int KS, cudaStream_t s) {
-    auto kern = gemm_tc_kernel<S, DUMP, SPLIT>;
+                        int N, int K, int r, uint16_t* Y, int32_t* P, int KS, cudaStream_t s, int sk_ctas = 0,
+                        int silu_I = 0) {
+    auto kern = gemm_tc_kernel<S, DUMP, SPLIT, SK>;
     static int attr_done[64] = {0};
     int dev = 0;
     cudaGetDevice(&dev);
@@ -614,14 +762,14 @@ w4a4_status launch_impl(const uint8_t* ws, const uint8_t* packed, const uint16_t
         attr_done[dev] = 1;
     }
     // the setmaxnreg split needs the launch-time register pool to cover it
-    if (launch_regs<S, DUMP, SPLIT>() * NUM_THREADS <
+    if (launch_regs<S, DUMP, SPLIT, SK>() * NUM_THREADS <
         NUM_EPI_WARPS * 32 * EPI_REGS + (NUM_THREADS - NUM_EPI_WARPS * 32) * OTHER_REGS)
         return W4A4_ERR_CUDA;
     const int MT = (M + BM - 1) / BM, NT = (N + BN - 1) / BN;
     const int tiles = MT * NT;
     const uint32_t smem = smem_map(S, rp, SPLIT).total;
     if (!SPLIT) {
-        const int grid = tiles < device_sm_count() ? tiles : device_sm_count();
+        const int grid = SK ? sk_ctas : (tiles < device_sm_count() ? tiles : device_sm_count());
         cudaLaunchConfig_t cfg{};
         cudaLaunchAttribute attr[1];
         cfg.attrs = attr;
@@ -630,12 +778,13 @@ w4a4_status launch_impl(const uint8_t* ws, const uint8_t* packed, const uint16_t
         cfg.blockDim = dim3(NUM_THREADS);
         cfg.dynamicSmemBytes = smem;
         cfg.stream = s;
-        if (cudaLaunchKernelEx(&cfg, kern, ws, packed, cs, bias, M, N, K, r, Y, P, 1) != cudaSuccess) {
+        if (cudaLaunchKernelEx(&cfg, kern, ws, packed, cs, bias, M, N, K, r, Y, P, 1, silu_I) != cudaSuccess) {
             cudaGetLastError();
             return W4A4_ERR_CUDA;
         }
-        set_dispatch("gemm_tc tcgen05.f8f6f4 tile=%dx%d groups/job=%d stages=%d tiles=%d grid=%d%s", BM, BN, GPJ, S,
-                     tiles, grid, DUMP ? " (partials dump)" : "");
+        set_dispatch("gemm_tc tcgen05.f8f6f4 tile=%dx%d groups/job=%d stages=%d tiles=%d grid=%d%s%s%s", BM, BN, GPJ,
+                     S, tiles, grid, SK ? " stream-K" : "", silu_I ? " silu(gate)*up" : "",
+                     DUMP ? " (partials dump)" : "");
         return launch_status();
     }
     // clusters of KS CTAs, as many as can be resident at once (persistent over tiles)
@@ -659,12 +808,13 @@ w4a4_status launch_impl(const uint8_t* ws, const uint8_t* packed, const uint16_t
     const int clusters = tiles < active ? tiles : active;
     cfg.gridDim = dim3(unsigned(clusters * KS));
     cfg.numAttrs = add_pdl_attr(attr, 1);
-    if (cudaLaunchKernelEx(&cfg, kern, ws, packed, cs, bias, M, N, K, r, Y, P, KS) != cudaSuccess) {
+    if (cudaLaunchKernelEx(&cfg, kern, ws, packed, cs, bias, M, N, K, r, Y, P, KS, silu_I) != cudaSuccess) {
         cudaGetLastError();
         return W4A4_ERR_CUDA;
     }
-    set_dispatch("gemm_tc tcgen05.f8f6f4 tile=%dx%d groups/job=%d stages=%d split-K=%d (cluster) tiles=%d grid=%d%s",
-                 BM, BN, GPJ, S, KS, tiles, clusters * KS, DUMP ? " (partials dump)" : "");
+    set_dispatch("gemm_tc tcgen05.f8f6f4 tile=%dx%d groups/job=%d stages=%d split-K=%d (cluster) tiles=%d grid=%d%s%s",
+                 BM, BN, GPJ, S, KS, tiles, clusters * KS, silu_I ? " silu(gate)*up" : "",
+                 DUMP ? " (partials dump)" : "");
     return launch_status();
 }
 
@@ -677,7 +827,7 @@ static int resident_clusters(int ks) {
     cudaGetDevice(&dev);
     if (dev < 0 || dev >= 64) return 0;
     if (cache[dev][ks] == 0) {
-        auto kern = gemm_tc_kernel<3, false, true>;
+        auto kern = gemm_tc_kernel<3, false, true, false>;
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  int(smem_map(3, 2, true).total)) != cudaSuccess) {
             cudaGetLastError();
@@ -704,35 +854,57 @@ static int resident_clusters(int ks) {
     return cache[dev][ks];
 }
 
-// Split factor along K: the one that minimises (rounds of tiles) x (jobs per
-// CTA + the cross-CTA reduction, about 1.5 jobs) for the machine's resident
-// clusters; rank 128 LoRA operands leave no room for the reduction buffer.
-static int split_factor(int M, int N, int K, int r) {
+// Schedule: the cheapest of round-robin tiles, split-K over clusters and
+// stream-K, in units of one job's time: rounds of tiles x jobs per tile;
+// rounds x (jobs / KS + the cluster reduction, about 1.5 jobs); or the longest
+// run of jobs + the hand-over of a tile's sums (about 1 job).  Rank 128 LoRA
+// operands leave no room for the cluster reduction buffer; stream-K needs the
+// hand-over area of the workspace.
+struct TcSchedule {
+    int ks, sk_ctas;  // sk_ctas > 0: stream-K over that many CTAs
+};
+static TcSchedule tc_schedule(int M, int N, int K, int r, bool sk_room) {
     const int tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
     const int jobs = (K / kGroup + GPJ - 1) / GPJ;
-    if (r > 32 || tiles <= 0) return 1;
+    TcSchedule best_s{1, 0};
+    if (tiles <= 0) return best_s;
     const int sms = device_sm_count();
     double best = double((tiles + sms - 1) / sms) * jobs;
-    int best_ks = 1;
-    for (int ks = 2; ks <= MAX_KS && ks <= jobs; ++ks) {
+    for (int ks = 2; r <= 32 && ks <= MAX_KS && ks <= jobs; ++ks) {
         const int cl = resident_clusters(ks);
         if (cl < 1) continue;
         const double cost = double((tiles + cl - 1) / cl) * (double((jobs + ks - 1) / ks) + 1.5);
         if (cost < best) {
             best = cost;
-            best_ks = ks;
+            best_s = TcSchedule{ks, 0};
         }
     }
-    return best_ks;
+    if (sk_room && (long long)tiles * jobs < (1ll << 31) / kStreamKSlots) {
+        const long long units = (long long)tiles * jobs;
+        long long p = sms < kStreamKSlots ? sms : kStreamKSlots;
+        if (p > units) p = units;
+        const double cost = double((units + p - 1) / p) + 1.0;
+        if (cost < best) best_s = TcSchedule{1, int(p)};
+    }
+    return best_s;
 }
 
 w4a4_status launch_gemm_tc(const uint8_t* ws, const uint8_t* packed, const uint16_t* colscale, const uint16_t* bias,
-                           int M, int N, int K, int r, uint16_t* Y, int32_t* P_dump, cudaStream_t s) {
+                           int M, int N, int K, int r, uint16_t* Y, int32_t* P_dump, bool sk_room, int silu_I,
+                           cudaStream_t s) {
     if (P_dump) return launch_impl<4, true, false>(ws, packed, colscale, bias, M, N, K, r, Y, P_dump, 1, s);
-    const int ks = split_factor(M, N, K, r);
-    if (ks > 1) return launch_impl<3, false, true>(ws, packed, colscale, bias, M, N, K, r, Y, nullptr, ks, s);
-    if (r > 32) return launch_impl<3, false, false>(ws, packed, colscale, bias, M, N, K, r, Y, nullptr, 1, s);
-    return launch_impl<4, false, false>(ws, packed, colscale, bias, M, N, K, r, Y, nullptr, 1, s);
+    const TcSchedule sc = tc_schedule(M, N, K, r, sk_room && tc_stream_k_enabled());
+    if (sc.sk_ctas > 0) {
+        if (r > 32)
+            return launch_impl<3, false, false, true>(ws, packed, colscale, bias, M, N, K, r, Y, nullptr, 1, s,
+                                                      sc.sk_ctas, silu_I);
+        return launch_impl<4, false, false, true>(ws, packed, colscale, bias, M, N, K, r, Y, nullptr, 1, s,
+                                                  sc.sk_ctas, silu_I);
+    }
+    if (sc.ks > 1)
+        return launch_impl<3, false, true>(ws, packed, colscale, bias, M, N, K, r, Y, nullptr, sc.ks, s, 0, silu_I);
+    if (r > 32) return launch_impl<3, false, false>(ws, packed, colscale, bias, M, N, K, r, Y, nullptr, 1, s, 0, silu_I);
+    return launch_impl<4, false, false>(ws, packed, colscale, bias, M, N, K, r, Y, nullptr, 1, s, 0, silu_I);
 }
 
 w4a4_status tc_read_and_clear_status() {

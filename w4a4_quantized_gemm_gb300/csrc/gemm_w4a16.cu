@@ -22,6 +22,12 @@
 // the tokens' B fragments are paired the same way from shared memory.  The
 // group's fp32 sum is scaled by sW (fp16) and added to the fp32 accumulator.
 //
+// Asymmetric group-128 weights ("How the weights are stored": codes 0..15,
+// value (q - zero) scale per 128-group): the same kernel with the nibble's
+// bias removed per row, (1024 + q) - (1024 + zero), exact in fp16 for zero
+// points in [-1024, 1023]; each 64-channel slot reads its group's scale and
+// zero from the two scale-plane slots of the group.
+//
 // LoRA: each CTA forms its K slice's part of X . L_down (fp16 MMA, fp32
 // accumulate) and applies the up-projection to that part before the exchange;
 // the map is linear, so the exchange of partial sums also sums the LoRA term.
@@ -54,13 +60,13 @@ struct W4A16Plan {
     int ns;  // group slots: two halves of ns / 2, refilled alternately
     uint32_t wq, xs, sw, lu, la, red, bar, total;
 };
-__host__ __device__ inline W4A16Plan w4a16_plan(int tok, int r) {
+__host__ __device__ inline W4A16Plan w4a16_plan(int tok, int r, bool asym) {
     W4A16Plan p;
     p.ns = tok <= 8 ? 16 : tok <= 32 ? 8 : 4;  // two CTAs per SM fit for every token count
     uint32_t o = 0;
     p.wq = o, o += uint32_t(p.ns) * kTileN * 32;                 // [slot][128 rows][32 B]
     p.xs = o, o += uint32_t(p.ns) * tok * kXs * 2;               // [slot][tok][72 halves]
-    p.sw = o, o += uint32_t(p.ns) * kTileN * 2;                  // [slot][128] fp16
+    p.sw = o, o += uint32_t(p.ns) * kTileN * (asym ? 4 : 2);     // [slot][128] fp16 (asym: scale, zero)
     p.lu = o, o += uint32_t(r / 16) * kTileN * 32;               // [plane][128 rows][32 B]
     p.la = o, o += 2u * uint32_t(r / 16) * tok * 32;             // [hi|lo][plane][tok][32 B]
     p.red = o, o += uint32_t(kMaxKS - 1) * 32 * (tok / 8) * 16;  // [sender slot][lane][tok / 8] float4
@@ -72,16 +78,17 @@ __host__ __device__ inline W4A16Plan w4a16_plan(int tok, int r) {
 // (contiguous) once every group has been consumed: tok * 136 * 2 bytes <=
 // ns * (4 KB + tok * 144 bytes) for every slot count above.
 
-// Nibbles j and j + 4 of w -> exact fp16 codes (u - 8) in the low and high half.
-__device__ __forceinline__ uint32_t nib_pair_f16(uint32_t w, int j) {
+// Nibbles j and j + 4 of w -> exact fp16 values u - (bias - 1024) in the low
+// and high half: bias2 = 1032 (offset-binary codes u - 8) or 1024 + zero.
+__device__ __forceinline__ uint32_t nib_pair_f16(uint32_t w, int j, __half2 bias2) {
     uint32_t h;
     const uint32_t x = w >> (4 * j);
     asm("lop3.b32 %0, %1, %2, %3, 0xea;\n" : "=r"(h) : "r"(x), "r"(0x000F000Fu), "r"(0x64006400u));  // (x & m) | c
-    const __half2 v = __hsub2(*reinterpret_cast<const __half2*>(&h), __float2half2_rn(1032.f));
+    const __half2 v = __hsub2(*reinterpret_cast<const __half2*>(&h), bias2);
     return *reinterpret_cast<const uint32_t*>(&v);
 }
 
-template <int NT8>
+template <int NT8, bool ASYM>
 __global__ void __launch_bounds__(kWarps * 32) gemm_w4a16_kernel(
     const uint16_t* __restrict__ X, const uint8_t* __restrict__ packed, const uint16_t* __restrict__ colscale,
     const uint16_t* __restrict__ bias, int M, int N, int K, int r, uint16_t* __restrict__ Y, int KS) {
@@ -89,9 +96,8 @@ __global__ void __launch_bounds__(kWarps * 32) gemm_w4a16_kernel(
     constexpr int NT = kWarps * 32;
     extern __shared__ __align__(128) uint8_t smraw[];
     __shared__ int abort_flag, never_abort;
-    pdl_wait();
-    pdl_launch_dependents();
-    const W4A16Plan PLN = w4a16_plan(TOK, r);
+    const W4A16Plan PLN = w4a16_plan(TOK, r, ASYM);
+    constexpr uint32_t kSwSlot = kTileN * (ASYM ? 4 : 2);  // scale-plane bytes per slot
     const uint32_t sbase = smem_u32(smraw);
     const uint32_t full0 = sbase + PLN.bar;  // full[s] = full0 + 8 s
     const uint32_t aux_full = full0 + 8u * PLN.ns, red_full = aux_full + 8u;
@@ -117,8 +123,9 @@ __global__ void __launch_bounds__(kWarps * 32) gemm_w4a16_kernel(
 
     const uint8_t* qW = packed + PL.qW;
     const uint8_t* sWg = packed + PL.sW;
-    // 16-byte pieces of one group besides the weight records: weight scales, the tokens' values
-    const int pc_sw = rows_valid / 8, pc_x = tok_valid * 8;
+    // 16-byte pieces of one group besides the weight records: weight scales (asym: the
+    // group's scale and zero rows), the tokens' values
+    const int pc_sw1 = rows_valid / 8, pc_sw = ASYM ? 2 * pc_sw1 : pc_sw1, pc_x = tok_valid * 8;
 
     // chunk c -- groups g_begin + c * half ... -- into slot half c & 1; every thread takes part
     auto issue_chunk = [&](int c) {
@@ -133,7 +140,10 @@ __global__ void __launch_bounds__(kWarps * 32) gemm_w4a16_kernel(
             }
             for (int p = threadIdx.x; p < pc_sw + pc_x; p += NT) {
                 if (p < pc_sw) {
-                    cp_async16(smraw + PLN.sw + slot * (kTileN * 2) + p * 16, sWg + ((size_t)g * N + nbase) * 2 + p * 16);
+                    const int hz = ASYM ? (p >= pc_sw1) : 0, pp = p - hz * pc_sw1;
+                    const int gs = ASYM ? ((g & ~1) | hz) : g;  // asym: the 128-group's scale / zero slot
+                    cp_async16(smraw + PLN.sw + slot * kSwSlot + hz * (kTileN * 2) + pp * 16,
+                               sWg + ((size_t)gs * N + nbase) * 2 + pp * 16);
                 } else {
                     const int e = p - pc_sw, t = e >> 3, c8 = e & 7;
                     cp_async16(smraw + PLN.xs + (slot * TOK + t) * (kXs * 2) + c8 * 16,
@@ -161,6 +171,17 @@ __global__ void __launch_bounds__(kWarps * 32) gemm_w4a16_kernel(
     }
     __syncthreads();  // barriers initialised for this CTA's threads
     if (KS > 1) cluster_arrive_release();  // ... and, once every rank has arrived, for the peers
+    // The setup above touches only shared memory and overlaps the previous kernel;
+    // so does warming L2 with this CTA's share of the weight records and scales
+    // (a prefetch only fills the cache; every copy proper comes after the wait).
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < n_groups; ++i) {
+            prefetch_l2(qW + ((size_t)(g_begin + i) * N + nbase) * 32, uint32_t(rows_valid) * 32);
+            prefetch_l2(sWg + ((size_t)(g_begin + i) * N + nbase) * 2, uint32_t(rows_valid) * 2);
+        }
+    }
+    pdl_wait();
+    pdl_launch_dependents();
     // L_up rows of all 128 weight rows (every warp applies the up-projection to its CTA's LoRA part)
     for (int p = threadIdx.x; p < (r / 16) * (rows_valid * 2); p += NT) {
         const int pl = p / (rows_valid * 2), e = p % (rows_valid * 2);
@@ -225,9 +246,16 @@ __global__ void __launch_bounds__(kWarps * 32) gemm_w4a16_kernel(
             if (warp_active) {
             const uint2 wa = *reinterpret_cast<const uint2*>(smw + slot * (kTileN * 32));
             const uint2 wb = *reinterpret_cast<const uint2*>(smw + slot * (kTileN * 32) + 8 * 32);
-            const float swa = __half2float(__ushort_as_half(smsw[slot * kTileN]));
-            const float swb = __half2float(__ushort_as_half(smsw[slot * kTileN + 8]));
+            const uint16_t* sws = smsw + slot * (kSwSlot / 2);
+            const float swa = __half2float(__ushort_as_half(sws[0]));
+            const float swb = __half2float(__ushort_as_half(sws[8]));
             const uint64_t swa2 = f2_pack(swa, swa), swb2 = f2_pack(swb, swb);
+            __half2 bias_a = __float2half2_rn(1032.f), bias_b = bias_a;
+            if constexpr (ASYM) {  // 1024 + zero of rows a and b (exact for |zero| <= 1024)
+                const __half za = __ushort_as_half(sws[kTileN]), zb = __ushort_as_half(sws[kTileN + 8]);
+                bias_a = __hadd2(__halves2half2(za, za), __float2half2_rn(1024.f));
+                bias_b = __hadd2(__halves2half2(zb, zb), __float2half2_rn(1024.f));
+            }
             // word h of this lane's record bytes holds codes k = 32h + 4q + i and 32h + 16 + 4q + i
             // (i = 0..3, nibbles i and i + 4); MMA (h, jp) takes i = jp, jp + 1
             uint32_t af[4][4];
@@ -236,10 +264,10 @@ __global__ void __launch_bounds__(kWarps * 32) gemm_w4a16_kernel(
                 const uint32_t xa = h ? wa.y : wa.x, xb = h ? wb.y : wb.x;
 #pragma unroll
                 for (int jp = 0; jp < 2; ++jp) {
-                    af[2 * h + jp][0] = nib_pair_f16(xa, 2 * jp);
-                    af[2 * h + jp][2] = nib_pair_f16(xa, 2 * jp + 1);
-                    af[2 * h + jp][1] = nib_pair_f16(xb, 2 * jp);
-                    af[2 * h + jp][3] = nib_pair_f16(xb, 2 * jp + 1);
+                    af[2 * h + jp][0] = nib_pair_f16(xa, 2 * jp, bias_a);
+                    af[2 * h + jp][2] = nib_pair_f16(xa, 2 * jp + 1, bias_a);
+                    af[2 * h + jp][1] = nib_pair_f16(xb, 2 * jp, bias_b);
+                    af[2 * h + jp][3] = nib_pair_f16(xb, 2 * jp + 1, bias_b);
                 }
             }
 #pragma unroll
@@ -446,15 +474,15 @@ int w4a16_split(int M, int N, int K, int TOK) {
     return ks;
 }
 
-template <int NT8>
+template <int NT8, bool ASYM>
 w4a4_status launch_nt(const uint16_t* X, const uint8_t* packed, const uint16_t* cs, const uint16_t* bias, int M,
                       int N, int K, int r, uint16_t* Y, cudaStream_t s) {
-    const int smem_max = int(w4a16_plan(NT8 * 8, W4A4_MAX_RANK).total);  // the attribute covers every rank
+    const int smem_max = int(w4a16_plan(NT8 * 8, W4A4_MAX_RANK, ASYM).total);  // the attribute covers every rank
     static int attr_done[64] = {0};
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev >= 0 && dev < 64 && !attr_done[dev]) {
-        if (cudaFuncSetAttribute(gemm_w4a16_kernel<NT8>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_max) !=
+        if (cudaFuncSetAttribute(gemm_w4a16_kernel<NT8, ASYM>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_max) !=
             cudaSuccess)
             return W4A4_ERR_CUDA;
         attr_done[dev] = 1;
@@ -471,14 +499,14 @@ w4a4_status launch_nt(const uint16_t* X, const uint8_t* packed, const uint16_t* 
     cfg.numAttrs = add_pdl_attr(attr, 1);
     cfg.gridDim = grid;
     cfg.blockDim = dim3(kWarps * 32);
-    cfg.dynamicSmemBytes = w4a16_plan(NT8 * 8, r).total;
+    cfg.dynamicSmemBytes = w4a16_plan(NT8 * 8, r, ASYM).total;
     cfg.stream = s;
-    if (cudaLaunchKernelEx(&cfg, gemm_w4a16_kernel<NT8>, X, packed, cs, bias, M, N, K, r, Y, KS) != cudaSuccess) {
+    if (cudaLaunchKernelEx(&cfg, gemm_w4a16_kernel<NT8, ASYM>, X, packed, cs, bias, M, N, K, r, Y, KS) != cudaSuccess) {
         cudaGetLastError();
         return W4A4_ERR_CUDA;
     }
-    set_dispatch("gemm_w4a16 mma.sync.f16 tokens/CTA=%d split-K=%d (cluster) grid=%ux%u", NT8 * 8, KS, grid.x,
-                 grid.y);
+    set_dispatch("gemm_w4a16%s mma.sync.f16 tokens/CTA=%d split-K=%d (cluster) grid=%ux%u",
+                 ASYM ? " (asymmetric g128)" : "", NT8 * 8, KS, grid.x, grid.y);
     return launch_status();
 }
 
@@ -498,12 +526,20 @@ w4a4_status w4a16_read_and_clear_status() {
     return W4A4_OK;
 }
 
+template <bool ASYM>
+w4a4_status launch_w4a16(const uint16_t* X, const uint8_t* packed, const uint16_t* colscale, const uint16_t* bias,
+                         int M, int N, int K, int r, uint16_t* Y, cudaStream_t s) {
+    if (M <= 8) return launch_nt<1, ASYM>(X, packed, colscale, bias, M, N, K, r, Y, s);
+    if (M <= 16) return launch_nt<2, ASYM>(X, packed, colscale, bias, M, N, K, r, Y, s);
+    if (M <= 32) return launch_nt<4, ASYM>(X, packed, colscale, bias, M, N, K, r, Y, s);
+    return launch_nt<8, ASYM>(X, packed, colscale, bias, M, N, K, r, Y, s);
+}
+
 w4a4_status launch_gemm_w4a16(const uint16_t* X, const uint8_t* packed, const uint16_t* colscale,
-                              const uint16_t* bias, int M, int N, int K, int r, uint16_t* Y, cudaStream_t s) {
-    if (M <= 8) return launch_nt<1>(X, packed, colscale, bias, M, N, K, r, Y, s);
-    if (M <= 16) return launch_nt<2>(X, packed, colscale, bias, M, N, K, r, Y, s);
-    if (M <= 32) return launch_nt<4>(X, packed, colscale, bias, M, N, K, r, Y, s);
-    return launch_nt<8>(X, packed, colscale, bias, M, N, K, r, Y, s);
+                              const uint16_t* bias, int M, int N, int K, int r, uint16_t* Y, bool asym,
+                              cudaStream_t s) {
+    return asym ? launch_w4a16<true>(X, packed, colscale, bias, M, N, K, r, Y, s)
+                : launch_w4a16<false>(X, packed, colscale, bias, M, N, K, r, Y, s);
 }
 
 }  // namespace w4a4

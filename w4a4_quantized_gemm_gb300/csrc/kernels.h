@@ -6,9 +6,12 @@
 namespace w4a4 {
 
 // pack.cu
+// silu_I > 0: W is a fused gate|up weight (I gate rows, then I up rows), packed in gate_up_row order
 void launch_pack_weights(const float* W, const int8_t* codes, const uint16_t* scales, int N, int K, int r,
-                         uint8_t* packed, cudaStream_t s);
-void launch_pack_lora(const uint16_t* L_down, const uint16_t* L_up, int N, int K, int r,
+                         int silu_I, uint8_t* packed, cudaStream_t s);
+// asymmetric group-128 weights; synchronises s; W4A4_ERR_INVALID_ARG when a zero point leaves [-1024, 1023]
+w4a4_status launch_pack_weights_asym(const float* W, int N, int K, int r, uint8_t* packed, cudaStream_t s);
+void launch_pack_lora(const uint16_t* L_down, const uint16_t* L_up, int N, int K, int r, int silu_I,
                       uint8_t* packed, cudaStream_t s);
 void launch_unpack_weights(const uint8_t* packed, int N, int K, int r, int8_t* codes, uint16_t* scales,
                            uint16_t* L_down, uint16_t* L_up, cudaStream_t s);
@@ -25,17 +28,21 @@ w4a4_status launch_gemm_smallm(const uint8_t* ws, const uint8_t* packed, const u
                                int32_t* P_dump, cudaStream_t s);
 
 // gemm_tc.cu (tcgen05 + TMEM)
+// sk_room: the workspace holds the stream-K hand-over area (act_layout().full bytes)
+// silu_I > 0: weights packed by w4a4_pack_weights_gate_up; Y receives silu(gate) * up [M, silu_I]
 w4a4_status launch_gemm_tc(const uint8_t* ws, const uint8_t* packed, const uint16_t* colscale,
                            const uint16_t* bias, int M, int N, int K, int r, uint16_t* Y, int32_t* P_dump,
-                           cudaStream_t s);
+                           bool sk_room, int silu_I, cudaStream_t s);
 
 // rmsnorm.cu (stack glue between linears)
 w4a4_status launch_quantize_act_rmsnorm(const uint16_t* Y, int ld_y, const uint8_t* packed, int M, int K, int r,
                                         uint8_t* ws, cudaStream_t s);
 w4a4_status launch_gemm_smallm_tc(const uint8_t* ws, const uint8_t* packed, const uint16_t* colscale,
-                                  const uint16_t* bias, int M, int N, int K, int r, uint16_t* Y, cudaStream_t s);
+                                  const uint16_t* bias, int M, int N, int K, int r, uint16_t* Y, int silu_I,
+                                  cudaStream_t s);
 w4a4_status launch_gemm_w4a16(const uint16_t* X, const uint8_t* packed, const uint16_t* colscale,
-                              const uint16_t* bias, int M, int N, int K, int r, uint16_t* Y, cudaStream_t s);
+                              const uint16_t* bias, int M, int N, int K, int r, uint16_t* Y, bool asym,
+                              cudaStream_t s);
 void launch_rmsnorm_f16(const uint16_t* Y, int M, int ld_y, int K, double eps, uint16_t* X, cudaStream_t s);
 
 }  // namespace w4a4

@@ -76,6 +76,10 @@ __global__ void __launch_bounds__(kWarps * 32) quantize_act_kernel(const uint16_
     const int row0 = (blockIdx.x / CK) * kRows;
     const int mt = row0 / kTileM;
     const int g_begin = (G * crank) / CK, g_end = (G * (crank + 1)) / CK;
+    if (blockIdx.x == 0) {  // the GEMM's stream-K ready flags start every call cleared
+        uint32_t* fl = reinterpret_cast<uint32_t*>(ws + AL.flags);
+        for (int i = threadIdx.x; i < kStreamKSlots * kStreamKWarps; i += kWarps * 32) fl[i] = 0u;
+    }
 
     // quantisation role: lane owns row (lane/2), columns 32*(lane%2) .. +31 of a group
     const int qrow = lane >> 1, qhalf = lane & 1;

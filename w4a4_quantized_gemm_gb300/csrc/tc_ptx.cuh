@@ -162,6 +162,32 @@ __device__ __forceinline__ bool warp_wait_parity_cluster(uint32_t bar, uint32_t 
     return __all_sync(0xffffffffu, ok);
 }
 // The two halves of a cluster barrier, for work placed between them.
+// ---- flags in global memory shared by the CTAs of one launch --------------
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];\n" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_release_gpu(uint32_t* p, uint32_t v) {
+    asm volatile("st.release.gpu.global.u32 [%0], %1;\n" ::"l"(p), "r"(v) : "memory");
+}
+// Release-ordered increment: this thread's earlier writes are visible to whoever
+// acquires the counter's new value.
+__device__ __forceinline__ void red_add_release_gpu(uint32_t* p, uint32_t v) {
+    asm volatile("red.release.gpu.global.add.u32 [%0], %1;\n" ::"l"(p), "r"(v) : "memory");
+}
+// Waits, for at most limit_ns, until *p == want (acquire: the writes released
+// with the flag are visible afterwards); false on time-out or abort.
+__device__ __forceinline__ bool wait_flag_gpu(const uint32_t* p, uint32_t want, volatile int* abort,
+                                              uint64_t limit_ns) {
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t n = 0;; ++n) {
+        if (ld_acquire_gpu(p) == want) return true;
+        if ((n & 15u) == 15u && (*abort || globaltimer_ns() - t0 > limit_ns)) return false;
+        __nanosleep(64);
+    }
+}
+
 __device__ __forceinline__ void cluster_arrive_release() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n" ::: "memory");
 }
@@ -182,6 +208,11 @@ __device__ __forceinline__ void cp_async_mbar_arrive_noinc(uint32_t bar) {
 
 __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+}
+
+// Prefetch `bytes` (a multiple of 16, 16-byte aligned) of global memory into L2.
+__device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;\n" ::"l"(src), "r"(bytes) : "memory");
 }
 
 // 1-D bulk copy global -> shared, completing `bytes` of transaction count on bar.
