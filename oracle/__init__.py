@@ -21,6 +21,10 @@ Status of the pins (tests/test_oracle_pins.py):
     w4a16_asym                   zero and values recovered; code range and the
                                  half-step bound; the layer on such weights equals
                                  a numpy fp64 matmul; one-hot rows)
+  * svd_lora                  -- pinned (a planted low-rank quantisation error is
+                                 recovered exactly; full rank leaves no error;
+                                 exactly representable W gives no LoRA; one round
+                                 reduces to the plain quantiser; errors fall)
   * silu_mul                  -- pinned (closed forms: silu(0) = 0, silu(ln 3) =
                                  (3/4) ln 3, silu(v) -> v and -> 0 in the tails;
                                  the gate/up column split on crafted rows)
@@ -273,6 +277,46 @@ def w4a16_asym_linear(X, W, L_down, L_up, colscale, bias) -> np.ndarray:
     """fp64 Y [M, N] of the W4A16 layer with asymmetric group-128 weights, from raw inputs."""
     q, s, z = quantize_weights_asym(W)
     return w4a16_asym_from_codes(X, q, s, z, lora_down(X, L_down), L_up, colscale, bias)
+
+
+def dequantize_weights(qW: np.ndarray, sW: np.ndarray) -> np.ndarray:
+    """fp64 [N, K]: codes times their fp16 group-64 scale."""
+    q = np.asarray(qW, np.float64)
+    s = f16_to_f32_array(np.asarray(sW, np.uint16)).astype(np.float64)
+    return q * np.repeat(s, GROUP, axis=1)
+
+
+def truncated_svd(A: np.ndarray, r: int):
+    """Rank-r truncated SVD of A in fp64 (LAPACK): U [N, r], S [r], V [K, r]."""
+    U, S, Vt = np.linalg.svd(np.asarray(A, np.float64), full_matrices=False)
+    return U[:, :r], S[:r], Vt[:r].T
+
+
+def svd_lora(W: np.ndarray, r: int, rounds: int = 3):
+    """LoRA correction of the INT4 weights from W alone ("W4A4 CUDA Kernel for
+    Voice Clone", 2.1: the quantisation error E = W - Q(W) and its rank-r SVD,
+    L_up = (U_r S_r)^T, L_down = V_r; 2.2: rounds that quantise W - LoRA_previous
+    and refit the SVD to the new error, stopping when the error stops falling),
+    with the plain round-to-nearest quantiser in place of GPTQ (no calibration
+    data).  The residual handed to the quantiser is rounded to fp32, its input
+    type.  Returns the round with the smallest ||W - Q - L_down L_up^T||_F as a
+    dict (codes, scales, L_down fp64 [K, r], L_up fp64 [r, N], err) and the list
+    of every round's error."""
+    W64 = np.asarray(W, np.float32).astype(np.float64)
+    LW = np.zeros_like(W64)
+    best, errs = None, []
+    for _ in range(rounds):
+        q, sc = quantize_weights((W64 - LW).astype(np.float32))
+        E = W64 - dequantize_weights(q, sc)
+        U, S, V = truncated_svd(E, r)
+        L_new = (U * S) @ V.T
+        err = float(np.linalg.norm(E - L_new))
+        errs.append(err)
+        if best is not None and err >= best["err"]:
+            break
+        best = dict(codes=q, scales=sc, L_down=V, L_up=(U * S).T, err=err)
+        LW = L_new
+    return best, errs
 
 
 def silu_mul(Y: np.ndarray) -> np.ndarray:

@@ -488,3 +488,58 @@ def test_silu_mul_sampled_matches_full():
     rows, cols = np.array([0, 3, 8, 8]), np.array([0, 31, 5, 31])
     Hs = oracle.silu_mul_linear_sampled(c.X, c.W, c.L_down, c.L_up, c.colscale, c.bias, rows, cols)
     assert np.array_equal(Hs, H[rows, cols])
+
+
+# ---- LoRA from the quantisation error ("W4A4 CUDA Kernel for Voice Clone", 2.1-2.2)
+def planted_rank_case(N=96, K=256, rank=2, seed=41):
+    """W = Q0 + D with Q0 = q0 s0 exactly quantisable (one element of each group at
+    exactly 7 s0, the others |q0| <= 6) and D of rank `rank`, |D| <= 0.4 s0 and zero
+    at the groups' first columns: the quantiser returns (q0, s0), so the error is D."""
+    rng = np.random.default_rng(seed)
+    G = K // 64
+    s0 = np.ldexp(1.0, -rng.integers(6, 9, size=(N, G)))
+    q0 = rng.integers(-6, 7, size=(N, K))
+    q0[:, ::64] = 7
+    u = rng.uniform(-1, 1, size=(N, rank))
+    v = rng.uniform(-1, 1, size=(K, rank))
+    v[::64] = 0.0
+    D = u @ v.T
+    smin = np.repeat(s0, 64, axis=1)
+    D *= 0.4 * smin.min() / np.abs(D).max()
+    W = (q0 * smin + D).astype(np.float32)
+    return W, q0, s0, D
+
+
+def test_svd_lora_recovers_a_planted_low_rank_error():
+    W, q0, s0, D = planted_rank_case()
+    best, errs = oracle.svd_lora(W, r=4, rounds=3)
+    assert np.array_equal(best["codes"], q0)
+    assert np.array_equal(oracle.f16_to_f32_array(best["scales"]).astype(np.float64), s0)
+    L = (best["L_down"] @ best["L_up"]).T
+    scale = np.linalg.norm(D)
+    assert np.linalg.norm(L - D) <= 1e-6 * scale   # (fp32 rounding of W leaves ~1e-8)
+    assert best["err"] <= 1e-5 * scale   # what is left is the fp32 rounding of W (~1e-7 here)
+
+
+def test_svd_lora_full_rank_and_representable_weights():
+    c = make_linear_case(1, 128, 32, 0, seed=42)
+    best, _ = oracle.svd_lora(c.W, r=32, rounds=1)     # rank = min(N, K): no error left
+    assert best["err"] <= 1e-12 * np.linalg.norm(c.W)
+    W, q0, s0, _ = planted_rank_case(N=32, K=128, rank=1)
+    Wq = (q0 * np.repeat(s0, 64, axis=1)).astype(np.float32)  # exactly representable
+    best, errs = oracle.svd_lora(Wq, r=8, rounds=3)
+    assert best["err"] == 0.0 and np.abs(best["L_up"]).max() == 0.0
+
+
+def test_svd_lora_one_round_is_the_plain_quantiser_and_errors_fall():
+    c = make_linear_case(1, 256, 64, 0, seed=43)
+    best, errs = oracle.svd_lora(c.W, r=16, rounds=1)
+    qW, sW = oracle.quantize_weights(c.W)
+    assert np.array_equal(best["codes"], qW) and np.array_equal(best["scales"], sW)
+    E = c.W.astype(np.float64) - oracle.dequantize_weights(qW, sW)
+    # the rank-16 correction removes the 16 largest singular values' energy
+    sv = np.linalg.svd(E, compute_uv=False)
+    assert abs(best["err"] - np.sqrt((sv[16:] ** 2).sum())) <= 1e-9 * np.linalg.norm(E)
+    best3, errs3 = oracle.svd_lora(c.W, r=16, rounds=3)
+    assert errs3[0] == errs[0] and best3["err"] <= errs3[0]
+    assert all(e2 < e1 for e1, e2 in zip(errs3[:-2], errs3[1:-1]))
