@@ -167,6 +167,32 @@ w4a4_status w4a4_linear_silu_mul(const void* act_ws, size_t act_ws_bytes, const 
                                  const uint16_t* colscale, const uint16_t* bias, int M, int N, int K, int r,
                                  uint16_t* H, cudaStream_t stream);
 
+/* ---- LoRA from the quantisation error ([VC] 2.1-2.2; offline, synchronous)
+ * w4a4_pack_weights_svd quantises W fp32 [N, K] like w4a4_pack_weights and
+ * derives the LoRA factors from the error instead of taking them: in each of
+ * `rounds` rounds, W - LoRA_previous (W in the first) is quantised (the
+ * packer's round-to-nearest in place of GPTQ), E = W - Q is formed and its
+ * rank-r SVD U S V^T taken (randomized subspace iteration with `power_iters`
+ * power steps on a block of 64 or 128 columns, start block drawn
+ * from `seed`); the rounds stop once the residual ||E - U S V^T||_F stops
+ * falling.  The round with the smallest residual is kept: its codes and
+ * scales go into `packed` together with L_down = fp16(V) [K, r] and
+ * L_up = fp16((U S)^T) [r, N], which are also written to the device buffers
+ * L_down, L_up.  errs (host, may be NULL) receives each round's residual
+ * (fp32; -1 for rounds not run).  16 <= r <= 128; scratch: device memory of
+ * w4a4_svd_lora_scratch_bytes(N, K, r) bytes.  16 power steps give the
+ * residual within ~1e-4 of the exact truncated SVD's on quantisation errors.
+ * w4a4_truncated_svd exposes the rank-r SVD alone: A fp32 [N, K] -> U [N, r],
+ * S [r], V [K, r] (fp32, device), with the same scratch. */
+size_t w4a4_svd_lora_scratch_bytes(int N, int K, int r);
+w4a4_status w4a4_pack_weights_svd(const float* W, int N, int K, int r, int rounds, int power_iters,
+                                  unsigned long long seed, void* packed, size_t packed_bytes, uint16_t* L_down,
+                                  uint16_t* L_up, float* errs, void* scratch, size_t scratch_bytes,
+                                  cudaStream_t stream);
+w4a4_status w4a4_truncated_svd(const float* A, int N, int K, int r, int power_iters, unsigned long long seed,
+                               float* U, float* S, float* V, void* scratch, size_t scratch_bytes,
+                               cudaStream_t stream);
+
 /* Same as w4a4_linear with an explicit kernel choice (tests, measurements). */
 w4a4_status w4a4_linear_select(const void* act_ws, size_t act_ws_bytes, const void* packed,
                                size_t packed_bytes, const uint16_t* colscale, const uint16_t* bias,

@@ -53,6 +53,9 @@ SIGNATURES = {
     "w4a16_linear": (I, [P, P, Z, P, P, I, I, I, I, P, P]),
     "w4a16_pack_weights_asym": (I, [P, P, P, I, I, I, P, Z, P]),
     "w4a4_pack_weights_gate_up": (I, [P, P, P, I, I, I, P, Z, P]),
+    "w4a4_svd_lora_scratch_bytes": (Z, [I, I, I]),
+    "w4a4_pack_weights_svd": (I, [P, I, I, I, I, I, ctypes.c_ulonglong, P, Z, P, P, P, P, Z, P]),
+    "w4a4_truncated_svd": (I, [P, I, I, I, I, ctypes.c_ulonglong, P, P, P, P, Z, P]),
     "w4a4_linear_silu_mul": (I, [P, Z, P, Z, P, P, I, I, I, I, P, P]),
     "w4a16_linear_asym": (I, [P, P, Z, P, P, I, I, I, I, P, P]),
     "w4a4_debug_unpack_weights": (I, [P, I, I, I, P, P, P, P, P]),
@@ -169,6 +172,45 @@ def w4a4_linear_silu_mul(act_ws, packed, colscale, bias, H, K: int, r: int, stre
     M, I = H.shape
     _check(lib().w4a4_linear_silu_mul(_ptr(act_ws), _nbytes(act_ws), _ptr(packed), _nbytes(packed), _ptr(colscale),
                                       _ptr(bias), M, 2 * I, K, r, _ptr(H), _stream(stream)), "w4a4_linear_silu_mul")
+
+
+def svd_lora_scratch_bytes(N: int, K: int, r: int) -> int:
+    n = lib().w4a4_svd_lora_scratch_bytes(N, K, r)
+    if n == 0:
+        raise W4A4Error(2, "w4a4_svd_lora_scratch_bytes")
+    return n
+
+
+def w4a4_pack_weights_svd(W, r: int, packed, rounds: int = 3, power_iters: int = 16, seed: int = 0,
+                          scratch=None, stream=None):
+    """Quantise W [N, K] and derive its rank-r LoRA from the quantisation error
+    (SVD refit rounds).  Returns (L_down fp16 [K, r], L_up fp16 [r, N], per-round
+    residuals) and fills `packed`."""
+    N, K = W.shape
+    dev = W.device
+    Ld = torch.empty((K, r), dtype=torch.float16, device=dev)
+    Lu = torch.empty((r, N), dtype=torch.float16, device=dev)
+    if scratch is None:
+        scratch = torch.empty(svd_lora_scratch_bytes(N, K, r), dtype=torch.uint8, device=dev)
+    errs = (ctypes.c_float * rounds)()
+    _check(lib().w4a4_pack_weights_svd(_ptr(W), N, K, r, rounds, power_iters, seed, _ptr(packed), _nbytes(packed),
+                                       _ptr(Ld), _ptr(Lu), ctypes.cast(errs, ctypes.c_void_p), _ptr(scratch),
+                                       _nbytes(scratch), _stream(stream)), "w4a4_pack_weights_svd")
+    return Ld, Lu, [float(e) for e in errs]
+
+
+def w4a4_truncated_svd(A, r: int, power_iters: int = 16, seed: int = 0, scratch=None, stream=None):
+    """Rank-r SVD of A fp32 [N, K] on the GPU: (U [N, r], S [r], V [K, r])."""
+    N, K = A.shape
+    dev = A.device
+    U = torch.empty((N, r), dtype=torch.float32, device=dev)
+    S = torch.empty((r,), dtype=torch.float32, device=dev)
+    V = torch.empty((K, r), dtype=torch.float32, device=dev)
+    if scratch is None:
+        scratch = torch.empty(svd_lora_scratch_bytes(N, K, r), dtype=torch.uint8, device=dev)
+    _check(lib().w4a4_truncated_svd(_ptr(A), N, K, r, power_iters, seed, _ptr(U), _ptr(S), _ptr(V), _ptr(scratch),
+                                    _nbytes(scratch), _stream(stream)), "w4a4_truncated_svd")
+    return U, S, V
 
 
 def w4a16_pack_weights_asym(W, L_down, L_up, packed, r: int, stream=None):

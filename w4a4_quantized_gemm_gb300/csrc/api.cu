@@ -212,6 +212,45 @@ w4a4_status w4a4_pack_weights_gate_up(const float* W, const uint16_t* L_down, co
     return pack_common(W, nullptr, nullptr, L_down, L_up, N, K, r, packed, packed_bytes, stream, N / 2);
 }
 
+size_t w4a4_svd_lora_scratch_bytes(int N, int K, int r) {
+    if (check_kn(N, K, r) != W4A4_OK || r < 16) return 0;
+    return svd_scratch_bytes(N, K, r);
+}
+
+w4a4_status w4a4_pack_weights_svd(const float* W, int N, int K, int r, int rounds, int power_iters,
+                                  unsigned long long seed, void* packed, size_t packed_bytes, uint16_t* L_down,
+                                  uint16_t* L_up, float* errs, void* scratch, size_t scratch_bytes,
+                                  cudaStream_t stream) {
+    w4a4_status st = check_kn(N, K, r);
+    if (st != W4A4_OK) return st;
+    if (r < 16) return W4A4_ERR_UNSUPPORTED_SHAPE;
+    if (rounds < 1 || rounds > 16 || power_iters < 0 || power_iters > 64) return W4A4_ERR_INVALID_ARG;
+    if (!W || !packed || !L_down || !L_up || !scratch) return W4A4_ERR_INVALID_ARG;
+    if (!aligned16(W) || !aligned16(packed) || !aligned16(L_down) || !aligned16(L_up) || !aligned16(scratch))
+        return W4A4_ERR_MISALIGNED;
+    if (packed_bytes < packed_layout(N, K, r).total || scratch_bytes < svd_scratch_bytes(N, K, r))
+        return W4A4_ERR_WORKSPACE;
+    if ((st = check_device()) != W4A4_OK) return st;
+    set_dispatch("pack_weights_svd N=%d K=%d r=%d rounds=%d power=%d", N, K, r, rounds, power_iters);
+    return run_svd_lora(W, N, K, r, rounds, power_iters, seed, static_cast<uint8_t*>(packed), L_down, L_up, errs,
+                        static_cast<uint8_t*>(scratch), stream);
+}
+
+w4a4_status w4a4_truncated_svd(const float* A, int N, int K, int r, int power_iters, unsigned long long seed,
+                               float* U, float* S, float* V, void* scratch, size_t scratch_bytes,
+                               cudaStream_t stream) {
+    w4a4_status st = check_kn(N, K, r);
+    if (st != W4A4_OK) return st;
+    if (r < 16) return W4A4_ERR_UNSUPPORTED_SHAPE;
+    if (power_iters < 0 || power_iters > 64) return W4A4_ERR_INVALID_ARG;
+    if (!A || !U || !S || !V || !scratch) return W4A4_ERR_INVALID_ARG;
+    if (!aligned16(A) || !aligned16(U) || !aligned16(V) || !aligned16(scratch)) return W4A4_ERR_MISALIGNED;
+    if (scratch_bytes < svd_scratch_bytes(N, K, r)) return W4A4_ERR_WORKSPACE;
+    if ((st = check_device()) != W4A4_OK) return st;
+    set_dispatch("truncated_svd N=%d K=%d r=%d power=%d", N, K, r, power_iters);
+    return run_truncated_svd(A, N, K, r, power_iters, seed, U, S, V, static_cast<uint8_t*>(scratch), stream);
+}
+
 w4a4_status w4a4_pack_weight_codes(const int8_t* codes, const uint16_t* scales, const uint16_t* L_down,
                                    const uint16_t* L_up, int N, int K, int r, void* packed, size_t packed_bytes,
                                    cudaStream_t stream) {

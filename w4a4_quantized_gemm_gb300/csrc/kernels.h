@@ -43,6 +43,13 @@ w4a4_status launch_gemm_smallm_tc(const uint8_t* ws, const uint8_t* packed, cons
 w4a4_status launch_gemm_w4a16(const uint16_t* X, const uint8_t* packed, const uint16_t* colscale,
                               const uint16_t* bias, int M, int N, int K, int r, uint16_t* Y, bool asym,
                               cudaStream_t s);
+// svd_lora.cu (LoRA from the quantisation error; synchronous)
+size_t svd_scratch_bytes(int N, int K, int r);
+w4a4_status run_truncated_svd(const float* A, int N, int K, int r, int power, unsigned long long seed, float* U,
+                              float* S, float* V, uint8_t* scratch, cudaStream_t st);
+w4a4_status run_svd_lora(const float* W, int N, int K, int r, int rounds, int power, unsigned long long seed,
+                         uint8_t* packed, uint16_t* L_down, uint16_t* L_up, float* errs, uint8_t* scratch,
+                         cudaStream_t st);
 void launch_rmsnorm_f16(const uint16_t* Y, int M, int ld_y, int K, double eps, uint16_t* X, cudaStream_t s);
 
 }  // namespace w4a4
