@@ -335,6 +335,22 @@ def run_ours(args, rank, world, local_rank):
     lin_reps = max(4, reps // R)
     q_us = {n: 1e3 * timed(capture(one_linear(n, "q"))[:1], lin_reps) / (lin_reps * R) for n in names}
     g_us = {n: 1e3 * timed(capture(one_linear(n, "g"))[:1], lin_reps) / (lin_reps * R) for n in names}
+    # the gate_up linear with the SiLU(gate) * up epilogue (fused gate|up weights packed in
+    # the epilogue's order, H [M, N/2] out), on the same activations, against its plain GEMM
+    gu = L["gate_up"]
+    cgu = gu["c"]
+    Wgu = torch.from_numpy(cgu.W).to(dev)
+    pk_silu = torch.empty_like(gu["packed"][0])
+    w4.w4a4_pack_weights_gate_up(Wgu, torch.from_numpy(cgu.L_down.view(np.float16).copy()).to(dev),
+                                 torch.from_numpy(cgu.L_up.view(np.float16).copy()).to(dev), pk_silu, cgu.r)
+    del Wgu
+    pks_silu = [pk_silu.clone() for _ in range(R)]
+    Hs = [torch.empty((cgu.M, cgu.N // 2), dtype=torch.float16, device=dev) for _ in range(R)]
+    w4.w4a4_linear_silu_mul(gu["ws"][0], pks_silu[0], gu["cs"][0], gu["b"][0], Hs[0], cgu.K, cgu.r)
+    silu_dispatch = w4.w4a4_last_dispatch()
+    silu_graph = capture(lambda rep, st: [w4.w4a4_linear_silu_mul(gu["ws"][j], pks_silu[j], gu["cs"][j], gu["b"][j],
+                                                                   Hs[j], cgu.K, cgu.r, st) for j in range(R)])
+    silu_us = 1e3 * timed(silu_graph[:1], lin_reps) / (lin_reps * R)
     peaks = {}
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -353,6 +369,7 @@ def run_ours(args, rank, world, local_rank):
                 "peak_source": f"{peak_src} bf16 burst x 2 (fp8 kind)",
                 "gemm_us_per_step": gemm_s * 1e6, "quantize_us_per_step": q_s * 1e6,
                 "per_linear_gemm_us": g_us, "per_linear_quantize_us": q_us,
+                "gate_up_silu_mul_us": silu_us, "gate_up_silu_mul_dispatch": silu_dispatch,
                 "gemm_algorithmic_bytes": sum(metrics.gemm_bytes(**DECODER_LAYER_M700[n]) for n in names),
                 "quantize_algorithmic_bytes": sum(metrics.act_bytes(DECODER_LAYER_M700[n]["M"],
                                                                     DECODER_LAYER_M700[n]["K"],
@@ -646,6 +663,18 @@ def run_decode(args, rank, world, local_rank):
     w4.w4a4_pack_weights(W, Ld, Lu, packed0, base.r)
     del W
     packs = [packed0.clone() for _ in range(R)]
+    # the same weights as asymmetric group-128 codes (fp16 scale + zero point), for the W4A16 variant
+    W = torch.from_numpy(base.W).to(dev)
+    packed_a = torch.empty_like(packed0)
+    w4.w4a16_pack_weights_asym(W, Ld, Lu, packed_a, base.r)
+    packs_a = [packed_a.clone() for _ in range(R)]
+    # LoRA from the quantisation error (offline): one K=N=4096, r=32 layer, 3 rounds, 16 power steps
+    torch.cuda.synchronize()
+    t_svd = time.perf_counter()
+    _, _, svd_errs = w4.w4a4_pack_weights_svd(W, base.r, torch.empty_like(packed0), rounds=3, power_iters=16)
+    torch.cuda.synchronize()
+    svd_s = time.perf_counter() - t_svd
+    del W
     cs = torch.from_numpy(base.colscale.view(np.float16).copy()).to(dev)
     b = torch.from_numpy(base.bias.view(np.float16).copy()).to(dev)
     wbytes = metrics.weight_bytes(base.N, base.K)
@@ -685,13 +714,19 @@ def run_decode(args, rank, world, local_rank):
         with torch.cuda.graph(gw):
             for p_ in packs:
                 w4.w4a16_linear(X, p_, cs, b, Y, base.r, torch.cuda.current_stream())
+        ga = torch.cuda.CUDAGraph()  # the W4A16 linear on asymmetric group-128 weights
+        with torch.cuda.graph(ga):
+            for p_ in packs_a:
+                w4.w4a16_linear_asym(X, p_, cs, b, Y, base.r, torch.cuda.current_stream())
         torch.cuda.synchronize()
         us = tm(g)
         uq = tm(gq)
         uw = tm(gw)
+        ua = tm(ga)
         results[M] = {"gemm_us": us, "quantize_us": uq, "weight_gbs": wbytes / (us * 1e-6) / 1e9,
                       "frac_hbm": wbytes / (us * 1e-6) / 1e9 / hbm, "dispatch": disp,
-                      "w4a16_linear_us": uw, "w4a16_weight_gbs": wbytes / (uw * 1e-6) / 1e9}
+                      "w4a16_linear_us": uw, "w4a16_weight_gbs": wbytes / (uw * 1e-6) / 1e9,
+                      "w4a16_asym_g128_us": ua, "w4a16_asym_g128_weight_gbs": wbytes / (ua * 1e-6) / 1e9}
         if M == 32 and not args.no_e2e:
             # end to end through the public API at the metric's binding M: pinned host X in, the two
             # C-ABI calls per weight replica, Y back to pinned host, all in one graph
@@ -720,7 +755,10 @@ def run_decode(args, rank, world, local_rank):
         "vs_baseline": None, "dtype": "int4 codes (fp8 e4m3 operands), fp32 accumulate, fp16 out",
         "data": "synthetic",
         "config": {"workload": "small_m_sweep_K4096_N4096", "group": 64, "rank": 32, "replicas": R,
-                   "l2": f"{R} weight replicas, {R * wbytes / 2**20:.0f} MiB > L2", "per_M": results},
+                   "l2": f"{R} weight replicas, {R * wbytes / 2**20:.0f} MiB > L2", "per_M": results,
+                   "svd_lora": {"seconds_per_layer": svd_s, "rounds": 3, "power_iters": 16,
+                                "residual_per_round": svd_errs,
+                                "what": "w4a4_pack_weights_svd on the K=N=4096 weights, r=32 (offline)"}},
         "gpu_launches": args.steps * R * len(results) * 2, "e2e": e2e, "clocks": sampler.summary(),
         "roofline": {"bound": "hbm", "achieved": low, "peak": hbm, "unit": "GB/s", "frac": low / hbm,
                      "traffic": None, "kernel": "w4a4_linear (small-M weight-streaming kernel)",

@@ -9,13 +9,16 @@
 // Tropp, "Finding structure with randomness", 2011, Algorithm 4.4) on a block
 // of s = 64 or 128 columns: Y = A Omega; q times { Z = orth(A^T Q); Q = orth(A Z) };
 // B^T = A^T Q; the eigen-decomposition B B^T = W diag(lambda) W^T gives
-// U = Q W, S = sqrt(lambda), V = B^T W / S.  Orthonormalisation goes through
-// the Gram matrix: G = Y^T Y (fp64), G = W diag(mu) W^T, Q = Y W diag(mu)^-1/2
-// (directions with mu below 1e-10 mu_max -- singular values below 1e-5 of the
-// largest, where fp32 products carry only rounding noise -- are dropped), which
-// tolerates the rank-deficient blocks of an exactly low-rank error.  Symmetric
-// eigen-decompositions are cyclic Jacobi sweeps (parallel round-robin order)
-// in one CTA.  The residual ||E - U S V^T||_F^2 = ||E||_F^2 - sum_{i<r} lambda_i.
+// U = Q W, S = sqrt(lambda), V = B^T W / S.  Orthonormalisation is shifted
+// Cholesky QR applied twice (Fukaya, Kannan, Nakatsukasa, Yamamoto and Yanagisawa,
+// "Shifted Cholesky QR for computing the QR factorization of ill-conditioned
+// matrices", 2020): G = Y^T Y (fp64), G + s I = R^T R with s = 1e-11 tr(G),
+// Y <- Y R^-1; the shift keeps the factorisation defined for the rank-deficient
+// blocks of an exactly low-rank error, the second pass restores orthogonality.
+// The final eigen-decomposition is cyclic Jacobi (parallel round-robin order)
+// in fp64 in one CTA, where eigenvalues below 1e-10 of the largest (singular
+// values below 1e-5, fp32 rounding noise) are dropped.  The residual
+// ||E - U S V^T||_F^2 = ||E||_F^2 - sum_{i<r} lambda_i.
 //
 // All arithmetic runs in these kernels; the host only sequences the launches
 // and reads each round's error (the rounds stop on it).
@@ -181,16 +184,33 @@ __global__ void __launch_bounds__(1024) jacobi_eig_kernel(const double* __restri
     }
     for (int e = tid; e < S; e += nt) pr[e] = e;
     __syncthreads();
-    double frob = 0.0;
-    for (int e = 0; e < S * S; ++e) frob += a[e] * a[e];  // every thread, the same order
-    for (int sweep = 0; sweep < 30; ++sweep) {
+    __shared__ double frob, red[32];
+    auto block_sum = [&](double v) {  // fixed-order block reduction, result in red[0]
+        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+        __syncthreads();
+        if ((tid & 31) == 0) red[tid >> 5] = v;
+        __syncthreads();
         if (tid == 0) {
-            double o = 0.0;
-            for (int i = 0; i < S; ++i)
-                for (int j = 0; j < S; ++j)
-                    if (i != j) o += a[i * S + j] * a[i * S + j];
-            off = o;
+            double t = 0.0;
+            for (int w = 0; w < (nt + 31) / 32; ++w) t += red[w];
+            red[0] = t;
         }
+        __syncthreads();
+        return red[0];
+    };
+    {
+        double f = 0.0;
+        for (int e = tid; e < S * S; e += nt) f += a[e] * a[e];
+        const double tf = block_sum(f);
+        if (tid == 0) frob = tf;
+    }
+    __syncthreads();
+    for (int sweep = 0; sweep < 30; ++sweep) {
+        double o = 0.0;
+        for (int e = tid; e < S * S; e += nt)
+            if (e / S != e % S) o += a[e] * a[e];
+        const double to = block_sum(o);
+        if (tid == 0) off = to;
         __syncthreads();
         if (off <= 1e-28 * frob) break;
         for (int step = 0; step < S - 1; ++step) {
@@ -270,6 +290,56 @@ __global__ void __launch_bounds__(1024) jacobi_eig_kernel(const double* __restri
             const double l = a[ord[col] * S + ord[col]];
             T[e] = (l > 1e-10 * lmax && l > 0.0) ? float(double(w) / sqrt(l)) : 0.f;
         }
+    }
+}
+
+// T = R^-1 (fp32, upper triangular) for G + s I = R^T R, s = 1e-11 tr(G), G
+// fp64 S x S symmetric positive semidefinite; one CTA.  Right-looking
+// Cholesky of the lower factor L = R^T in shared memory, then the columns of
+// L^-1 by forward substitution, one column per thread; T = (L^-1)^T.
+__global__ void __launch_bounds__(256) chol_inv_kernel(const double* __restrict__ G, int S,
+                                                       float* __restrict__ T) {
+    extern __shared__ double cm[];  // L [S][S] fp64, then X = L^-1 [S][S] fp32 (fp64 sums)
+    double* a = cm;
+    float* x = reinterpret_cast<float*>(cm + S * S);
+    __shared__ double shift;
+    const int tid = threadIdx.x, nt = blockDim.x;
+    for (int e = tid; e < S * S; e += nt) a[e] = G[e];
+    __syncthreads();
+    if (tid == 0) {
+        double tr = 0.0;
+        for (int i = 0; i < S; ++i) tr += a[i * S + i];
+        shift = tr > 0.0 ? 1e-11 * tr : 1e-300;
+    }
+    __syncthreads();
+    for (int i = tid; i < S; i += nt) a[i * S + i] += shift;
+    __syncthreads();
+    for (int k = 0; k < S; ++k) {
+        if (tid == 0) a[k * S + k] = sqrt(a[k * S + k] > shift ? a[k * S + k] : shift);
+        __syncthreads();
+        const double d = a[k * S + k];
+        for (int i = k + 1 + tid; i < S; i += nt) a[i * S + k] /= d;
+        __syncthreads();
+        // trailing lower triangle: a[i][j] -= a[i][k] a[j][k], k < j <= i
+        const int m = S - k - 1;
+        for (int e = tid; e < m * m; e += nt) {
+            const int i = k + 1 + e / m, j = k + 1 + e % m;
+            if (j <= i) a[i * S + j] -= a[i * S + k] * a[j * S + k];
+        }
+        __syncthreads();
+    }
+    // X = L^-1, column c by forward substitution (threads over columns)
+    for (int c = tid; c < S; c += nt) {
+        for (int i = 0; i < S; ++i) {
+            double v = (i == c) ? 1.0 : 0.0;
+            for (int j = c; j < i; ++j) v -= a[i * S + j] * double(x[j * S + c]);
+            x[i * S + c] = i < c ? 0.f : float(v / a[i * S + i]);
+        }
+    }
+    __syncthreads();
+    for (int e = tid; e < S * S; e += nt) {
+        const int i = e / S, j = e % S;
+        T[e] = x[j * S + i];  // (L^-1)^T: upper triangular R^-1
     }
 }
 
@@ -415,13 +485,15 @@ struct Svd {
         return sizeof(double) * S * S + sizeof(float) * S * S + sizeof(int) * (S + (S & 1)) +
                sizeof(double) * S + sizeof(int) * S;
     }
-    // M [rows, S] <- M . T with T from the eigen-decomposition of M^T M (orthonormal columns)
+    // M [rows, S] <- M R^-1, twice (shifted Cholesky QR): orthonormal columns
     template <int SS>
     void orth(float* M, int rows, float* tmp) const {
-        gram_kernel<<<dim3(SS / 16, SS / 16), 256, 0, st>>>(M, rows, SS, d(L.G));
-        jacobi_eig_kernel<<<1, 1024, eig_smem(), st>>>(d(L.G), SS, r, f(L.Wv), d(L.lam), f(L.T), nullptr);
-        nn<SS>(M, rows, SS, SS, f(L.T), tmp);
-        cudaMemcpyAsync(M, tmp, sizeof(float) * size_t(rows) * SS, cudaMemcpyDeviceToDevice, st);
+        for (int pass = 0; pass < 2; ++pass) {
+            gram_kernel<<<dim3(SS / 16, SS / 16), 256, 0, st>>>(M, rows, SS, d(L.G));
+            chol_inv_kernel<<<1, 256, (sizeof(double) + sizeof(float)) * SS * SS, st>>>(d(L.G), SS, f(L.T));
+            nn<SS>(M, rows, SS, SS, f(L.T), tmp);
+            cudaMemcpyAsync(M, tmp, sizeof(float) * size_t(rows) * SS, cudaMemcpyDeviceToDevice, st);
+        }
     }
     // rank-r SVD of the N x K matrix at L.A: U [N, S], V [K, S] (first r columns used),
     // eigenvalues lam[S] (singular values squared), sum of the first r at sum[0]
@@ -470,7 +542,9 @@ w4a4_status eig_attr(int S) {
     const size_t smem = sizeof(double) * S * S + sizeof(float) * S * S + sizeof(int) * (S + (S & 1)) +
                         sizeof(double) * S + sizeof(int) * S;
     if (cudaFuncSetAttribute(jacobi_eig_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) !=
-        cudaSuccess)
+            cudaSuccess ||
+        cudaFuncSetAttribute(chol_inv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             int((sizeof(double) + sizeof(float)) * S * S)) != cudaSuccess)
         return W4A4_ERR_CUDA;
     return W4A4_OK;
 }
