@@ -61,7 +61,7 @@ __global__ void __launch_bounds__(kWarps * 32) quantize_act_kernel(const uint16_
                                                                    const uint2* __restrict__ Ldp, int M,
                                                                    int K, uint8_t* __restrict__ ws) {
     extern __shared__ __align__(16) uint8_t qsm[];
-    __shared__ double ssq[kWarps][kRows], row_inv[kRows];
+    __shared__ double ssq[kWarps][kRows], row_part[kRows], row_inv[kRows];
     pdl_wait();
     pdl_launch_dependents();
     uint16_t(*xs)[kRows * kXsStride] = reinterpret_cast<uint16_t(*)[kRows * kXsStride]>(qsm);
@@ -97,10 +97,12 @@ __global__ void __launch_bounds__(kWarps * 32) quantize_act_kernel(const uint16_
     double inv = 1.0;
     float inva = 1.f, invb = 0.f;
     if constexpr (NORM) {
-        // sum of squares of row qrow over all K columns (this lane's half of each
-        // of the warp's groups, then the lane pair, then the 8 warps in order)
+        // sum of squares of row qrow over this CTA's groups (this lane's half of each
+        // of the warp's groups, then the lane pair, then the 8 warps in order); the
+        // cluster's CTAs then add their partial sums in rank order, so every CTA of
+        // the cluster holds the same total
         float hi = 0.f, lo = 0.f;
-        for (int g0 = warp; g0 < G; g0 += kWarps) {
+        for (int g0 = g_begin + warp; g0 < g_end; g0 += kWarps) {
             uint4 v[4];
 #pragma unroll
             for (int i = 0; i < 4; ++i)
@@ -116,6 +118,12 @@ __global__ void __launch_bounds__(kWarps * 32) quantize_act_kernel(const uint16_
             double t = 0.0;
 #pragma unroll
             for (int w = 0; w < kWarps; ++w) t += ssq[w][threadIdx.x];
+            row_part[threadIdx.x] = t;
+        }
+        cluster.sync();
+        if (threadIdx.x < kRows) {
+            double t = 0.0;
+            for (int c = 0; c < CK; ++c) t += cluster.map_shared_rank(row_part, c)[threadIdx.x];
             row_inv[threadIdx.x] = 1.0 / sqrt(t / double(K) + W4A4_RMSNORM_EPS);
         }
         __syncthreads();
@@ -271,6 +279,7 @@ __global__ void __launch_bounds__(kWarps * 32) quantize_act_kernel(const uint16_
         }
         cluster.sync();  // peers' shared memory stays alive until every read is done
     }
+    if constexpr (NORM && R == 0) cluster.sync();  // (the peers' reads of row_part are done)
 }
 
 __global__ void unpack_act_kernel(const uint8_t* __restrict__ ws, int M, int K, int r, int8_t* codes,
