@@ -63,13 +63,14 @@ w4a4_status sync_status(cudaStream_t s) {
     }
     return W4A4_OK;
 }
-// Reads and clears the status words of both GEMM kernels' bounded waits.
+// Reads and clears the status words of every kernel with bounded waits.
 w4a4_status device_status_words() {
     const w4a4_status a = tc_read_and_clear_status();
     const w4a4_status b = smallm_read_and_clear_status();
     const w4a4_status c = w4a16_read_and_clear_status();
     const w4a4_status d = smtc_read_and_clear_status();
-    return a != W4A4_OK ? a : b != W4A4_OK ? b : c != W4A4_OK ? c : d;
+    const w4a4_status e = q_read_and_clear_status();
+    return a != W4A4_OK ? a : b != W4A4_OK ? b : c != W4A4_OK ? c : d != W4A4_OK ? d : e;
 }
 }  // namespace
 

@@ -190,4 +190,5 @@ w4a4_status tc_read_and_clear_status();      // bounded-wait status of the tcgen
 w4a4_status smallm_read_and_clear_status();  // bounded-wait status of the small-M kernel
 w4a4_status w4a16_read_and_clear_status();   // bounded-wait status of the W4A16 kernel
 w4a4_status smtc_read_and_clear_status();    // bounded-wait status of the tcgen05 small-M kernel
+w4a4_status q_read_and_clear_status();       // bounded-wait status of the activation kernel
 }  // namespace w4a4

@@ -5,10 +5,14 @@
 //
 // GB300 design:
 //  * A thread-block cluster of CK CTAs (8 warps each) owns 16 rows; each CTA
-//    takes a contiguous range of the K groups, about two per warp.  The fp32 LoRA partials of the CK CTAs
-//    are summed through distributed shared memory in a fixed order: no
-//    atomics, deterministic results, and no separate repack kernel (the
-//    page's pack_lora_act exists only to wait for its atomics).
+//    takes a contiguous range of the K groups, about two per warp.  Every
+//    warp pushes its fp32 LoRA partial tiles (16 rows x 8 columns each) with
+//    st.async into the shared memory of the CTA that owns the tile (tile t
+//    belongs to cluster rank t % CK), completing bytes on that CTA's
+//    mbarrier; the owner adds the 8 x CK partials in a fixed (rank, warp)
+//    order and stores fp16.  No atomics, deterministic results, one split
+//    cluster barrier (overlapping the main loop) and no separate repack
+//    kernel (the page's pack_lora_act exists only to wait for its atomics).
 //  * Codes are stored as FP8 E4M3 bytes, the operand encoding the tcgen05
 //    tensor core reads (GB300 has no INT4 tensor-core kind).
 //  * Division x / scale is done as a multiplication by the reciprocal, which
@@ -29,19 +33,28 @@
 
 #include "kernels.h"
 #include "norm.cuh"
+#include "tc_ptx.cuh"
 
 namespace cg = cooperative_groups;
 
 namespace w4a4 {
 namespace {
+using namespace tc;
 
 constexpr int kRows = 16;      // rows per cluster (one m16 tile of the LoRA MMA)
 constexpr int kWarps = 8;
 constexpr int kXsStride = 72;  // halves per staged row (64 + 8 pad: conflict-free ldmatrix)
 constexpr int kMaxCluster = 8;
+constexpr uint64_t kWaitNs = 2000000000ull;
+constexpr uint32_t kTileBytes = kRows * 8 * 4;  // one fp32 16 x 8 LoRA partial tile
+// staged fp16 tiles, then the LoRA receive area [rank][warp][CK-strided tile][16 x 8] fp32
+// (CK * ceil(NT / CK) <= NT + kMaxCluster - 1 tiles per (rank, warp))
 __host__ __device__ constexpr int q_smem_bytes(int R) {
-    return kWarps * kRows * kXsStride * 2 + (R > 0 ? kWarps * kRows * R * 4 : 0);
+    return kWarps * kRows * kXsStride * 2 + (R > 0 ? (R / 8 + kMaxCluster - 1) * kWarps * int(kTileBytes) : 0);
 }
+
+// Status word of the kernel's bounded wait (W4A4_ERR_TIMEOUT once it gave up).
+__device__ int g_q_status = 0;
 
 __device__ __forceinline__ void ldmatrix_x4(uint32_t (&r)[4], const void* p) {
     asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
@@ -62,10 +75,10 @@ __global__ void __launch_bounds__(kWarps * 32) quantize_act_kernel(const uint16_
                                                                    int K, uint8_t* __restrict__ ws) {
     extern __shared__ __align__(16) uint8_t qsm[];
     __shared__ double ssq[kWarps][kRows], row_part[kRows], row_inv[kRows];
-    pdl_wait();
-    pdl_launch_dependents();
+    __shared__ __align__(8) uint64_t lora_bar_word;
+    __shared__ int q_abort;
     uint16_t(*xs)[kRows * kXsStride] = reinterpret_cast<uint16_t(*)[kRows * kXsStride]>(qsm);
-    float* red = reinterpret_cast<float*>(qsm + kWarps * kRows * kXsStride * 2);
+    float* recv = reinterpret_cast<float*>(qsm + kWarps * kRows * kXsStride * 2);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int G = K / kGroup;
@@ -76,6 +89,21 @@ __global__ void __launch_bounds__(kWarps * 32) quantize_act_kernel(const uint16_
     const int row0 = (blockIdx.x / CK) * kRows;
     const int mt = row0 / kTileM;
     const int g_begin = (G * crank) / CK, g_end = (G * (crank + 1)) / CK;
+    constexpr int NT = R / 8;
+    // LoRA tiles t with t % CK == crank are this CTA's to finish; receive layout stride
+    const int own_tiles = crank < NT ? (NT - crank + CK - 1) / CK : 0;
+    const int slot_tiles = (NT + CK - 1) / CK;
+    const uint32_t lora_bar = smem_u32(&lora_bar_word);
+    if (R > 0 && threadIdx.x == 0) {
+        q_abort = 0;
+        mbar_init(lora_bar, 1);
+        fence_mbar_init();
+        // this thread's arrival, and the bytes the other ranks' warps will push
+        mbar_expect_tx(lora_bar, uint32_t((CK - 1) * kWarps * own_tiles) * kTileBytes);
+    }
+    // (the barrier set-up above touches only this CTA's shared memory)
+    pdl_wait();
+    pdl_launch_dependents();
     if (blockIdx.x == 0) {  // the GEMM's stream-K ready flags start every call cleared
         uint32_t* fl = reinterpret_cast<uint32_t*>(ws + AL.flags);
         for (int i = threadIdx.x; i < kStreamKSlots * kStreamKWarps; i += kWarps * 32) fl[i] = 0u;
@@ -87,7 +115,6 @@ __global__ void __launch_bounds__(kWarps * 32) quantize_act_kernel(const uint16_
     const int rr = m % kTileM;
     const bool valid = m < M;
 
-    constexpr int NT = R / 8;
     float acc[NT > 0 ? NT : 1][4];
 #pragma unroll
     for (int t = 0; t < (NT > 0 ? NT : 1); ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.f;
@@ -130,6 +157,10 @@ __global__ void __launch_bounds__(kWarps * 32) quantize_act_kernel(const uint16_
         inv = row_inv[qrow];
         split_inv(inv, inva, invb);
     }
+    // split cluster barrier: arriving says "my receive barrier is set up" (and, with the
+    // norm, "I have read my peers' row sums"); the wait before the first push follows the
+    // main loop, so its latency is hidden
+    if (R > 0 && CK > 1) cluster_arrive_release();
     int g = g_begin + warp;
     uint4 xv[4];
 #pragma unroll
@@ -248,36 +279,50 @@ __global__ void __launch_bounds__(kWarps * 32) quantize_act_kernel(const uint16_
     }
 
     if constexpr (R > 0) {
-        // warps' partials -> smem, summed in a fixed order inside the CTA, then across the cluster
+        // push this warp's partial tiles to their owners: lane (gid, tig) holds rows gid and
+        // gid + 8, columns 2 tig and 2 tig + 1 of every 16 x 8 tile
         const int gid = lane >> 2, tig = lane & 3;
-        float* rw = red + warp * kRows * R;
+        if (CK > 1) cluster_wait_acquire();
 #pragma unroll
         for (int t = 0; t < NT; ++t) {
-            rw[gid * R + 8 * t + 2 * tig] = acc[t][0];
-            rw[gid * R + 8 * t + 2 * tig + 1] = acc[t][1];
-            rw[(gid + 8) * R + 8 * t + 2 * tig] = acc[t][2];
-            rw[(gid + 8) * R + 8 * t + 2 * tig + 1] = acc[t][3];
+            const int o = t % CK, lt = t / CK;
+            const uint32_t off =
+                ((uint32_t(crank * kWarps + warp) * slot_tiles + lt) * (kRows * 8) + gid * 8 + 2 * tig) * 4;
+            if (o == crank) {
+                *reinterpret_cast<float2*>(reinterpret_cast<uint8_t*>(recv) + off) = make_float2(acc[t][0], acc[t][1]);
+                *reinterpret_cast<float2*>(reinterpret_cast<uint8_t*>(recv) + off + 8 * 8 * 4) =
+                    make_float2(acc[t][2], acc[t][3]);
+            } else {
+                const uint32_t dst = mapa_shared(smem_u32(recv) + off, uint32_t(o));
+                const uint32_t rbar = mapa_shared(lora_bar, uint32_t(o));
+                st_async_v2(dst, acc[t][0], acc[t][1], rbar);
+                st_async_v2(dst + 8 * 8 * 4, acc[t][2], acc[t][3], rbar);
+            }
         }
-        __syncthreads();
-        for (int idx = threadIdx.x; idx < kRows * R; idx += kWarps * 32) {
-            float v = red[idx];
+        __syncthreads();  // this CTA's own partials are in place
+        if (own_tiles > 0) {
+            if (!wait_parity_suspend(lora_bar, 0u, &q_abort, kWaitNs, 20000u)) {
+                q_abort = 1;
+                atomicExch(&g_q_status, int(W4A4_ERR_TIMEOUT));
+            }
+            if (!q_abort) {
+                // finish the owned tiles: the 8 x CK partials in (rank, warp) order, fp16 out
+                uint16_t* La = reinterpret_cast<uint16_t*>(ws + AL.La);
+                for (int e = threadIdx.x; e < own_tiles * kRows * 8; e += kWarps * 32) {
+                    const int lt = e / (kRows * 8), rc = e % (kRows * 8), row = rc / 8, col = rc % 8;
+                    float v = 0.f;
+                    for (int c = 0; c < CK; ++c)
 #pragma unroll
-            for (int w = 1; w < kWarps; ++w) v += red[w * kRows * R + idx];
-            red[idx] = v;  // CTA partial in warp 0's slot
+                        for (int w = 0; w < kWarps; ++w)
+                            v += recv[((c * kWarps + w) * slot_tiles + lt) * (kRows * 8) + rc];
+                    const int j = 8 * (lt * CK + crank) + col;
+                    const int r2 = (row0 + row) % kTileM;
+                    const int p = j >> 4, jj = j & 15;
+                    La[((size_t)(mt * (R / 16) + p) * kTileM + r2) * 16 + swz32(r2, jj >> 3) * 8 + (jj & 7)] =
+                        __half_as_ushort(__float2half_rn(v));
+                }
+            }
         }
-        cluster.sync();
-        // cluster rank c finalises elements c, c + CK, ... of the 16 x R block
-        uint16_t* La = reinterpret_cast<uint16_t*>(ws + AL.La);
-        for (int idx = crank + CK * int(threadIdx.x); idx < kRows * R; idx += CK * kWarps * 32) {
-            float v = 0.f;
-            for (int c = 0; c < CK; ++c) v += cluster.map_shared_rank(red, c)[idx];
-            const int row = idx / R, j = idx % R;
-            const int r2 = (row0 + row) % kTileM;
-            const int p = j >> 4, jj = j & 15;
-            La[((size_t)(mt * (R / 16) + p) * kTileM + r2) * 16 + swz32(r2, jj >> 3) * 8 + (jj & 7)] =
-                __half_as_ushort(__float2half_rn(v));
-        }
-        cluster.sync();  // peers' shared memory stays alive until every read is done
     }
     if constexpr (NORM && R == 0) cluster.sync();  // (the peers' reads of row_part are done)
 }
@@ -371,6 +416,20 @@ w4a4_status launch_qr(const uint16_t* X, int ld_x, const uint8_t* packed, int M,
 }
 
 }  // namespace
+
+w4a4_status q_read_and_clear_status() {
+    int v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_q_status, sizeof(int)) != cudaSuccess) {
+        cudaGetLastError();
+        return W4A4_ERR_CUDA;
+    }
+    if (v != 0) {
+        const int zero = 0;
+        cudaMemcpyToSymbol(g_q_status, &zero, sizeof(int));
+        return W4A4_ERR_TIMEOUT;
+    }
+    return W4A4_OK;
+}
 
 w4a4_status launch_quantize_act(const uint16_t* X, const uint8_t* packed, int M, int K, int r, uint8_t* ws,
                                 cudaStream_t s) {

@@ -119,6 +119,12 @@ __device__ __forceinline__ void st_cluster_v4(uint32_t addr, float4 v) {
 // 16 bytes of transaction count on an mbarrier of that CTA (both addresses
 // from mapa_shared); no fence is needed for the receiver to see the data once
 // it observes the barrier phase.
+__device__ __forceinline__ void st_async_v2(uint32_t remote_addr, float a, float b, uint32_t remote_bar) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.f32 [%0], {%1, %2}, [%3];\n" ::"r"(
+                     remote_addr),
+                 "f"(a), "f"(b), "r"(remote_bar)
+                 : "memory");
+}
 __device__ __forceinline__ void st_async_v4(uint32_t remote_addr, float4 v, uint32_t remote_bar) {
     asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];\n" ::"r"(
                      remote_addr),
