@@ -24,11 +24,12 @@
 //  * Fused variant (NORM): the input is the previous linear's output, and the
 //    RMSNorm between the two linears ("W4A4 CUDA Kernel for Voice Clone", 3.9)
 //    is applied on the way in: every CTA first sums the squares of its 16 rows
-//    over all K columns (the rows are L2-resident after the producing GEMM;
-//    every CTA of a cluster sums in the same order, so all agree on the
-//    inverse RMS without exchanging it), then each group's values are
-//    normalised to fp16 -- the same bits as the glue kernel writes -- before
-//    they are quantised and fed to the LoRA down-projection.
+//    over its own groups (the rows are L2-resident after the producing GEMM),
+//    pushes the partial row sums to every rank of its cluster (st.async onto
+//    the peers' mbarriers), and each CTA adds the CK partials in rank order, so
+//    all agree on the inverse RMS; then each group's values are normalised to
+//    fp16 -- the same bits as the glue kernel writes -- before they are
+//    quantised and fed to the LoRA down-projection.
 #include <cooperative_groups.h>
 
 #include "kernels.h"
@@ -74,8 +75,9 @@ __global__ void __launch_bounds__(kWarps * 32) quantize_act_kernel(const uint16_
                                                                    const uint2* __restrict__ Ldp, int M,
                                                                    int K, uint8_t* __restrict__ ws) {
     extern __shared__ __align__(16) uint8_t qsm[];
-    __shared__ double ssq[kWarps][kRows], row_part[kRows], row_inv[kRows];
-    __shared__ __align__(8) uint64_t lora_bar_word;
+    __shared__ double ssq[kWarps][kRows], row_inv[kRows];
+    __shared__ double row_recv[kMaxCluster][kRows];  // (NORM) every rank's partial row sums
+    __shared__ __align__(8) uint64_t lora_bar_word, norm_bar_word;
     __shared__ int q_abort;
     uint16_t(*xs)[kRows * kXsStride] = reinterpret_cast<uint16_t(*)[kRows * kXsStride]>(qsm);
     float* recv = reinterpret_cast<float*>(qsm + kWarps * kRows * kXsStride * 2);
@@ -93,15 +95,25 @@ __global__ void __launch_bounds__(kWarps * 32) quantize_act_kernel(const uint16_
     // LoRA tiles t with t % CK == crank are this CTA's to finish; receive layout stride
     const int own_tiles = crank < NT ? (NT - crank + CK - 1) / CK : 0;
     const int slot_tiles = (NT + CK - 1) / CK;
-    const uint32_t lora_bar = smem_u32(&lora_bar_word);
-    if (R > 0 && threadIdx.x == 0) {
+    const uint32_t lora_bar = smem_u32(&lora_bar_word), norm_bar = smem_u32(&norm_bar_word);
+    if (threadIdx.x == 0) {
         q_abort = 0;
-        mbar_init(lora_bar, 1);
+        if (R > 0) {
+            mbar_init(lora_bar, 1);
+            // this thread's arrival, and the bytes the other ranks' warps will push
+            mbar_expect_tx(lora_bar, uint32_t((CK - 1) * kWarps * own_tiles) * kTileBytes);
+        }
+        if (NORM) {
+            mbar_init(norm_bar, 1);
+            mbar_expect_tx(norm_bar, uint32_t((CK - 1) * kRows) * 8u);  // the other ranks' row sums
+        }
         fence_mbar_init();
-        // this thread's arrival, and the bytes the other ranks' warps will push
-        mbar_expect_tx(lora_bar, uint32_t((CK - 1) * kWarps * own_tiles) * kTileBytes);
     }
-    // (the barrier set-up above touches only this CTA's shared memory)
+    // split cluster barrier: arriving says "my receive barriers are set up"; the wait
+    // comes before this CTA's first push into a peer, so its latency overlaps the loads.
+    // (The set-up touches only this CTA's shared memory, so it also overlaps the
+    // previous kernel.)
+    if (CK > 1 && (R > 0 || NORM)) cluster_arrive_release();
     pdl_wait();
     pdl_launch_dependents();
     if (blockIdx.x == 0) {  // the GEMM's stream-K ready flags start every call cleared
@@ -141,26 +153,31 @@ __global__ void __launch_bounds__(kWarps * 32) quantize_act_kernel(const uint16_
         ss += __shfl_xor_sync(0xffffffffu, ss, 1);
         if (qhalf == 0) ssq[warp][qrow] = ss;
         __syncthreads();
+        if (CK > 1) cluster_wait_acquire();  // (every rank's receive barriers are set up)
         if (threadIdx.x < kRows) {
             double t = 0.0;
 #pragma unroll
             for (int w = 0; w < kWarps; ++w) t += ssq[w][threadIdx.x];
-            row_part[threadIdx.x] = t;
+            // this CTA's partial row sum into slot [crank] of every rank of the cluster
+            row_recv[crank][threadIdx.x] = t;
+            for (int c = 0; c < CK; ++c)
+                if (c != crank)
+                    st_async_b64(mapa_shared(smem_u32(&row_recv[crank][threadIdx.x]), uint32_t(c)),
+                                 __double_as_longlong(t), mapa_shared(norm_bar, uint32_t(c)));
         }
-        cluster.sync();
         if (threadIdx.x < kRows) {
+            if (CK > 1 && !wait_parity_suspend(norm_bar, 0u, &q_abort, kWaitNs, 20000u)) {
+                q_abort = 1;
+                atomicExch(&g_q_status, int(W4A4_ERR_TIMEOUT));
+            }
             double t = 0.0;
-            for (int c = 0; c < CK; ++c) t += cluster.map_shared_rank(row_part, c)[threadIdx.x];
-            row_inv[threadIdx.x] = 1.0 / sqrt(t / double(K) + W4A4_RMSNORM_EPS);
+            for (int c = 0; c < CK; ++c) t += row_recv[c][threadIdx.x];  // rank order, the same in every CTA
+            row_inv[threadIdx.x] = __drcp_rn(__dsqrt_rn(t / double(K) + W4A4_RMSNORM_EPS));  // = 1.0 / sqrt(.)
         }
         __syncthreads();
         inv = row_inv[qrow];
         split_inv(inv, inva, invb);
     }
-    // split cluster barrier: arriving says "my receive barrier is set up" (and, with the
-    // norm, "I have read my peers' row sums"); the wait before the first push follows the
-    // main loop, so its latency is hidden
-    if (R > 0 && CK > 1) cluster_arrive_release();
     int g = g_begin + warp;
     uint4 xv[4];
 #pragma unroll
@@ -282,7 +299,7 @@ __global__ void __launch_bounds__(kWarps * 32) quantize_act_kernel(const uint16_
         // push this warp's partial tiles to their owners: lane (gid, tig) holds rows gid and
         // gid + 8, columns 2 tig and 2 tig + 1 of every 16 x 8 tile
         const int gid = lane >> 2, tig = lane & 3;
-        if (CK > 1) cluster_wait_acquire();
+        if (CK > 1 && !NORM) cluster_wait_acquire();  // (with the norm, waited for before the row sums)
 #pragma unroll
         for (int t = 0; t < NT; ++t) {
             const int o = t % CK, lt = t / CK;
@@ -324,7 +341,6 @@ __global__ void __launch_bounds__(kWarps * 32) quantize_act_kernel(const uint16_
             }
         }
     }
-    if constexpr (NORM && R == 0) cluster.sync();  // (the peers' reads of row_part are done)
 }
 
 __global__ void unpack_act_kernel(const uint8_t* __restrict__ ws, int M, int K, int r, int8_t* codes,

@@ -119,6 +119,11 @@ __device__ __forceinline__ void st_cluster_v4(uint32_t addr, float4 v) {
 // 16 bytes of transaction count on an mbarrier of that CTA (both addresses
 // from mapa_shared); no fence is needed for the receiver to see the data once
 // it observes the barrier phase.
+__device__ __forceinline__ void st_async_b64(uint32_t remote_addr, long long v, uint32_t remote_bar) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b64 [%0], %1, [%2];\n" ::"r"(remote_addr),
+                 "l"(v), "r"(remote_bar)
+                 : "memory");
+}
 __device__ __forceinline__ void st_async_v2(uint32_t remote_addr, float a, float b, uint32_t remote_bar) {
     asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.f32 [%0], {%1, %2}, [%3];\n" ::"r"(
                      remote_addr),
