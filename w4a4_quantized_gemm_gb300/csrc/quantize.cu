@@ -376,11 +376,13 @@ w4a4_status launch_q(const uint16_t* X, int ld_x, const uint8_t* packed, int M, 
     // split K over a (small) cluster: one group per warp where that takes at most
     // two CTAs, else about two groups per warp (larger clusters cost more in
     // their reduction than they gain)
+    // (with few row blocks -- decode -- the SMs are idle anyway: one group per warp
+    // up to the largest cluster)
+    const int row_blocks = (M + kRows - 1) / kRows;
     int CK = (G + kWarps - 1) / kWarps;
-    if (CK > 2) CK = (G + 2 * kWarps - 1) / (2 * kWarps);
+    if (CK > 2 && row_blocks > 8) CK = (G + 2 * kWarps - 1) / (2 * kWarps);
     if (CK > kMaxCluster) CK = kMaxCluster;
     if (CK < 1) CK = 1;
-    const int row_blocks = (M + kRows - 1) / kRows;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(unsigned(row_blocks * CK));
     cfg.blockDim = dim3(kWarps * 32);
