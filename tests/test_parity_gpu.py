@@ -306,3 +306,32 @@ def _stream_k_case(M, N, K, r):
     assert "stream-K" not in w4.w4a4_last_dispatch(), w4.w4a4_last_dispatch()
     check_tol(Y3.cpu()[rows], y, f"round-robin {M}x{N}x{K} r={r}")
     assert w4.w4a4_device_status() == 0
+
+
+def test_stream_k_wait_runs_out_and_reports_timeout():
+    """A bounded wait that can never be satisfied: the stream-K finisher waits for
+    its hand-over counters to reach 32, and the test sets them to a value that the
+    producers' increments cannot bring there.  The launch must end by itself with
+    W4A4_ERR_TIMEOUT in the status word, and the context must stay usable: the
+    same linear, re-quantised, then matches the oracle."""
+    M, N, K, r = 129, 256, 4096, 32
+    was = w4.w4a4_stream_k()
+    w4.w4a4_set_stream_k(True)
+    try:
+        c = make_linear_case(M, K, N, r, seed=77)
+        t = to_dev(c)
+        packed = pack(c, t)
+        ws = quantize(c, t, packed)
+        flags_end = w4.act_workspace_min_bytes(M, K, r)
+        ws[flags_end - 160 * 16 * 4: flags_end] = 0xFF  # counters at 2^32 - 1: +32 never gives 32
+        run_linear(c, t, packed, ws, w4.KERNEL_TC)
+        assert "stream-K" in w4.w4a4_last_dispatch(), w4.w4a4_last_dispatch()
+        assert w4.w4a4_device_status() == w4.W4A4_ERR_TIMEOUT
+        assert w4.w4a4_device_status() == 0  # read and cleared
+        ws = quantize(c, t, packed)  # the activation kernel clears the counters
+        Y = run_linear(c, t, packed, ws, w4.KERNEL_TC)
+        assert w4.w4a4_device_status() == 0
+        y = oracle.linear(c.X, c.W, c.L_down, c.L_up, c.colscale, c.bias)
+        check_tol(Y, y, "after a timed-out launch")
+    finally:
+        w4.w4a4_set_stream_k(was)

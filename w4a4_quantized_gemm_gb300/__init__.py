@@ -19,6 +19,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libw4a4.so")
 
 W4A4_OK = 0
+W4A4_ERR_TIMEOUT = 6
 KERNEL_AUTO, KERNEL_TC, KERNEL_SMALLM, KERNEL_SMALLM_TC = 0, 1, 2, 3
 GROUP = 64
 
