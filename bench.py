@@ -42,6 +42,23 @@ STACK_WORKLOAD = "qwen3_1024_28_layer_stack_M700"
 L2_BYTES = 129 * 2 ** 20
 
 
+def max_over_ranks(x: float, dev, world: int) -> float:
+    """The largest of every rank's x: a job's time is its slowest rank's."""
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(world: int, units_per_rank_step: float, ms_per_step: float) -> float:
+    """Whole-job throughput (units per second): every rank runs its own replica of
+    the step (weak scaling), and the step takes the slowest rank's time."""
+    return world * units_per_rank_step / (ms_per_step * 1e-3)
+
+
 def _env_int(k, d):
     try:
         return int(os.environ.get(k, d))
@@ -302,13 +319,11 @@ def run_ours(args, rank, world, local_rank):
     ms = timed(step_graphs, args.steps)
     if sampler:
         sampler.__exit__()
+    ms = max_over_ranks(ms, dev, world)
     if world > 1:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
         dist.barrier()
     ms_per_step = ms / args.steps
-    value = world * layer_ops() / (ms_per_step * 1e-3) / 1e12
+    value = job_rate(world, layer_ops(), ms_per_step) / 1e12
 
     # per-kernel durations.  Per step: one graph per replica holding the step's
     # four GEMMs (or four activation kernels), the same buffers as the step.
@@ -420,12 +435,8 @@ def run_ours(args, rank, world, local_rank):
             st.wait_stream(s_in)
             st.wait_stream(s_out)
 
-        e_ms = timed(capture(e2e_fn), args.steps) / args.steps
-        if world > 1:
-            t = torch.tensor([e_ms], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e_ms = float(t.item())
-        e2e = {"value": world * layer_ops() / (e_ms * 1e-3) / 1e12, "unit": UNIT, "h2d_bytes_per_step": h2d,
+        e_ms = max_over_ranks(timed(capture(e2e_fn), args.steps) / args.steps, dev, world)
+        e2e = {"value": job_rate(world, layer_ops(), e_ms) / 1e12, "unit": UNIT, "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "ms_per_step": e_ms,
                "how": "CUDA graph per step: H2D of the 4 inputs X from pinned host on a copy stream, the two "
                       "C-ABI calls per linear once its X has landed, D2H of each Y on a second copy stream "
@@ -586,13 +597,10 @@ def run_stack(args, rank, world, local_rank):
     ms = timed(fwd, args.steps)
     if sampler:
         sampler.__exit__()
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, dev, world)
     ms_per_step = ms / args.steps
     ops = stack_ops()
-    value = world * ops / (ms_per_step * 1e-3) / 1e12
+    value = job_rate(world, ops, ms_per_step) / 1e12
     gemm_s = timed(g_gemm, args.steps) / args.steps * 1e-3
     peaks = {}
     try:
@@ -626,8 +634,8 @@ def run_stack(args, rank, world, local_rank):
             stack.forward(torch.cuda.current_stream())
             Oh.copy_(stack.out, non_blocking=True)
         torch.cuda.synchronize()
-        e_ms = timed(g_e2e, args.steps) / args.steps
-        e2e = {"value": world * ops / (e_ms * 1e-3) / 1e12, "unit": UNIT, "ms_per_step": e_ms,
+        e_ms = max_over_ranks(timed(g_e2e, args.steps) / args.steps, dev, world)
+        e2e = {"value": job_rate(world, ops, e_ms) / 1e12, "unit": UNIT, "ms_per_step": e_ms,
                "h2d_bytes_per_step": Xh.numel() * 2, "d2h_bytes_per_step": Oh.numel() * 2,
                "how": "one CUDA graph: H2D of the stack input from pinned host, the 336 C-ABI launches, D2H of the output"}
 
