@@ -98,8 +98,8 @@ typedef enum {
 
 /* Kernel selection for w4a4_linear_select / w4a4_debug_group_partials. */
 typedef enum {
-    W4A4_KERNEL_AUTO = 0,   /* by M: M <= 8 the warp-MMA small-M kernel, M <= threshold the tcgen05
-                               small-M kernel, else tensor-core tiles */
+    W4A4_KERNEL_AUTO = 0,   /* by M: M <= threshold the tcgen05 small-M kernel, else tensor-core
+                               tiles (the partials dump takes the warp-MMA kernel at small M) */
     W4A4_KERNEL_TC = 1,     /* tcgen05 (TMEM accumulators, bulk-copy pipeline) */
     W4A4_KERNEL_SMALLM = 2, /* weight-streaming kernel (warp-level MMA, split over K) */
     W4A4_KERNEL_SMALLM_TC = 3 /* weight-streaming kernel on tcgen05 (weights as the 128-row operand, tokens

@@ -15,7 +15,6 @@ namespace w4a4 {
 namespace {
 thread_local char t_dispatch[256] = "none";
 int g_small_m_threshold = -1;  // -1: read W4A4_SMALL_M on first use
-constexpr int kWarpMmaMaxM = 8;     // M <= this -> the warp-MMA weight-streaming kernel
 constexpr int kStreamKDefault = 0;  // stream-K measured slower than split-K / round-robin on every layer shape
 constexpr int kDefaultSmallM = 32;  // M <= this -> weight-streaming kernel, else tcgen05 tiles (measured crossover: 32..48)
 std::mutex g_mu;
@@ -288,13 +287,15 @@ w4a4_status w4a4_quantize_act_rmsnorm(const uint16_t* Y, int ld_y, const void* p
                                        static_cast<uint8_t*>(act_ws), stream);
 }
 
-// AUTO: up to 8 rows the warp-MMA weight-streaming kernel, up to the small-M
-// threshold the tcgen05 weight-streaming kernel, above it the tcgen05 tiles
-// (measured crossovers on the decoder-layer and K = N = 4096 shapes).
-static int pick_kernel(int M, int kernel) {
+// AUTO: up to the small-M threshold the tcgen05 weight-streaming kernel (it
+// beats the warp-MMA one from M = 1 on), above it the tcgen05 tiles (measured
+// crossovers on the decoder-layer and K = N = 4096 shapes).  The partials dump,
+// which the tcgen05 weight-streaming kernel does not have, takes the warp-MMA
+// kernel at small M.
+static int pick_kernel(int M, int kernel, bool dump = false) {
     if (kernel == W4A4_KERNEL_TC || kernel == W4A4_KERNEL_SMALLM || kernel == W4A4_KERNEL_SMALLM_TC) return kernel;
     if (M > w4a4_small_m_threshold()) return W4A4_KERNEL_TC;
-    return M <= kWarpMmaMaxM ? W4A4_KERNEL_SMALLM : W4A4_KERNEL_SMALLM_TC;
+    return dump ? W4A4_KERNEL_SMALLM : W4A4_KERNEL_SMALLM_TC;
 }
 
 static w4a4_status linear_checks(const void* act_ws, size_t act_ws_bytes, const void* packed, size_t packed_bytes,
@@ -447,7 +448,7 @@ w4a4_status w4a4_debug_group_partials(const void* act_ws, const void* packed, in
     if ((st = check_device()) != W4A4_OK) return st;
     const uint8_t* ws = static_cast<const uint8_t*>(act_ws);
     const uint8_t* pk = static_cast<const uint8_t*>(packed);
-    if (pick_kernel(M, kernel) == W4A4_KERNEL_TC)
+    if (pick_kernel(M, kernel, true) == W4A4_KERNEL_TC)
         st = launch_gemm_tc(ws, pk, nullptr, nullptr, M, N, K, r, nullptr, P, false, 0, stream);
     else
         st = launch_gemm_smallm(ws, pk, nullptr, nullptr, M, N, K, r, nullptr, P, stream);

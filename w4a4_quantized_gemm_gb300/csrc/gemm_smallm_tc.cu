@@ -12,15 +12,17 @@
 // per two tokens).
 //
 // CTA: 128 weight rows x one token block x a K slice; K is split over a
-// cluster of KS CTAs as in the warp-MMA small-M kernel.  Roles (6 warps):
+// cluster of KS CTAs as in the warp-MMA small-M kernel.  Roles (10 warps):
 //   warps 0-3  expand the weight nibbles of their 32 rows into the E4M3 A
-//              operand (32-byte swizzled K-major planes) and, one group
-//              behind, run the epilogue on the same tensor-memory lane quarter;
+//              operand (32-byte swizzled K-major planes);
 //   warp 4     producer: 1-D bulk copies of each group's weight records,
 //              weight scales, the token block's codes and (sA, SA), in an
 //              S-deep ring; on rank 0 the LoRA planes;
 //   warp 5     tensor-memory owner and MMA issuer (one thread): on rank 0 a
-//              kind::f16 LoRA-up chain, then per group two kind::f8f6f4 MMAs.
+//              kind::f16 LoRA-up chain, then per group two kind::f8f6f4 MMAs;
+//   warps 6-9  epilogue, one tensor-memory lane quarter each (warp w: rows
+//              32 (w % 4) ...), running one group behind the expansion, so the
+//              two overlap; then the exchange, the affine and the store.
 // The partial sums are exchanged in blocks of 4 tokens: block b belongs to
 // cluster rank b % KS, the other ranks push their fp32 sums there with
 // st.async, and the owner adds them in rank order before the affine and the
@@ -36,8 +38,8 @@ namespace {
 using namespace tc;
 
 constexpr int kRows = 128;  // weight rows per CTA (MMA M, tensor-memory lanes)
-constexpr int kThreads = 192;
-constexpr int WARP_PROD = 4, WARP_MMA = 5;
+constexpr int kThreads = 320;
+constexpr int WARP_PROD = 4, WARP_MMA = 5, WARP_EPI0 = 6;
 constexpr int kMaxKS = 8;
 constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr uint32_t kSuspendNs = 20000;
@@ -76,7 +78,7 @@ __host__ __device__ inline TcPlan tc_plan(int tokn, int r, int ks) {
 }
 
 template <int TOKN>
-__global__ void __launch_bounds__(kThreads, 1) gemm_smallm_tc_kernel(
+__global__ void __launch_bounds__(kThreads, TOKN >= 64 ? 1 : 2) gemm_smallm_tc_kernel(
     const uint8_t* __restrict__ ws, const uint8_t* __restrict__ packed, const uint16_t* __restrict__ colscale,
     const uint16_t* __restrict__ bias, int M, int N, int K, int r, uint16_t* __restrict__ Y, int KS, int silu_I) {
     constexpr int BLK = TOKN / 4;  // 4-token blocks
@@ -228,13 +230,67 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_smallm_tc_kernel(
         __syncwarp();
     }
 
-    // ---- warps 0-3: expansion of group i, epilogue of group i - 1
-    const int row = warp * 32 + lane;  // weight row = tensor-memory lane
-    uint64_t acc[TOKN / 2];            // running sums, token pairs
+    // ---- warps 0-3: expansion; warps 6-9: epilogue, one group behind
+    const bool is_epi = warp >= WARP_EPI0;
+    const int row = is_epi ? (warp & 3) * 32 + lane : warp * 32 + lane;  // weight row = tensor-memory lane
+    uint64_t acc[TOKN / 2];                                                // running sums, token pairs
 #pragma unroll
     for (int c = 0; c < TOKN / 2; ++c) acc[c] = 0ull;
     if (warp < 4) {
-        const uint32_t tl = tmem + (uint32_t(warp * 32) << 16);
+        for (int i = 0; i < n_groups && ok; ++i) {
+            const int s = i % kS;
+            const uint32_t ph = uint32_t(i / kS) & 1u;
+            if (!warp_wait_parity_suspend(full(s), ph, abort, kWaitNs, kSuspendNs)) {
+                ok = false;
+                break;
+            }
+            // nibbles -> E4M3: row `row`, k-plane p, 16-byte chunk c at row * 32 + swz32(row, c) * 16
+            const uint8_t* wr = smraw + PLN.wraw + s * (kRows * 32) + row * 32;
+            const uint4 w01 = *reinterpret_cast<const uint4*>(wr);
+            const uint4 w23 = *reinterpret_cast<const uint4*>(wr + 16);
+            const uint4 p0c0 = make_uint4(expand4(w01.x), expand4(w01.z), expand4(w23.x), expand4(w23.z));
+            const uint4 p0c1 =
+                make_uint4(expand4(w01.x >> 16), expand4(w01.z >> 16), expand4(w23.x >> 16), expand4(w23.z >> 16));
+            const uint4 p1c0 = make_uint4(expand4(w01.y), expand4(w01.w), expand4(w23.y), expand4(w23.w));
+            const uint4 p1c1 =
+                make_uint4(expand4(w01.y >> 16), expand4(w01.w >> 16), expand4(w23.y >> 16), expand4(w23.w >> 16));
+            uint8_t* ep = smraw + PLN.wexp + s * (2 * kRows * 32);
+            *reinterpret_cast<uint4*>(ep + row * 32 + swz32(row, 0) * 16) = p0c0;
+            *reinterpret_cast<uint4*>(ep + row * 32 + swz32(row, 1) * 16) = p0c1;
+            *reinterpret_cast<uint4*>(ep + kRows * 32 + row * 32 + swz32(row, 0) * 16) = p1c0;
+            *reinterpret_cast<uint4*>(ep + kRows * 32 + row * 32 + swz32(row, 1) * 16) = p1c1;
+            if (warp == 0) {
+                // (sA, SA) pairs -> sA[] and cc[] = -8 SA sA, in place (the pairs' 8 bytes per token)
+                float* sp = reinterpret_cast<float*>(smraw + PLN.sa + s * (TOKN * 8));
+                float v0[TOKN / 32 + 1], v1[TOKN / 32 + 1];
+#pragma unroll
+                for (int u = 0; u * 32 < TOKN; ++u) {
+                    const int m = u * 32 + lane;
+                    if (m < TOKN) {
+                        v0[u] = sp[2 * m];
+                        v1[u] = sp[2 * m + 1];
+                    }
+                }
+                __syncwarp();
+#pragma unroll
+                for (int u = 0; u * 32 < TOKN; ++u) {
+                    const int m = u * 32 + lane;
+                    if (m < TOKN) {
+                        sp[m] = v0[u];
+                        sp[TOKN + m] = (-8.f * v1[u]) * v0[u];
+                    }
+                }
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(expd(s));
+        }
+        if (!ok && lane == 0) {
+            atomicExch(&g_smtc_status, int(W4A4_ERR_TIMEOUT));
+            *abort = 1;
+        }
+    } else if (is_epi) {
+        const uint32_t tl = tmem + (uint32_t((warp & 3) * 32) << 16);
         if (RP > 0) {
             const bool w_ok = warp_wait_parity_suspend(tlora, 0u, abort, kWaitNs, kSuspendNs);
             if (w_ok) {
@@ -253,90 +309,39 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_smallm_tc_kernel(
                 ok = false;
             }
         }
-        const uint64_t m8 = f2_pack(-8.f, -8.f);
-        for (int i = 0; i <= n_groups && ok; ++i) {
-            if (i < n_groups) {
-                const int s = i % kS;
-                const uint32_t ph = uint32_t(i / kS) & 1u;
-                if (!warp_wait_parity_suspend(full(s), ph, abort, kWaitNs, kSuspendNs)) {
-                    ok = false;
-                    break;
-                }
-                // nibbles -> E4M3: row `row`, k-plane p, 16-byte chunk c at row * 32 + swz32(row, c) * 16
-                const uint8_t* wr = smraw + PLN.wraw + s * (kRows * 32) + row * 32;
-                const uint4 w01 = *reinterpret_cast<const uint4*>(wr);
-                const uint4 w23 = *reinterpret_cast<const uint4*>(wr + 16);
-                const uint4 p0c0 = make_uint4(expand4(w01.x), expand4(w01.z), expand4(w23.x), expand4(w23.z));
-                const uint4 p0c1 =
-                    make_uint4(expand4(w01.x >> 16), expand4(w01.z >> 16), expand4(w23.x >> 16), expand4(w23.z >> 16));
-                const uint4 p1c0 = make_uint4(expand4(w01.y), expand4(w01.w), expand4(w23.y), expand4(w23.w));
-                const uint4 p1c1 =
-                    make_uint4(expand4(w01.y >> 16), expand4(w01.w >> 16), expand4(w23.y >> 16), expand4(w23.w >> 16));
-                uint8_t* ep = smraw + PLN.wexp + s * (2 * kRows * 32);
-                *reinterpret_cast<uint4*>(ep + row * 32 + swz32(row, 0) * 16) = p0c0;
-                *reinterpret_cast<uint4*>(ep + row * 32 + swz32(row, 1) * 16) = p0c1;
-                *reinterpret_cast<uint4*>(ep + kRows * 32 + row * 32 + swz32(row, 0) * 16) = p1c0;
-                *reinterpret_cast<uint4*>(ep + kRows * 32 + row * 32 + swz32(row, 1) * 16) = p1c1;
-                if (warp == 0) {
-                    // (sA, SA) pairs -> sA[] and cc[] = -8 SA sA, in place (the pairs' 8 bytes per token)
-                    float* sp = reinterpret_cast<float*>(smraw + PLN.sa + s * (TOKN * 8));
-                    float v0[TOKN / 32 + 1], v1[TOKN / 32 + 1];
-#pragma unroll
-                    for (int u = 0; u * 32 < TOKN; ++u) {
-                        const int m = u * 32 + lane;
-                        if (m < TOKN) {
-                            v0[u] = sp[2 * m];
-                            v1[u] = sp[2 * m + 1];
-                        }
-                    }
-                    __syncwarp();
-#pragma unroll
-                    for (int u = 0; u * 32 < TOKN; ++u) {
-                        const int m = u * 32 + lane;
-                        if (m < TOKN) {
-                            sp[m] = v0[u];
-                            sp[TOKN + m] = (-8.f * v1[u]) * v0[u];
-                        }
-                    }
-                }
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(expd(s));
+        for (int e = 0; e < n_groups && ok; ++e) {
+            const int s = e % kS;
+            const uint32_t ph = uint32_t(e / kS) & 1u;
+            if (!warp_wait_parity_suspend(tfull(s), ph, abort, kWaitNs, kSuspendNs)) {
+                ok = false;
+                break;
             }
-            if (i >= 1) {
-                const int e = i - 1, s = e % kS;
-                const uint32_t ph = uint32_t(e / kS) & 1u;
-                if (!warp_wait_parity_suspend(tfull(s), ph, abort, kWaitNs, kSuspendNs)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                // (the expansion barrier of this stage, already complete: orders warp 0's rewrite of the
-                // stage's (sA, SA) into (sA, cc) before the reads below)
-                if (!warp_wait_parity_suspend(expd(s), ph, abort, kWaitNs, kSuspendNs)) {
-                    ok = false;
-                    break;
-                }
-                float d[TOKN];
-                if constexpr (TOKN == 16) {
-                    tmem_ld16(tl + uint32_t(s * TOKN), d);
-                } else {
-#pragma unroll
-                    for (int c = 0; c < TOKN / 32; ++c) tmem_ld32_at(tl + uint32_t(s * TOKN + 32 * c), d + 32 * c);
-                }
-                tmem_wait_ld();
-                const float sw = __half2float(__ushort_as_half(
-                    reinterpret_cast<const uint16_t*>(smraw + PLN.sw + s * (kRows * 2))[row]));
-                const uint64_t sw2 = f2_pack(sw, sw);
-                const uint64_t* sa2 = reinterpret_cast<const uint64_t*>(smraw + PLN.sa + s * (TOKN * 8));
-                const uint64_t* cc2 = sa2 + TOKN / 2;
-#pragma unroll
-                for (int c = 0; c < TOKN / 2; ++c)
-                    acc[c] = ffma2_b64(sw2, ffma2_b64(sa2[c], f2_pack(d[2 * c], d[2 * c + 1]), cc2[c]), acc[c]);
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(sfree(s));
+            tc_fence_after();
+            // (the expansion barrier of this stage, already complete: orders warp 0's rewrite of the
+            // stage's (sA, SA) into (sA, cc) before the reads below)
+            if (!warp_wait_parity_suspend(expd(s), ph, abort, kWaitNs, kSuspendNs)) {
+                ok = false;
+                break;
             }
+            float d[TOKN];
+            if constexpr (TOKN == 16) {
+                tmem_ld16(tl + uint32_t(s * TOKN), d);
+            } else {
+#pragma unroll
+                for (int c = 0; c < TOKN / 32; ++c) tmem_ld32_at(tl + uint32_t(s * TOKN + 32 * c), d + 32 * c);
+            }
+            tmem_wait_ld();
+            const float sw = __half2float(__ushort_as_half(
+                reinterpret_cast<const uint16_t*>(smraw + PLN.sw + s * (kRows * 2))[row]));
+            const uint64_t sw2 = f2_pack(sw, sw);
+            const uint64_t* sa2 = reinterpret_cast<const uint64_t*>(smraw + PLN.sa + s * (TOKN * 8));
+            const uint64_t* cc2 = sa2 + TOKN / 2;
+#pragma unroll
+            for (int c = 0; c < TOKN / 2; ++c)
+                acc[c] = ffma2_b64(sw2, ffma2_b64(sa2[c], f2_pack(d[2 * c], d[2 * c + 1]), cc2[c]), acc[c]);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(sfree(s));
         }
         if (!ok && lane == 0) {
             atomicExch(&g_smtc_status, int(W4A4_ERR_TIMEOUT));
@@ -362,7 +367,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_smallm_tc_kernel(
     const int own = (BLK + KS - 1) / KS;
     if (KS > 1) {
         cluster_wait_acquire();  // every rank's barriers are initialised
-        if (warp < 4) {
+        if (is_epi) {
 #pragma unroll
             for (int b = 0; b < BLK; ++b) {
                 const int o = b % KS;
@@ -406,11 +411,12 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_smallm_tc_kernel(
     // ---- affine of the owned token blocks, staged as rows [token][128 + 8] over the weight planes
     uint16_t* ys = reinterpret_cast<uint16_t*>(smraw + PLN.wexp);
     constexpr int LDY = kRows + 8;
-    if (warp < 4 && !*abort && silu_I > 0) {
-        // fused gate|up weights (gate_up_row order): lanes 0..15 of warp w hold the gates
-        // of outputs j = 64 t + 16 w + lane, lanes 16..31 the matching ups; h = silu(g) u
-        // is staged as [token][64 + 8] at column 16 w + lane
-        const int j = (nbase >> 1) + 16 * warp + (lane & 15);
+    if (is_epi && !*abort && silu_I > 0) {
+        // fused gate|up weights (gate_up_row order): lanes 0..15 of the warp on lane quarter q
+        // hold the gates of outputs j = 64 t + 16 q + lane, lanes 16..31 the matching ups;
+        // h = silu(g) u is staged as [token][64 + 8] at column 16 q + lane
+        const int q = warp & 3;
+        const int j = (nbase >> 1) + 16 * q + (lane & 15);
         const bool gate = lane < 16, valid = j < silu_I;
         const int src = gate ? j : silu_I + j;
         const float cs = valid ? __half2float(__ushort_as_half(colscale[src])) : 0.f;
@@ -425,11 +431,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_smallm_tc_kernel(
                 const float y = fmaf(cs, v[i], bs);
                 const float u = __shfl_down_sync(0xffffffffu, y, 16);
                 if (gate)  // silu(y) u, fast exponential and divide (relative error ~1e-6)
-                    ys[(4 * b + i) * LDY + 16 * warp + lane] =
+                    ys[(4 * b + i) * LDY + 16 * q + lane] =
                         __half_as_ushort(__float2half_rn(__fdividef(y, 1.0f + __expf(-y)) * u));
             }
         }
-    } else if (warp < 4 && !*abort) {
+    } else if (is_epi && !*abort) {
         const int n = nbase + row;
         const float cs = n < N ? __half2float(__ushort_as_half(colscale[n])) : 0.f;
         const float bs = (bias && n < N) ? __half2float(__ushort_as_half(bias[n])) : 0.f;
