@@ -668,9 +668,13 @@ DECODE_METRIC = "W4A4+LoRA linear packed-weight GB/s (K=N=4096, small M; min ove
 def run_decode(args, rank, world, local_rank):
     """Config 3: M in {1, 4, 16, 32, 76}, K = N = 4096.  Each timed GEMM call
     reads a different replica of the packed weights (20 replicas > L2), so the
-    weights come from HBM; value = the lowest weight bandwidth over M <= 32."""
+    weights come from HBM; value = the lowest weight bandwidth over M <= 32
+    (with N ranks: every rank streams its own weights, the job's bandwidth)."""
     import torch
+    import torch.distributed as dist
     torch.cuda.set_device(local_rank)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
     from w4a4_quantized_gemm_gb300 import build as wbuild
     wbuild.build()
     import w4a4_quantized_gemm_gb300 as w4
@@ -750,14 +754,12 @@ def run_decode(args, rank, world, local_rank):
             for p_ in packs_a:
                 w4.w4a16_linear_asym(X, p_, cs, b, Y, base.r, torch.cuda.current_stream())
         torch.cuda.synchronize()
-        us = tm(g)
-        uq = tm(gq)
-        uw = tm(gw)
-        ua = tm(ga)
-        results[M] = {"gemm_us": us, "quantize_us": uq, "weight_gbs": wbytes / (us * 1e-6) / 1e9,
-                      "frac_hbm": wbytes / (us * 1e-6) / 1e9 / hbm, "dispatch": disp,
-                      "w4a16_linear_us": uw, "w4a16_weight_gbs": wbytes / (uw * 1e-6) / 1e9,
-                      "w4a16_asym_g128_us": ua, "w4a16_asym_g128_weight_gbs": wbytes / (ua * 1e-6) / 1e9}
+        us, uq, uw, ua = (max_over_ranks(tm(x), dev, world) for x in (g, gq, gw, ga))
+        gbs = job_rate(world, wbytes, us * 1e-3) / 1e9
+        results[M] = {"gemm_us": us, "quantize_us": uq, "weight_gbs": gbs,
+                      "frac_hbm": gbs / (world * hbm), "dispatch": disp,
+                      "w4a16_linear_us": uw, "w4a16_weight_gbs": job_rate(world, wbytes, uw * 1e-3) / 1e9,
+                      "w4a16_asym_g128_us": ua, "w4a16_asym_g128_weight_gbs": job_rate(world, wbytes, ua * 1e-3) / 1e9}
         if M == 32 and not args.no_e2e:
             # end to end through the public API at the metric's binding M: pinned host X in, the two
             # C-ABI calls per weight replica, Y back to pinned host, all in one graph
@@ -793,17 +795,22 @@ def run_decode(args, rank, world, local_rank):
                 st.wait_stream(s_in)
                 st.wait_stream(s_out)
             torch.cuda.synchronize()
-            ue = tm(ge)
-            e2e = {"value": wbytes / (ue * 1e-6) / 1e9, "unit": "GB/s", "h2d_bytes_per_step": M * base.K * 2,
+            ue = max_over_ranks(tm(ge), dev, world)
+            e2e = {"value": job_rate(world, wbytes, ue * 1e-3) / 1e9, "unit": "GB/s", "h2d_bytes_per_step": M * base.K * 2,
                    "d2h_bytes_per_step": M * base.N * 2, "us_per_call": ue, "M": M,
                    "how": "per call: H2D of X from pinned host (copy stream), quantize + linear through the C-ABI, "
                           "D2H of Y (second copy stream, overlapping the next call); CUDA graph over the weight "
                           "replicas"}
     sampler.__exit__()
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    if rank != 0:
+        return 0
     low = min(v["weight_gbs"] for m, v in results.items() if m <= 32)
     m32 = results[32]
     print(json.dumps({
-        "metric": DECODE_METRIC, "value": low, "unit": "GB/s", "n_gpus": 1, "steps": args.steps,
+        "metric": DECODE_METRIC, "value": low, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": m32["gemm_us"] * 1e-3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "int4 codes (fp8 e4m3 operands), fp32 accumulate, fp16 out",
         "data": "synthetic",
@@ -813,7 +820,7 @@ def run_decode(args, rank, world, local_rank):
                                 "residual_per_round": svd_errs,
                                 "what": "w4a4_pack_weights_svd on the K=N=4096 weights, r=32 (offline)"}},
         "gpu_launches": args.steps * R * len(results) * 2, "e2e": e2e, "clocks": sampler.summary(),
-        "roofline": {"bound": "hbm", "achieved": low, "peak": hbm, "unit": "GB/s", "frac": low / hbm,
+        "roofline": {"bound": "hbm", "achieved": low / world, "peak": hbm, "unit": "GB/s", "frac": low / world / hbm,
                      "traffic": None, "kernel": "w4a4_linear (small-M weight-streaming kernel)",
                      "peak_source": f"{hbm_src} HBM copy bandwidth",
                      "algorithmic_bytes_per_call": wbytes}}), flush=True)
