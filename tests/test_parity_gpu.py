@@ -65,8 +65,12 @@ def test_pack_weight_codes_full_range_roundtrip():
 
 
 # -------------------------------------------------------- activation kernel
-@pytest.mark.parametrize("M,K,r", [(1, 64, 0), (17, 128, 16), (64, 1024, 32), (200, 3072, 32), (33, 512, 128)])
+@pytest.mark.parametrize("M,K,r", [(1, 64, 0), (17, 128, 16), (64, 1024, 32), (200, 3072, 32), (33, 512, 128),
+                                   (2061, 5120, 32), (2048, 640, 16)])
 def test_quantize_act_bitexact(M, K, r):
+    """Includes the prefill cluster split (M >= 2048): K in two cluster ranks with
+    a ragged last row block, and a single CTA per row block with unequal groups
+    per warp."""
     c = make_linear_case(M, K, 32, r, seed=M * 7 + K)
     t = to_dev(c)
     packed = pack(c, t)

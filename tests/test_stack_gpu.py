@@ -106,7 +106,7 @@ def test_stack_two_layers_teacher_forced(fused):
 
 
 @pytest.mark.parametrize("M,ld,K,r", [(37, 6144, 3072, 32), (130, 4096, 2048, 0), (5, 1032, 1024, 128),
-                                      (200, 1024, 1024, 16), (11, 10304, 10240, 32)])
+                                      (200, 1024, 1024, 16), (11, 10304, 10240, 32), (2053, 6144, 5120, 32)])
 def test_fused_rmsnorm_quantize_matches_oracle(M, ld, K, r):
     """The fused kernel on a wider-than-K row stride, ragged row counts, an
     all-zero row and outlier columns: codes and scales bit-exact against the
