@@ -15,6 +15,8 @@ Prints one JSON line (metric: effective TOPS = (2MNK + 2Mr(K+N)) / time).
   --impl reference : the CPU oracle timed on the host cores (bounded sample).
   --workload stack : instead, the 28-layer stack of those four linears with
                      RMSNorm glue (112 linears, one CUDA graph per forward pass).
+  --workload decode : the small-M sweep, M in {1, 4, 16, 32, 76}, K = N = 4096.
+  --workload prefill : the two M = 8192 prefill linears (4096->14336, 14336->4096).
 """
 from __future__ import annotations
 
@@ -39,6 +41,8 @@ UNIT = "TOPS"
 WORKLOAD = "qwen3_1024_decoder_layer_linears_M700"
 STACK_METRIC = "W4A4+LoRA linear effective TOPS (28-layer stack, M=700, RMSNorm glue, CUDA graph)"
 STACK_WORKLOAD = "qwen3_1024_28_layer_stack_M700"
+PREFILL_METRIC = "W4A4+LoRA linear effective TOPS (prefill, M=8192: 4096->14336 and 14336->4096)"
+PREFILL_WORKLOAD = "prefill_M8192_K4096_N14336_and_K14336_N4096"
 L2_BYTES = 129 * 2 ** 20
 
 
@@ -827,6 +831,207 @@ def run_decode(args, rank, world, local_rank):
     return 0
 
 
+def run_prefill(args, rank, world, local_rank):
+    """Config 4: one step = the gate/up-style (K=4096, N=14336) and the down-style
+    (K=14336, N=4096) linear at M = 8192, each as quantize + GEMM.  Every step
+    writes 470 MB of Y, so no input stays in L2 from one step to the next; two
+    replicas of every buffer are cycled all the same."""
+    import torch
+    import torch.distributed as dist
+    torch.cuda.set_device(local_rank)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    from w4a4_quantized_gemm_gb300 import build as wbuild
+    wbuild.build()
+    import w4a4_quantized_gemm_gb300 as w4
+    from synthetic import PREFILL
+
+    dev = torch.device("cuda", local_rank)
+    names = list(PREFILL)
+    R = 2
+    L = {}
+    for i, name in enumerate(names):
+        c = make_linear_case(seed=i, **PREFILL[name])
+        W = torch.from_numpy(c.W).to(dev)
+        Ld = torch.from_numpy(c.L_down.view(np.float16).copy()).to(dev)
+        Lu = torch.from_numpy(c.L_up.view(np.float16).copy()).to(dev)
+        packed = torch.empty(w4.packed_weights_bytes(c.N, c.K, c.r), dtype=torch.uint8, device=dev)
+        w4.w4a4_pack_weights(W, Ld, Lu, packed, c.r)
+        del W
+        X = torch.from_numpy(c.X.view(np.float16).copy()).to(dev)
+        cs = torch.from_numpy(c.colscale.view(np.float16).copy()).to(dev)
+        b = torch.from_numpy(c.bias.view(np.float16).copy()).to(dev)
+        wsb = w4.act_workspace_bytes(c.M, c.K, c.r)
+        L[name] = dict(c=c, X=[X] + [X.clone() for _ in range(R - 1)],
+                       packed=[packed] + [packed.clone() for _ in range(R - 1)], cs=cs, b=b,
+                       ws=[torch.empty(wsb, dtype=torch.uint8, device=dev) for _ in range(R)],
+                       Y=[torch.empty((c.M, c.N), dtype=torch.float16, device=dev) for _ in range(R)])
+    torch.cuda.synchronize()
+    ops = sum(metrics.linear_ops(PREFILL[n]["M"], PREFILL[n]["N"], PREFILL[n]["K"], PREFILL[n]["r"]) for n in names)
+    footprint = sum(sum(t.numel() * t.element_size() for k in ("X", "packed", "ws", "Y") for t in d[k])
+                    for d in L.values())
+
+    def launch(name, kind, rep, st, Xsrc=None):
+        d = L[name]
+        c = d["c"]
+        if kind in ("q", "qg"):
+            w4.w4a4_quantize_act(d["X"][rep] if Xsrc is None else Xsrc, d["packed"][rep], d["ws"][rep], c.r, st)
+        if kind in ("g", "qg"):
+            w4.w4a4_linear(d["ws"][rep], d["packed"][rep], d["cs"], d["b"], d["Y"][rep], c.K, c.r,
+                           w4.KERNEL_AUTO, st)
+
+    dispatch = {}
+    for rep in range(R):
+        for n in names:
+            launch(n, "qg", rep, torch.cuda.current_stream())
+            dispatch[n] = w4.w4a4_last_dispatch()
+    torch.cuda.synchronize()
+
+    def capture(fn):
+        graphs = []
+        for rep in range(R):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                fn(rep, torch.cuda.current_stream())
+            graphs.append(g)
+        torch.cuda.synchronize()
+        return graphs
+
+    def timed(graphs, steps):
+        for i in range(args.warmup):
+            graphs[i % len(graphs)].replay()
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for i in range(steps):
+            graphs[i % len(graphs)].replay()
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1)
+
+    step_graphs = capture(lambda rep, st: [launch(n, "qg", rep, st) for n in names])
+    sampler = ClockSampler(local_rank) if rank == 0 else None
+    if sampler:
+        sampler.__enter__()
+        time.sleep(0.3)
+    ms = timed(step_graphs, args.steps)
+    if sampler:
+        sampler.__exit__()
+    ms_per_step = max_over_ranks(ms, dev, world) / args.steps
+    value = job_rate(world, ops, ms_per_step) / 1e12
+
+    # per linear: graphs holding that linear's GEMM (or activation kernel) alone, replicas alternating
+    g_us = {n: 1e3 * timed(capture(lambda rep, st, n=n: launch(n, "g", rep, st)), args.steps) / args.steps
+            for n in names}
+    q_us = {n: 1e3 * timed(capture(lambda rep, st, n=n: launch(n, "q", rep, st)), args.steps) / args.steps
+            for n in names}
+    gemm_s = sum(g_us.values()) * 1e-6
+    peaks = {}
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            peaks = json.load(f)
+    except (OSError, ValueError):
+        pass
+    if "bf16_tflops" in peaks:
+        bf16, peak_src = float(peaks["bf16_tflops"]), "measured"
+    else:
+        bf16, peak_src = 1900.0, "fallback"
+    fp8_peak = 2.0 * bf16  # FP8 tensor kind: measured bf16 burst x nominal fp8/bf16 ratio (4.5/2.25)
+    achieved = ops / gemm_s / 1e12
+    roofline = {"bound": "tensor", "achieved": achieved, "peak": fp8_peak, "unit": "TFLOP/s",
+                "frac": achieved / fp8_peak, "traffic": None,
+                "kernel": "w4a4_linear (GEMM + LoRA up + affine), 2 launches per step",
+                "peak_source": f"{peak_src} bf16 burst x 2 (fp8 kind)",
+                "per_linear_gemm_us": g_us, "per_linear_quantize_us": q_us,
+                "per_linear_gemm_tops": {n: metrics.linear_ops(PREFILL[n]["M"], PREFILL[n]["N"], PREFILL[n]["K"],
+                                                               PREFILL[n]["r"]) / (g_us[n] * 1e-6) / 1e12
+                                         for n in names},
+                "gemm_algorithmic_bytes": sum(metrics.gemm_bytes(**PREFILL[n]) for n in names),
+                "quantize_algorithmic_bytes": sum(metrics.act_bytes(PREFILL[n]["M"], PREFILL[n]["K"],
+                                                                    PREFILL[n]["r"]) for n in names)}
+    roofline["quantize_gbs"] = roofline["quantize_algorithmic_bytes"] / (sum(q_us.values()) * 1e-6) / 1e9
+    i8 = int8_dense_peak_tops()
+    roofline["int8_dense_tops_measured"] = i8
+    roofline["frac_of_int8_dense"] = achieved / i8 if i8 else None
+
+    # end to end through the public API: pinned host X in (copy stream), the two C-ABI calls per
+    # linear once its X has landed, Y back to pinned host (second copy stream)
+    e2e = None
+    if not args.no_e2e:
+        Xh = {n: torch.empty_like(L[n]["X"][0], device="cpu").pin_memory() for n in names}
+        Yh = {n: torch.empty_like(L[n]["Y"][0], device="cpu").pin_memory() for n in names}
+        for n in names:
+            Xh[n].copy_(L[n]["X"][0])
+        h2d = sum(Xh[n].numel() * 2 for n in names)
+        d2h = sum(Yh[n].numel() * 2 for n in names)
+        s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+
+        def e2e_fn(rep, st):
+            start = torch.cuda.Event()
+            start.record(st)
+            s_in.wait_event(start)
+            s_out.wait_event(start)
+            arrived = []
+            with torch.cuda.stream(s_in):
+                for n in names:
+                    L[n]["X"][rep].copy_(Xh[n], non_blocking=True)
+                    ev = torch.cuda.Event()
+                    ev.record(s_in)
+                    arrived.append(ev)
+            for i, n in enumerate(names):
+                st.wait_event(arrived[i])
+                launch(n, "qg", rep, st)
+                done = torch.cuda.Event()
+                done.record(st)
+                s_out.wait_event(done)
+                with torch.cuda.stream(s_out):
+                    Yh[n].copy_(L[n]["Y"][rep], non_blocking=True)
+            st.wait_stream(s_in)
+            st.wait_stream(s_out)
+
+        e_ms = max_over_ranks(timed(capture(e2e_fn), args.steps) / args.steps, dev, world)
+        e2e = {"value": job_rate(world, ops, e_ms) / 1e12, "unit": UNIT, "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "ms_per_step": e_ms,
+               "how": "CUDA graph per step: H2D of both inputs X from pinned host on a copy stream, the two "
+                      "C-ABI calls per linear once its X has landed, D2H of each Y on a second copy stream"}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle
+        oracle.build()
+        done, rows, t0 = 0, 0, time.perf_counter()
+        while time.perf_counter() - t0 < args.cpu_budget and rows < 64:
+            for n in names:
+                c = L[n]["c"]
+                oracle.linear(c.X[rows:rows + 4], c.W, c.L_down, c.L_up, c.colscale, c.bias)
+                done += metrics.linear_ops(4, c.N, c.K, c.r)
+            rows += 4
+        sec = time.perf_counter() - t0
+        cpu = {"value": done / sec / 1e12, "unit": UNIT, "cores": 1, "kind": "oracle",
+               "sample": f"rows 0..{rows - 1} of both linears, 4 rows per call ({done / 1e9:.1f} Gop, {sec:.1f} s)"}
+
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    if rank != 0:
+        return 0
+    line = {
+        "metric": PREFILL_METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "int4 codes (fp8 e4m3 operands), fp32 accumulate, fp16 out",
+        "data": "synthetic",
+        "config": {"workload": PREFILL_WORKLOAD, "M": 8192, "group": 64, "rank": 32,
+                   "linears": {n: [PREFILL[n]["K"], PREFILL[n]["N"]] for n in names}, "replicas": R,
+                   "l2": f"inputs larger than L2: {footprint / 2**20:.0f} MiB cycled", "dispatch": dispatch},
+        "gpu_launches": args.steps * 2 * len(names),
+        "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "clocks": sampler.summary() if sampler else None,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -838,7 +1043,7 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--workload", choices=["layer", "stack", "decode"], default="layer")
+    ap.add_argument("--workload", choices=["layer", "stack", "decode", "prefill"], default="layer")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -847,6 +1052,8 @@ def main():
     local_rank = _env_int("LOCAL_RANK", 0)
     if args.workload == "decode" and args.impl == "ours":
         return run_decode(args, rank, world, local_rank)
+    if args.workload == "prefill" and args.impl == "ours":
+        return run_prefill(args, rank, world, local_rank)
     if args.workload == "stack":
         if args.impl == "reference":
             return run_stack_reference(args, rank, world)
