@@ -532,6 +532,66 @@ def run_stack_reference(args, rank, world):
     return 0
 
 
+def _reference_line(args, world, metric, unit, value, sec_per_step, config, sample):
+    return {
+        "impl": "reference", "metric": metric, "value": value, "unit": unit, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * sec_per_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int64/f64",
+        "data": "synthetic", "config": dict(config, sample=sample),
+        "cpu_baseline": {"value": value, "unit": unit, "cores": 1, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def run_prefill_reference(args, rank, world, rows_per_step=2):
+    """The oracle on the prefill workload: each step, `rows_per_step` rows of
+    both M = 8192 linears (every call quantises the whole weight matrix)."""
+    if rank != 0:
+        return 0
+    import oracle
+    from synthetic import PREFILL
+    oracle.build()
+    cases = [make_linear_case(seed=i, **s) for i, s in enumerate(PREFILL.values())]
+    ops, sec = 0, 0.0
+    for i in range(args.warmup + args.steps):
+        r0 = (i * rows_per_step) % (8192 - rows_per_step)
+        t0 = time.perf_counter()
+        for c in cases:
+            oracle.linear(c.X[r0:r0 + rows_per_step], c.W, c.L_down, c.L_up, c.colscale, c.bias)
+        dt = time.perf_counter() - t0
+        if i >= args.warmup:
+            ops += sum(metrics.linear_ops(rows_per_step, c.N, c.K, c.r) for c in cases)
+            sec += dt
+    config = {"workload": PREFILL_WORKLOAD, "M": 8192, "group": 64, "rank": 32,
+              "linears": {n: [s["K"], s["N"]] for n, s in PREFILL.items()}}
+    print(json.dumps(_reference_line(args, world, PREFILL_METRIC, UNIT, ops / sec / 1e12, sec / args.steps, config,
+                                     f"{rows_per_step} of 8192 rows of both linears per step")), flush=True)
+    return 0
+
+
+def run_decode_reference(args, rank, world):
+    """The oracle on the small-M sweep: each step, the whole M = 32 call (of the
+    sweep's M <= 32, the one with the most work per weight byte, so the lowest
+    bandwidth: the metric's binding case)."""
+    if rank != 0:
+        return 0
+    import oracle
+    from synthetic import SMALL_M_SWEEP
+    oracle.build()
+    c = make_linear_case(seed=0, **SMALL_M_SWEEP[-1])
+    wbytes = metrics.weight_bytes(c.N, c.K)
+    sec = 0.0
+    for i in range(args.warmup + args.steps):
+        t0 = time.perf_counter()
+        oracle.linear(c.X[:32], c.W, c.L_down, c.L_up, c.colscale, c.bias)
+        if i >= args.warmup:
+            sec += time.perf_counter() - t0
+    config = {"workload": "small_m_sweep_K4096_N4096", "group": 64, "rank": 32}
+    value = wbytes * args.steps / sec / 1e9
+    print(json.dumps(_reference_line(args, world, DECODE_METRIC, "GB/s", value, sec / args.steps, config,
+                                     "the M = 32 call of the sweep, whole, per step")), flush=True)
+    return 0
+
+
 def run_stack(args, rank, world, local_rank):
     import torch
     import torch.distributed as dist
@@ -1050,9 +1110,13 @@ def main():
     rank = _env_int("RANK", 0)
     world = _env_int("WORLD_SIZE", 1)
     local_rank = _env_int("LOCAL_RANK", 0)
-    if args.workload == "decode" and args.impl == "ours":
+    if args.workload == "decode":
+        if args.impl == "reference":
+            return run_decode_reference(args, rank, world)
         return run_decode(args, rank, world, local_rank)
-    if args.workload == "prefill" and args.impl == "ours":
+    if args.workload == "prefill":
+        if args.impl == "reference":
+            return run_prefill_reference(args, rank, world)
         return run_prefill(args, rank, world, local_rank)
     if args.workload == "stack":
         if args.impl == "reference":
