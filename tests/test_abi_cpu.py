@@ -38,6 +38,29 @@ def test_library_exports_every_declared_symbol(L):
         assert name in w4.SIGNATURES, f"binding has no signature for {name}"
 
 
+def declared_arity():
+    """Parameter count of every declared entry point, read off its prototype."""
+    src = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    src = re.sub(r"//[^\n]*", "", src)
+    out = {}
+    for m in re.finditer(r"\b(w4a(?:4|16)_[a-z0-9_]+)\s*\(", src):
+        depth, i = 1, m.end()
+        while depth:
+            depth += {"(": 1, ")": -1}.get(src[i], 0)
+            i += 1
+        params = src[m.end():i - 1].strip()
+        if src[i:].lstrip().startswith(";") or src[i:].lstrip().startswith("{"):
+            out[m.group(1)] = 0 if params in ("", "void") else params.count(",") + 1
+    return out
+
+
+def test_binding_signatures_match_the_header_arity():
+    arity = declared_arity()
+    assert set(arity) == set(declared_functions())
+    for name, n in arity.items():
+        assert len(w4.SIGNATURES[name][1]) == n, f"{name}: header {n} parameters, binding {len(w4.SIGNATURES[name][1])}"
+
+
 def test_size_queries(L):
     G = 1024 // 64
     # packed: L_down first, then codes, scales, L_up; 256-byte aligned sections
