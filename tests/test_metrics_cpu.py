@@ -66,3 +66,29 @@ def test_ridge_and_crossover():
     ridge = V["dense_fp16_flops"][0] / V["hbm_bytes_per_s"][0]
     assert _agrees(ridge, *V["ridge_flops_per_byte"])
     assert _agrees(metrics.crossover_m(ridge, group=128), *V["crossover_m"])
+
+
+# Per-config totals as tabulated from the definition ops = 2MNK + 2Mr(K+N) and
+# bytes = codes + fp16 group scales (hand-computed, one line per config).
+OPS = {
+    (64, 1024, 1024): 142_606_336,
+    (700, 4096, 1024): 6_101_401_600,      # qkv (M, N, K)
+    (700, 1024, 2048): 3_073_638_400,      # o
+    (700, 6144, 1024): 9_129_164_800,      # gate_up
+    (700, 1024, 3072): 4_587_520_000,      # down
+    (8192, 14336, 4096): 971_736_350_720,  # prefill, gate/up-style
+    (8192, 4096, 14336): 971_736_350_720,  # prefill, down-style
+}
+
+
+@pytest.mark.parametrize("MNK,ops", list(OPS.items()))
+def test_linear_ops_per_config(MNK, ops):
+    assert metrics.linear_ops(*MNK, 32) == ops
+
+
+def test_workload_totals():
+    import bench
+    assert bench.layer_ops() == 6_101_401_600 + 3_073_638_400 + 9_129_164_800 + 4_587_520_000
+    assert bench.stack_ops() == 640_968_294_400
+    assert metrics.weight_bytes(4096, 4096) == 8_912_896     # the small-M sweep's packed weights + scales
+    assert metrics.weight_bytes(1024, 1024) == 524_288 + 32_768
