@@ -5,7 +5,7 @@
 //
 // GB300 design:
 //  * A thread-block cluster of CK CTAs (8 warps each) owns 16 rows; each CTA
-//    takes a contiguous range of the K groups, about two per warp.  Every
+//    takes a contiguous range of the K groups, one or two per warp.  Every
 //    warp pushes its fp32 LoRA partial tiles (16 rows x 8 columns each) with
 //    st.async into the shared memory of the CTA that owns the tile (tile t
 //    belongs to cluster rank t % CK), completing bytes on that CTA's
