@@ -25,6 +25,7 @@ def _run(args, rank=0, world=1):
 @pytest.mark.parametrize("workload,metric,unit", [
     ("layer", bench.METRIC, "TOPS"),
     ("decode", bench.DECODE_METRIC, "GB/s"),
+    ("prefill", bench.PREFILL_METRIC, "TOPS"),
 ])
 def test_reference_line(workload, metric, unit):
     lines = _run(["--workload", workload, "--steps", "1", "--warmup", "3"])
