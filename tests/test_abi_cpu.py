@@ -123,6 +123,70 @@ def test_argument_checks_precede_any_launch(L):
     assert L.w4a4_quantize_act_rmsnorm(A, 1024, A, 0, 1024, 32, A, big, None) == 0  # M == 0: no-op
 
 
+def test_argument_checks_of_the_variant_entry_points(L):
+    """W4A16 (plain and asymmetric), the gate|up packer and SiLU linear, the SVD
+    LoRA calls and the allocation-free layer refuse bad calls on the host."""
+    A = _vp(0x10000)
+    big = 1 << 40
+    w16 = lambda M, N, K, r, X=A, y=A, pkb=big: L.w4a16_linear(X, A, pkb, A, None, M, N, K, r, y, None)
+    assert w16(4, 1024, 1000, 32) == 2
+    assert w16(-1, 1024, 1024, 32) == 1
+    assert w16(0, 1024, 1024, 32) == 0
+    assert w16(4, 1024, 1024, 32, X=None) == 1
+    assert w16(4, 1024, 1024, 32, y=_vp(0x10008)) == 3
+    assert w16(4, 1024, 1024, 32, pkb=100) == 4
+    wa = lambda M, N, K, r, pkb=big: L.w4a16_linear_asym(A, A, pkb, A, None, M, N, K, r, A, None)
+    assert wa(4, 1024, 192, 32) == 2           # K % 128 != 0 (group-128 weights)
+    assert wa(-1, 1024, 1024, 32) == 1
+    assert wa(0, 1024, 1024, 32) == 0
+    assert wa(4, 1024, 1024, 32, pkb=100) == 4
+    pa = lambda N, K, r, W=A, pkb=big: L.w4a16_pack_weights_asym(W, A, A, N, K, r, A, pkb, None)
+    assert pa(1024, 192, 32) == 2
+    assert pa(1024, 1024, 32, W=None) == 1
+    assert pa(1024, 1024, 32, W=_vp(0x10004)) == 3
+    assert pa(1024, 1024, 32, pkb=100) == 4
+    gu = lambda N, K, r, W=A, pkb=big: L.w4a4_pack_weights_gate_up(W, A, A, N, K, r, A, pkb, None)
+    assert gu(48, 1024, 32) == 2                # gate|up halves of 16 columns each: N % 32 != 0
+    assert gu(1024, 1024, 32, W=None) == 1
+    assert gu(1024, 1024, 32, pkb=100) == 4
+    sm = lambda M, N, K, r, wsb=big: L.w4a4_linear_silu_mul(A, wsb, A, big, A, None, M, N, K, r, A, None)
+    assert sm(64, 48, 1024, 32) == 2
+    assert sm(-1, 1024, 1024, 32) == 1
+    assert sm(0, 1024, 1024, 32) == 0
+    assert sm(64, 1024, 1024, 32, wsb=100) == 4
+    sv = lambda r=32, rounds=3, power=8, scratch=A, sb=big, W=A: L.w4a4_pack_weights_svd(
+        W, 1024, 1024, r, rounds, power, 7, A, big, A, A, None, scratch, sb, None)
+    assert sv(r=0) == 2 and sv(r=8) == 2        # rank below 16, or not a multiple of 16
+    assert sv(rounds=0) == 1 and sv(rounds=17) == 1 and sv(power=-1) == 1 and sv(power=65) == 1
+    assert sv(scratch=None) == 1
+    assert sv(W=_vp(0x10004)) == 3
+    assert sv(sb=16) == 4
+    ts = lambda r=32, power=8, U=A, sb=big, Amat=A: L.w4a4_truncated_svd(
+        Amat, 1024, 1024, r, power, 7, U, A, A, A, sb, None)
+    assert ts(r=0) == 2 and ts(power=-1) == 1 and ts(power=65) == 1 and ts(U=None) == 1
+    assert ts(Amat=_vp(0x10004)) == 3
+    assert ts(sb=16) == 4
+    assert L.w4a4_svd_lora_scratch_bytes(1024, 1024, 0) == 0
+    assert L.w4a4_svd_lora_scratch_bytes(1024, 1000, 32) == 0
+    assert L.w4a4_svd_lora_scratch_bytes(1024, 1024, 32) > 0
+    na = lambda M, N, K, r: L.w4a4_linear_noalloc(A, A, big, A, None, M, N, K, r, A, None)
+    assert na(-1, 1024, 1024, 32) == 1
+    assert na(0, 1024, 1024, 32) == 0
+    assert na(64, 1024, 1000, 32) == 2 and na(64, 1024, 1024, 24) == 2
+    assert na(8192, 1024, 4096, 32) == 4        # the workspace would not fit the library's array
+
+
+def test_stream_k_switch(L):
+    before = L.w4a4_stream_k()
+    try:
+        L.w4a4_set_stream_k(1)
+        assert L.w4a4_stream_k() == 1
+        L.w4a4_set_stream_k(0)
+        assert L.w4a4_stream_k() == 0
+    finally:
+        L.w4a4_set_stream_k(before)
+
+
 @pytest.mark.skipif(torch.cuda.is_available(), reason="valid shapes would launch on a GPU box")
 def test_valid_call_without_device_reports_no_device(L):
     A = _vp(0x10000)
