@@ -187,7 +187,7 @@ def test_stream_k_switch(L):
         L.w4a4_set_stream_k(before)
 
 
-@pytest.mark.skipif(torch.cuda.is_available(), reason="valid shapes would launch on a GPU box")
+@pytest.mark.skipif(torch.cuda.is_available(), reason="valid shapes would launch on a machine with a GPU")
 def test_valid_call_without_device_reports_no_device(L):
     A = _vp(0x10000)
     st = L.w4a4_linear(A, 1 << 40, A, 1 << 40, A, None, 64, 1024, 1024, 32, A, None)
