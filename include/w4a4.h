@@ -305,7 +305,10 @@ int w4a4_small_m_threshold(void);
  * at load. */
 int w4a4_stream_k(void);
 void w4a4_set_stream_k(int on);
-void w4a4_set_small_m_threshold(int m);     /* M <= threshold -> small-M kernel */
+/* AUTO dispatch: M <= threshold -> the small-M kernel, else the tcgen05 tiles.
+ * Default 32, or W4A4_SMALL_M at the first query; a negative value means 0
+ * (the tiles for every M). */
+void w4a4_set_small_m_threshold(int m);
 int w4a4_layout_version(void);
 
 #ifdef __cplusplus

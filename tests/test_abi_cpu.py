@@ -187,6 +187,19 @@ def test_stream_k_switch(L):
         L.w4a4_set_stream_k(before)
 
 
+def test_small_m_threshold_setting(L):
+    before = L.w4a4_small_m_threshold()
+    assert before >= 0
+    try:
+        L.w4a4_set_small_m_threshold(16)
+        assert L.w4a4_small_m_threshold() == 16
+        L.w4a4_set_small_m_threshold(-5)          # negative means never: the tiled kernel for every M
+        assert L.w4a4_small_m_threshold() == 0
+    finally:
+        L.w4a4_set_small_m_threshold(before)
+    assert L.w4a4_small_m_threshold() == before
+
+
 @pytest.mark.skipif(torch.cuda.is_available(), reason="valid shapes would launch on a machine with a GPU")
 def test_valid_call_without_device_reports_no_device(L):
     A = _vp(0x10000)

@@ -166,7 +166,8 @@ int w4a4_small_m_threshold(void) {
     std::lock_guard<std::mutex> lk(g_mu);
     if (g_small_m_threshold < 0) {
         const char* e = std::getenv("W4A4_SMALL_M");
-        g_small_m_threshold = e ? std::atoi(e) : kDefaultSmallM;
+        const int v = e ? std::atoi(e) : kDefaultSmallM;
+        g_small_m_threshold = v < 0 ? 0 : v;
     }
     return g_small_m_threshold;
 }
