@@ -166,10 +166,16 @@ def run_reference(args, rank, world):
 
 # ------------------------------------------------------------------ clocks
 class ClockSampler:
+    """nvidia-smi samples (every 200 ms) of the SM clock and the throttle
+    reasons while the benchmark runs.  The caller keeps the GPU under the timed
+    load for the whole sampling window (an untimed pre-roll of the same work,
+    then the timed region, marked with mark_start / mark_end)."""
+
     def __init__(self, gpu_index: int):
         self.gpu = gpu_index
         self.proc = None
         self.lines = []
+        self.t_start = self.t_end = None
 
     def __enter__(self):
         q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -187,7 +193,13 @@ class ClockSampler:
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.lines.append((time.monotonic(), line.strip()))
+
+    def mark_start(self):
+        self.t_start = time.monotonic()
+
+    def mark_end(self):
+        self.t_end = time.monotonic()
 
     def __exit__(self, *a):
         if self.proc is not None:
@@ -198,9 +210,9 @@ class ClockSampler:
                 self.proc.kill()
 
     def summary(self):
-        sm, mx, reasons = [], None, set()
+        sm, mx, reasons, inside = [], None, set(), 0
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
+        for t, ln in self.lines:
             p = [x.strip() for x in ln.split(",")]
             if len(p) < 9:
                 continue
@@ -212,9 +224,33 @@ class ClockSampler:
             for n, v in zip(names, p[5:9]):
                 if v.lower().startswith("active"):
                     reasons.add(n)
+            if self.t_start is not None and self.t_end is not None and self.t_start <= t <= self.t_end:
+                inside += 1
         if not sm:
             return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": ["unavailable"], "samples": 0}
-        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+        out = {"sm_mhz": float(np.median(sm)), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+        if self.t_start is not None and self.t_end is not None:
+            out.update(samples_in_timed_region=inside,
+                       window="untimed pre-roll of the timed work, then the timed region")
+        return out
+
+
+def preroll(replay, seconds: float = 0.5, sync=None) -> int:
+    """Untimed replays of the timed work for `seconds`, so that the GPU is under
+    that load while the clock sampler starts (synchronising every 16 replays
+    keeps the launch queue short).  Returns the number of replays."""
+    if sync is None:
+        import torch
+        sync = torch.cuda.synchronize
+    t0 = time.perf_counter()
+    i = 0
+    while time.perf_counter() - t0 < seconds:
+        replay(i)
+        i += 1
+        if i % 16 == 0:
+            sync()
+    sync()
+    return i
 
 
 # ------------------------------------------------------------------ GPU arm
@@ -319,9 +355,12 @@ def run_ours(args, rank, world, local_rank):
     sampler = ClockSampler(local_rank) if rank == 0 else None
     if sampler:
         sampler.__enter__()
-        time.sleep(0.3)
+    preroll(lambda i: step_graphs[i % len(step_graphs)].replay())
+    if sampler:
+        sampler.mark_start()
     ms = timed(step_graphs, args.steps)
     if sampler:
+        sampler.mark_end()
         sampler.__exit__()
     ms = max_over_ranks(ms, dev, world)
     if world > 1:
@@ -657,9 +696,12 @@ def run_stack(args, rank, world, local_rank):
     sampler = ClockSampler(local_rank) if rank == 0 else None
     if sampler:
         sampler.__enter__()
-        time.sleep(0.3)
+    preroll(lambda i: fwd.replay())
+    if sampler:
+        sampler.mark_start()
     ms = timed(fwd, args.steps)
     if sampler:
+        sampler.mark_end()
         sampler.__exit__()
     ms = max_over_ranks(ms, dev, world)
     ms_per_step = ms / args.steps
@@ -975,9 +1017,12 @@ def run_prefill(args, rank, world, local_rank):
     sampler = ClockSampler(local_rank) if rank == 0 else None
     if sampler:
         sampler.__enter__()
-        time.sleep(0.3)
+    preroll(lambda i: step_graphs[i % len(step_graphs)].replay())
+    if sampler:
+        sampler.mark_start()
     ms = timed(step_graphs, args.steps)
     if sampler:
+        sampler.mark_end()
         sampler.__exit__()
     ms_per_step = max_over_ranks(ms, dev, world) / args.steps
     value = job_rate(world, ops, ms_per_step) / 1e12
