@@ -28,6 +28,11 @@ Status of the pins (tests/test_oracle_pins.py):
   * silu_mul                  -- pinned (closed forms: silu(0) = 0, silu(ln 3) =
                                  (3/4) ln 3, silu(v) -> v and -> 0 in the tails;
                                  the gate/up column split on crafted rows)
+  * rmsnorm_f16 / f64_to_f16  -- pinned (constant rows -> +-1 exactly, a zero row
+                                 -> 0, columns past K ignored, odd symmetry, unit
+                                 mean square; the encoder against numpy's rounding)
+  * linear_sampled /          -- pinned (equal to the full evaluators on the same
+    silu_mul_linear_sampled      rows and columns)
 """
 from __future__ import annotations
 
