@@ -253,6 +253,107 @@ def preroll(replay, seconds: float = 0.5, sync=None) -> int:
     return i
 
 
+# ------------------------------------------------------------ host and ncu facts
+def host_cpu():
+    """nproc and the CPU model name of this host (lscpu), for the oracle baseline."""
+    model = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for ln in out.splitlines():
+            if ln.lower().startswith("model name"):
+                model = ln.split(":", 1)[1].strip()
+                break
+    except (OSError, subprocess.SubprocessError):
+        pass
+    return {"nproc": os.cpu_count(), "cpu_model": model}
+
+
+def kernel_source_hash(name: str) -> str:
+    """sha256 (first 16 hex digits) of one CUDA source file of the library."""
+    import hashlib
+    with open(os.path.join(ROOT, "w4a4_quantized_gemm_gb300", "csrc", name), "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of the GEMM launches
+# of one step, from the ncu capture summarised under profiles/, keyed by the
+# hash of the kernel source they were taken on: once the kernel changes, the
+# counters no longer describe it and traffic is reported as null.
+NCU_TRAFFIC = {}
+
+
+def ncu_traffic(workload: str, source: str = "gemm_tc.cu"):
+    rec = NCU_TRAFFIC.get((workload, kernel_source_hash(source)))
+    return dict(rec) if rec else None
+
+
+def step_stats(ms):
+    """median, p10 and p90 of per-step times (ms)."""
+    a = np.asarray(ms, np.float64)
+    return {"median": float(np.median(a)), "p10": float(np.percentile(a, 10)), "p90": float(np.percentile(a, 90)),
+            "n": int(a.size)}
+
+
+def decode_sweep(w4, dev, steps: int, warmup: int, Ms=(1, 4, 16, 32), R: int = 20, hbm: float = 6800.0):
+    """The small-M calls (K = N = 4096, r = 32): per M, the whole call (the
+    activation kernel and the GEMM, back to back) and the GEMM alone, each in a
+    CUDA graph over R weight replicas (> L2), so the weights come from HBM.
+    GB/s = packed weights + scales (the bytes every call must stream) / time."""
+    import torch
+    from synthetic import SMALL_M_SWEEP
+    base = make_linear_case(seed=0, **SMALL_M_SWEEP[-1])
+    W = torch.from_numpy(base.W).to(dev)
+    Ld = torch.from_numpy(base.L_down.view(np.float16).copy()).to(dev)
+    Lu = torch.from_numpy(base.L_up.view(np.float16).copy()).to(dev)
+    packed0 = torch.empty(w4.packed_weights_bytes(base.N, base.K, base.r), dtype=torch.uint8, device=dev)
+    w4.w4a4_pack_weights(W, Ld, Lu, packed0, base.r)
+    del W
+    packs = [packed0.clone() for _ in range(R)]
+    cs = torch.from_numpy(base.colscale.view(np.float16).copy()).to(dev)
+    b = torch.from_numpy(base.bias.view(np.float16).copy()).to(dev)
+    wbytes = metrics.weight_bytes(base.N, base.K)
+    out = {}
+    for M in Ms:
+        X = torch.from_numpy(base.X[:M].view(np.float16).copy()).to(dev)
+        ws = torch.empty(w4.act_workspace_bytes(M, base.K, base.r), dtype=torch.uint8, device=dev)
+        Y = torch.empty((M, base.N), dtype=torch.float16, device=dev)
+        w4.w4a4_quantize_act(X, packs[0], ws, base.r)
+        w4.w4a4_linear(ws, packs[0], cs, b, Y, base.K, base.r)
+        disp = w4.w4a4_last_dispatch()
+        torch.cuda.synchronize()
+        gw, gg = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gw):
+            for p_ in packs:
+                st = torch.cuda.current_stream()
+                w4.w4a4_quantize_act(X, p_, ws, base.r, st)
+                w4.w4a4_linear(ws, p_, cs, b, Y, base.K, base.r, w4.KERNEL_AUTO, st)
+        with torch.cuda.graph(gg):
+            for p_ in packs:
+                w4.w4a4_linear(ws, p_, cs, b, Y, base.K, base.r, w4.KERNEL_AUTO, torch.cuda.current_stream())
+        torch.cuda.synchronize()
+
+        def tm(graph):
+            for _ in range(max(warmup, 3)):
+                graph.replay()
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            for _ in range(steps):
+                graph.replay()
+            e1.record()
+            torch.cuda.synchronize()
+            return e0.elapsed_time(e1) * 1e3 / (steps * R)
+
+        uw, ug = tm(gw), tm(gg)
+        out[M] = {"whole_call_us": uw, "whole_call_gbs": wbytes / (uw * 1e-6) / 1e9,
+                  "gemm_us": ug, "gemm_gbs": wbytes / (ug * 1e-6) / 1e9, "dispatch": disp}
+    low = min(out, key=lambda m: out[m]["whole_call_gbs"])
+    return {"per_M": out, "min_whole_call_gbs": out[low]["whole_call_gbs"], "at_M": low,
+            "frac_hbm": out[low]["whole_call_gbs"] / hbm, "hbm_gbs": hbm, "weight_bytes_per_call": wbytes,
+            "what": "whole call = w4a4_quantize_act + w4a4_linear (K = N = 4096, r = 32) per weight replica; "
+                    f"{R} replicas, {R * wbytes / 2**20:.0f} MiB > L2; min over M <= 32 is the headline"}
+
+
 # ------------------------------------------------------------------ GPU arm
 def run_ours(args, rank, world, local_rank):
     import torch
@@ -352,13 +453,35 @@ def run_ours(args, rank, world, local_rank):
         torch.cuda.synchronize()
         return e0.elapsed_time(e1)
 
+    # A step is P passes of the layer (each on the next replica), P chosen so that
+    # the K timed steps last at least --min-timed-s: long enough for the clock
+    # sampler (one sample per 200 ms) to see the timed region itself.
+    t_pass = timed(step_graphs, 4 * R) / (4 * R)
+    P = max(1, int(np.ceil(args.min_timed_s * 1e3 / (args.steps * t_pass))))
+
+    def timed_steps(steps):
+        for i in range(args.warmup * P):
+            step_graphs[i % R].replay()
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+        ev[0].record()
+        for k in range(steps):
+            for j in range(P):
+                step_graphs[(k * P + j) % R].replay()
+            ev[k + 1].record()
+        torch.cuda.synchronize()
+        per = [ev[k].elapsed_time(ev[k + 1]) for k in range(steps)]
+        return ev[0].elapsed_time(ev[steps]), per
+
     sampler = ClockSampler(local_rank) if rank == 0 else None
     if sampler:
         sampler.__enter__()
     preroll(lambda i: step_graphs[i % len(step_graphs)].replay())
     if sampler:
         sampler.mark_start()
-    ms = timed(step_graphs, args.steps)
+    ms, per_step = timed_steps(args.steps)
     if sampler:
         sampler.mark_end()
         sampler.__exit__()
@@ -366,7 +489,9 @@ def run_ours(args, rank, world, local_rank):
     if world > 1:
         dist.barrier()
     ms_per_step = ms / args.steps
-    value = job_rate(world, layer_ops(), ms_per_step) / 1e12
+    value = job_rate(world, P * layer_ops(), ms_per_step) / 1e12
+    stats = step_stats(per_step)
+    stats.update({f"{k}_tops": P * layer_ops() / (stats[k] * 1e-3) / 1e12 for k in ("median", "p10", "p90")})
 
     # per-kernel durations.  Per step: one graph per replica holding the step's
     # four GEMMs (or four activation kernels), the same buffers as the step.
@@ -421,9 +546,12 @@ def run_ours(args, rank, world, local_rank):
         bf16, peak_src = 1900.0, "fallback"
     fp8_peak = 2.0 * bf16  # FP8 tensor kind: measured bf16 burst x nominal fp8/bf16 ratio (4.5/2.25)
     achieved = layer_ops() / gemm_s / 1e12
+    traffic = ncu_traffic(WORKLOAD)
     roofline = {"bound": "tensor", "achieved": achieved, "peak": fp8_peak, "unit": "TFLOP/s",
-                "frac": achieved / fp8_peak, "traffic": None,
-                "kernel": "w4a4_linear (GEMM + LoRA up + affine), 4 launches per step",
+                "frac": achieved / fp8_peak, "traffic": traffic["bytes_per_pass"] if traffic else None,
+                "traffic_source": traffic["source"] if traffic else
+                "null: no ncu capture of the current gemm_tc.cu source",
+                "kernel": "w4a4_linear (GEMM + LoRA up + affine), 4 launches per layer pass",
                 "peak_source": f"{peak_src} bf16 burst x 2 (fp8 kind)",
                 "gemm_us_per_step": gemm_s * 1e6, "quantize_us_per_step": q_s * 1e6,
                 "per_linear_gemm_us": g_us, "per_linear_quantize_us": q_us,
@@ -485,11 +613,19 @@ def run_ours(args, rank, world, local_rank):
                       "C-ABI calls per linear once its X has landed, D2H of each Y on a second copy stream "
                       "while the next linear computes"}
 
+    # the small-M half of the metric: whole calls (activation kernel + GEMM) at M <= 32
+    decode = None
+    if not args.no_decode:
+        hbm = float(peaks["hbm_gbs"]) if "hbm_gbs" in peaks else 6800.0
+        decode = decode_sweep(w4, dev, max(args.steps, 20), args.warmup, hbm=hbm)
+        decode["peak_source"] = "measured HBM copy bandwidth" if "hbm_gbs" in peaks else "fallback"
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         ops, sec, rows = time_oracle(args.cpu_budget)
         cpu = {"value": ops / sec / 1e12, "unit": UNIT, "cores": 1, "kind": "oracle",
-               "sample": f"rows 0..{rows - 1} of each of the 4 linears ({ops / 1e9:.2f} Gop, {sec:.1f} s)"}
+               "sample": f"rows 0..{rows - 1} of each of the 4 linears ({ops / 1e9:.2f} Gop, {sec:.1f} s)",
+               **host_cpu()}
 
     if world > 1:
         dist.barrier()
@@ -503,9 +639,10 @@ def run_ours(args, rank, world, local_rank):
         "vs_baseline": None, "dtype": "int4 codes (fp8 e4m3 operands), fp32 accumulate, fp16 out",
         "data": "synthetic",
         "config": base_config({"replicas": R, "l2": f"inputs larger than L2: {footprint / 2**20:.0f} MiB cycled",
-                               "dispatch": dispatch}),
-        "gpu_launches": args.steps * 2 * len(names),
-        "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
+                               "passes_per_step": P, "dispatch": dispatch}),
+        "step_ms": stats, "ms_per_pass": ms_per_step / P,
+        "gpu_launches": args.steps * P * 2 * len(names),
+        "roofline": roofline, "decode": decode, "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
     }
     print(json.dumps(line), flush=True)
     return 0
@@ -768,7 +905,7 @@ def run_stack(args, rank, world, local_rank):
 
 
 # ------------------------------------------------------- config 3: small M
-DECODE_METRIC = "W4A4+LoRA linear packed-weight GB/s (K=N=4096, small M; min over M<=32)"
+DECODE_METRIC = "W4A4+LoRA linear packed-weight GB/s of the whole call (K=N=4096, small M; min over M<=32)"
 
 
 def run_decode(args, rank, world, local_rank):
@@ -907,17 +1044,26 @@ def run_decode(args, rank, world, local_rank):
                    "how": "per call: H2D of X from pinned host (copy stream), quantize + linear through the C-ABI, "
                           "D2H of Y (second copy stream, overlapping the next call); CUDA graph over the weight "
                           "replicas"}
+    # whole calls (activation kernel + GEMM back to back): the headline
+    whole = decode_sweep(w4, dev, args.steps, args.warmup, Ms=tuple(s_["M"] for s_ in SMALL_M_SWEEP), R=R, hbm=hbm)
     sampler.__exit__()
+    for m_, v in whole["per_M"].items():
+        v["whole_call_us"] = max_over_ranks(v["whole_call_us"], dev, world)
+        v["whole_call_gbs"] = job_rate(world, wbytes, v["whole_call_us"] * 1e-3) / 1e9
+        results[m_].update(whole_call_us=v["whole_call_us"], whole_call_gbs=v["whole_call_gbs"],
+                           frac_hbm_whole_call=v["whole_call_gbs"] / (world * hbm))
     if world > 1:
         dist.barrier()
         dist.destroy_process_group()
     if rank != 0:
         return 0
-    low = min(v["weight_gbs"] for m, v in results.items() if m <= 32)
+    low = min(v["whole_call_gbs"] for m, v in results.items() if m <= 32)
+    low_gemm = min(v["weight_gbs"] for m, v in results.items() if m <= 32)
     m32 = results[32]
     print(json.dumps({
         "metric": DECODE_METRIC, "value": low, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": m32["gemm_us"] * 1e-3, "higher_is_better": True, "scaling": "weak",
+        "warmup": args.warmup, "ms_per_step": m32["whole_call_us"] * 1e-3, "higher_is_better": True,
+        "scaling": "weak", "gemm_only_min_gbs": low_gemm,
         "vs_baseline": None, "dtype": "int4 codes (fp8 e4m3 operands), fp32 accumulate, fp16 out",
         "data": "synthetic",
         "config": {"workload": "small_m_sweep_K4096_N4096", "group": 64, "rank": 32, "replicas": R,
@@ -926,8 +1072,9 @@ def run_decode(args, rank, world, local_rank):
                                 "residual_per_round": svd_errs,
                                 "what": "w4a4_pack_weights_svd on the K=N=4096 weights, r=32 (offline)"}},
         "gpu_launches": args.steps * R * len(results) * 2, "e2e": e2e, "clocks": sampler.summary(),
-        "roofline": {"bound": "hbm", "achieved": low / world, "peak": hbm, "unit": "GB/s", "frac": low / world / hbm,
-                     "traffic": None, "kernel": "w4a4_linear (small-M weight-streaming kernel)",
+        "roofline": {"bound": "hbm", "achieved": low_gemm / world, "peak": hbm, "unit": "GB/s",
+                     "frac": low_gemm / world / hbm, "traffic": None,
+                     "kernel": "w4a4_linear (small-M weight-streaming kernel; the value above is the whole call)",
                      "peak_source": f"{hbm_src} HBM copy bandwidth",
                      "algorithmic_bytes_per_call": wbytes}}), flush=True)
     return 0
@@ -1148,6 +1295,9 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-decode", action="store_true", help="layer workload: skip the small-M sub-record")
+    ap.add_argument("--min-timed-s", type=float, default=0.5,
+                    help="layer workload: passes per step chosen so that the timed steps last at least this long")
     ap.add_argument("--workload", choices=["layer", "stack", "decode", "prefill"], default="layer")
     args = ap.parse_args()
     if args.warmup < 3:

@@ -19,9 +19,11 @@
  *
  * Conventions for every entry point
  *   - All data pointers are DEVICE pointers of the current CUDA device, owned by
- *     the caller.  The library never allocates, frees or keeps device memory,
- *     and keeps no state besides a per-device property cache and the text of
- *     the last dispatch decision.
+ *     the caller.  No entry point allocates or frees device memory.  The
+ *     library's only device memory of its own is the fixed array that
+ *     w4a4_linear_noalloc uses as its workspace (a __device__ variable, part
+ *     of the loaded module); besides it, the library keeps a per-device
+ *     property cache and the text of the last dispatch decision.
  *   - fp16 tensors are passed as uint16_t bit patterns (IEEE binary16).
  *   - Work is enqueued on `stream` (may be 0); nothing synchronises unless the
  *     function says so.  Argument checks happen on the host before any launch,
@@ -98,12 +100,11 @@ typedef enum {
 
 /* Kernel selection for w4a4_linear_select / w4a4_debug_group_partials. */
 typedef enum {
-    W4A4_KERNEL_AUTO = 0,   /* by M: M <= threshold the tcgen05 small-M kernel, else tensor-core
-                               tiles (the partials dump takes the warp-MMA kernel at small M) */
+    W4A4_KERNEL_AUTO = 0,   /* by M: M <= threshold the tcgen05 small-M kernel, else tensor-core tiles */
     W4A4_KERNEL_TC = 1,     /* tcgen05 (TMEM accumulators, bulk-copy pipeline) */
     W4A4_KERNEL_SMALLM = 2, /* weight-streaming kernel (warp-level MMA, split over K) */
     W4A4_KERNEL_SMALLM_TC = 3 /* weight-streaming kernel on tcgen05 (weights as the 128-row operand, tokens
-                                 as N; split over K); no partials dump (w4a4_debug_group_partials refuses it) */
+                                 as N; split over K) */
 } w4a4_kernel;
 
 /* ---- size queries (bytes of caller-allocated device buffers) ---- */
@@ -133,8 +134,11 @@ w4a4_status w4a4_pack_weight_codes(const int8_t* codes, const uint16_t* scales,
  * (fp32, IEEE division), qA = clamp(rint(X / sA), -8, 7), SA = sum of codes;
  * in the same pass lora_act[m, :] = X[m, :] L_down (fp16 inputs, fp32
  * accumulation, deterministic order), stored as fp16.  L_down is read from the
- * packed weight buffer.  Writes the activation workspace. */
-w4a4_status w4a4_quantize_act(const uint16_t* X, const void* packed, int M, int K, int r,
+ * packed weight buffer (its first K * r * 2 bytes; packed may be NULL when
+ * r == 0); packed_bytes is that buffer's size, and a size below K * r * 2
+ * returns W4A4_ERR_WORKSPACE before any launch.  Writes the activation
+ * workspace (act_ws_bytes >= w4a4_act_workspace_min_bytes(M, K, r)). */
+w4a4_status w4a4_quantize_act(const uint16_t* X, const void* packed, size_t packed_bytes, int M, int K, int r,
                               void* act_ws, size_t act_ws_bytes, cudaStream_t stream);
 
 /* ---- W4A4 GEMM + LoRA up + column affine ([VC] 3.7, [BW] 1)
@@ -206,9 +210,11 @@ w4a4_status w4a4_linear_select(const void* act_ws, size_t act_ws_bytes, const vo
  * outputs): it runs w4a4_quantize_act and w4a4_linear back to back with the
  * activation workspace in a fixed array of W4A4_NOALLOC_WORKSPACE_BYTES that
  * the library keeps in each device's memory from load until process exit.
- * X fp16 [M, K], packed/colscale/bias/Y as for w4a4_linear.  Returns
- * W4A4_ERR_WORKSPACE, before any launch, when w4a4_act_workspace_bytes(M, K, r)
- * exceeds the array.  The first call on a device looks up the array's device
+ * X fp16 [M, K], packed/colscale/bias/Y as for w4a4_linear.  Every argument
+ * check of both steps runs before anything is launched; among them, the call
+ * returns W4A4_ERR_WORKSPACE when w4a4_act_workspace_min_bytes(M, K, r) exceeds
+ * the array (the GEMM's optional stream-K hand-over area is never used through
+ * this entry point).  The first call on a device looks up the array's device
  * address (make that first call before any stream capture).  All calls share
  * the array: calls that overlap on the GPU race.  It allocates and frees
  * nothing. */
@@ -238,8 +244,8 @@ w4a4_status w4a4_rmsnorm_f16(const uint16_t* Y, int M, int ld_y, int K, uint16_t
  * w4a4_quantize_act would on those values.  The normalised fp16 values are
  * not written out.  Arguments and limits as for w4a4_quantize_act (with X
  * replaced by Y), plus ld_y >= K and ld_y % 8 == 0. */
-w4a4_status w4a4_quantize_act_rmsnorm(const uint16_t* Y, int ld_y, const void* packed, int M, int K, int r,
-                                      void* act_ws, size_t act_ws_bytes, cudaStream_t stream);
+w4a4_status w4a4_quantize_act_rmsnorm(const uint16_t* Y, int ld_y, const void* packed, size_t packed_bytes, int M,
+                                      int K, int r, void* act_ws, size_t act_ws_bytes, cudaStream_t stream);
 
 /* ---- W4A16 linear ([INT4] "W4A16 versus W4A4": fp16 activations, the
  * weights dequantised in registers), for the decode regime.  Same packed
@@ -286,10 +292,15 @@ w4a4_status w4a4_debug_unpack_weights(const void* packed, int N, int K, int r, i
 w4a4_status w4a4_debug_unpack_act(const void* act_ws, int M, int K, int r, int8_t* codes,
                                   float* sA, float* SA, float* lora_act, cudaStream_t stream);
 /* Exact per-group partial sums P[m, n, g] (int32 [M, N, K/64]) as produced by
- * the selected GEMM kernel's tensor-core path (its epilogue dumps instead of
- * scaling). */
-w4a4_status w4a4_debug_group_partials(const void* act_ws, const void* packed, int M, int N, int K,
-                                      int r, int kernel, int32_t* P, cudaStream_t stream);
+ * the GEMM that w4a4_linear_select(..., kernel) would run on the same
+ * arguments: the same kernel instantiation and the same schedule (split-K
+ * clusters, stream-K when it is on and act_ws_bytes holds the hand-over area),
+ * with its epilogue also writing each group's integer product before scaling.
+ * No Y is written, and colscale and bias are not needed.  Argument checks as
+ * for w4a4_linear. */
+w4a4_status w4a4_debug_group_partials(const void* act_ws, size_t act_ws_bytes, const void* packed,
+                                      size_t packed_bytes, int M, int N, int K, int r, int kernel, int32_t* P,
+                                      cudaStream_t stream);
 /* Reads and clears the device status word written by bounded waits
  * (W4A4_OK or W4A4_ERR_TIMEOUT); synchronises the device. */
 w4a4_status w4a4_device_status(void);

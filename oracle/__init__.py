@@ -32,7 +32,14 @@ Status of the pins (tests/test_oracle_pins.py):
                                  -> 0, columns past K ignored, odd symmetry, unit
                                  mean square; the encoder against numpy's rounding)
   * linear_sampled /          -- pinned (equal to the full evaluators on the same
-    silu_mul_linear_sampled      rows and columns)
+    silu_mul_linear_sampled /    rows and columns)
+    linear_rows
+  * pack_weights_v1 /         -- pinned (every code, scale and LoRA value lands in
+    pack_act_v1                  exactly one place, the defined bytes tile each
+                                 section; hand-derived byte positions of the layout
+                                 statement in tests/golden/layout_v1_positions.txt;
+                                 E4M3 bytes against torch's float8_e4m3fn cast;
+                                 decoding the bytes back gives the inputs)
 """
 from __future__ import annotations
 
@@ -50,7 +57,7 @@ _lock = threading.Lock()
 _lib = None
 
 GROUP = 64
-CFLAGS = ["-O2", "-std=c11", "-fPIC", "-shared", "-ffp-contract=off", "-fno-fast-math",
+CFLAGS = ["-O3", "-std=c11", "-fPIC", "-shared", "-ffp-contract=off", "-fno-fast-math",
           "-fno-unsafe-math-optimizations", "-frounding-math"]
 
 
@@ -90,6 +97,13 @@ def _load():
         lib.oracle_quantize_weights_asym.argtypes = [P, I, I, P, P, P]
         lib.oracle_silu_mul.argtypes = [P, I, I, P]
         lib.oracle_w4a16_asym_from_codes.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, P]
+        lib.oracle_linear_rows.argtypes = [P, P, P, P, P, P, I, I, I, P, I, P, P, P, P, P, P]
+        lib.oracle_packed_offsets.argtypes = [I, I, I, P]
+        lib.oracle_act_offsets.argtypes = [I, I, I, P]
+        lib.oracle_e4m3_of_int.argtypes = [ctypes.c_int]
+        lib.oracle_e4m3_of_int.restype = ctypes.c_uint8
+        lib.oracle_pack_weights_v1.argtypes = [P, P, P, P, I, I, I, P, P]
+        lib.oracle_pack_act_v1.argtypes = [P, P, P, I, I, I, P, P]
         _lib = lib
         return lib
 
@@ -372,3 +386,72 @@ def rmsnorm_f16(Y: np.ndarray, K: int, eps: float = RMSNORM_EPS) -> np.ndarray:
     X = np.empty((M, K), dtype=np.uint16)
     _load().oracle_rmsnorm_f16(_ptr(Y), M, ld, K, float(eps), _ptr(X))
     return X
+
+
+def linear_rows(X, W, L_down, L_up, colscale, bias, rows) -> np.ndarray:
+    """fp64 Y[rows[i], :] (every output column of the listed rows) from raw inputs;
+    the weights are quantised once."""
+    X = _c(X, np.uint16); W = _c(W, np.float32)
+    M, K = X.shape
+    N = W.shape[0]
+    r = 0 if L_down is None else np.asarray(L_down).reshape(K, -1).shape[1]
+    Ld = _c(L_down, np.uint16).reshape(K, r) if r else np.zeros((K, 0), np.uint16)
+    Lup = _c(L_up, np.uint16).reshape(r, N) if r else np.zeros((0, N), np.uint16)
+    rows = _c(rows, np.int64)
+    assert rows.size == 0 or (rows.min() >= 0 and rows.max() < M)
+    qW = np.empty((N, K), np.int8); sW = np.empty((N, K // GROUP), np.uint16)
+    qa = np.empty(K, np.int8); sa = np.empty(K // GROUP, np.float32)
+    d = np.zeros(max(r, 1), np.float64)
+    Y = np.empty((rows.size, N), np.float64)
+    _load().oracle_linear_rows(_ptr(X), _ptr(W), _ptr(Ld), _ptr(Lup), _ptr(_c(colscale, np.uint16)),
+                               _ptr(_c(bias, np.uint16)), N, K, r, _ptr(rows), rows.size, _ptr(qW), _ptr(sW),
+                               _ptr(qa), _ptr(sa), _ptr(d), _ptr(Y))
+    return Y
+
+
+def packed_offsets(N: int, K: int, r: int) -> dict:
+    """Section offsets of the packed weight buffer (layout version 1)."""
+    off = np.zeros(5, np.int64)
+    _load().oracle_packed_offsets(N, K, r, _ptr(off))
+    return dict(zip(("Ld", "qW", "sW", "Lu", "total"), (int(v) for v in off)))
+
+
+def act_offsets(M: int, K: int, r: int) -> dict:
+    """Section offsets of the activation workspace (layout version 1, minimum size)."""
+    off = np.zeros(5, np.int64)
+    _load().oracle_act_offsets(M, K, r, _ptr(off))
+    return dict(zip(("qA", "sS", "La", "flags", "total"), (int(v) for v in off)))
+
+
+def e4m3_of_int(c: int) -> int:
+    """FP8 E4M3 byte of an integer in [-8, 8]."""
+    return int(_load().oracle_e4m3_of_int(int(c)))
+
+
+def pack_weights_v1(qW, sW, L_down, L_up):
+    """Packed-weight bytes (layout version 1) of codes int8 [N, K], fp16 scales
+    (uint16 bits) [N, K/64] and the LoRA factors (uint16 bits [K, r], [r, N] or
+    None).  Returns (bytes uint8 [total], defined uint8 [total]): defined marks the
+    bytes the layout specifies (section padding is not)."""
+    qW = _c(qW, np.int8); sW = _c(sW, np.uint16)
+    N, K = qW.shape
+    r = 0 if L_down is None else np.asarray(L_down).reshape(K, -1).shape[1]
+    Ld = _c(L_down, np.uint16).reshape(K, r) if r else np.zeros((K, 0), np.uint16)
+    Lup = _c(L_up, np.uint16).reshape(r, N) if r else np.zeros((0, N), np.uint16)
+    total = packed_offsets(N, K, r)["total"]
+    out = np.zeros(total, np.uint8); defined = np.zeros(total, np.uint8)
+    _load().oracle_pack_weights_v1(_ptr(qW), _ptr(sW), _ptr(Ld), _ptr(Lup), N, K, r, _ptr(out), _ptr(defined))
+    return out, defined
+
+
+def pack_act_v1(qA, sA, La_f16, r: int):
+    """Activation-workspace bytes (layout version 1) of rows m < M: codes int8
+    [M, K], fp32 scales [M, K/64], lora_act as fp16 bits uint16 [M, r] (None when
+    r == 0).  Returns (bytes, defined) of the minimum workspace size."""
+    qA = _c(qA, np.int8); sA = _c(sA, np.float32)
+    M, K = qA.shape
+    La = _c(La_f16, np.uint16).reshape(M, r) if r else np.zeros((M, 0), np.uint16)
+    total = act_offsets(M, K, r)["total"]
+    out = np.zeros(total, np.uint8); defined = np.zeros(total, np.uint8)
+    _load().oracle_pack_act_v1(_ptr(qA), _ptr(sA), _ptr(La), M, K, r, _ptr(out), _ptr(defined))
+    return out, defined

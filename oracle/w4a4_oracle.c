@@ -355,3 +355,186 @@ void oracle_silu_mul(const double* Y, int64_t M, int64_t I, double* H) {
             H[m * I + j] = g / (1.0 + exp(-g)) * u;
         }
 }
+
+/* ---- whole output rows of the layer from the raw inputs -------------------
+ * Y[rows[i], n] for every n, fp64, [nrows, N]: the weights are quantised once
+ * (qW_buf [N, K], sW_buf [N, K/64]) and each listed row of X is quantised and
+ * projected on its own, then every output element is the definition above.
+ * For parity at sizes where the whole product is too slow on one CPU thread
+ * but every output column (every output tile) must be reached.             */
+void oracle_linear_rows(const uint16_t* X, const float* W, const uint16_t* Ld, const uint16_t* Lup,
+                        const uint16_t* cs, const uint16_t* bias, int64_t N, int64_t K, int64_t r,
+                        const int64_t* rows, int64_t nrows, int8_t* qW_buf, uint16_t* sW_buf,
+                        int8_t* qa_buf, float* sa_buf, double* d_buf, double* Y) {
+    int64_t G = K / OR_GROUP;
+    oracle_quantize_weights(W, N, K, qW_buf, sW_buf);
+    for (int64_t i = 0; i < nrows; ++i) {
+        const uint16_t* x = X + rows[i] * K;
+        oracle_quantize_act(x, 1, K, qa_buf, sa_buf);
+        if (r > 0) oracle_lora_down(x, Ld, 1, K, r, d_buf);
+        for (int64_t n = 0; n < N; ++n)
+            Y[i * N + n] = output_element(qa_buf, sa_buf, qW_buf + n * K, sW_buf + n * G, d_buf, Lup, n, N, K,
+                                          r, cs[n], bias[n]);
+    }
+}
+
+/* ---- the library's buffer layouts, version 1, written from their statement
+ * These functions turn the oracle's codes and scales into the bytes that the
+ * C ABI's layout description (include/w4a4.h, layout version 1) gives for the
+ * packed weights and for the activation workspace, so that the CUDA packer
+ * and the CUDA activation kernel can be compared with them byte for byte.
+ * The layout itself is the library's choice (the pages ask for nibble and
+ * tile order suited to the kernel: "INT4 Kernel Architecture, in depth",
+ * "How the weights are stored"; the weights are repacked once at load: "W4A4
+ * CUDA Kernel for Voice Clone", 3.10).  Every byte that the layout defines is
+ * written and flagged 1 in `defined`; padding between sections stays 0 / 0.  */
+
+static size_t or_align256(size_t x) { return (x + 255) / 256 * 256; }
+
+/* Section offsets of the packed weight buffer: Ld, qW, sW, Lu, total. */
+void oracle_packed_offsets(int64_t N, int64_t K, int64_t r, int64_t* off) {
+    size_t G = (size_t)(K / OR_GROUP);
+    size_t ld = 0;
+    size_t qw = or_align256((size_t)K * (size_t)r * 2);
+    size_t sw = or_align256(qw + G * (size_t)N * 32);
+    size_t lu = or_align256(sw + G * (size_t)N * 2);
+    size_t total = or_align256(lu + (size_t)r * (size_t)N * 2);
+    off[0] = (int64_t)ld; off[1] = (int64_t)qw; off[2] = (int64_t)sw; off[3] = (int64_t)lu; off[4] = (int64_t)total;
+}
+
+/* Section offsets of the activation workspace: qA, sS, La, flags, total (the
+ * minimum size; 160 x 16 uint32 stream-K flags end it). */
+void oracle_act_offsets(int64_t M, int64_t K, int64_t r, int64_t* off) {
+    size_t MT = (size_t)((M + 127) / 128), G = (size_t)(K / OR_GROUP);
+    size_t qa = 0;
+    size_t ss = or_align256(MT * G * 2 * 128 * 32);
+    size_t la = or_align256(ss + MT * G * 128 * 8);
+    size_t fl = or_align256(la + MT * (size_t)(r / 16) * 128 * 32);
+    size_t total = or_align256(fl + 160 * 16 * 4);
+    off[0] = (int64_t)qa; off[1] = (int64_t)ss; off[2] = (int64_t)la; off[3] = (int64_t)fl; off[4] = (int64_t)total;
+}
+
+static void put_byte(uint8_t* out, uint8_t* def, size_t at, uint8_t v) {
+    out[at] = v;
+    def[at] = 1;
+}
+static void put_u16(uint8_t* out, uint8_t* def, size_t at, uint16_t v) {
+    put_byte(out, def, at, (uint8_t)(v & 0xff));
+    put_byte(out, def, at + 1, (uint8_t)(v >> 8));
+}
+
+/* Position of code k (0..63) of a group inside its 32-byte weight record:
+ * the 32-bit little-endian word at byte 8 q + 4 h holds in nibble j the code
+ * of k = 32 h + (j < 4 ? 4 q + j : 16 + 4 q + (j - 4)).  Returns the byte
+ * offset and sets *hi when the code is the byte's upper nibble.            */
+static int record_position(int k, int* hi) {
+    int h = k / 32, kk = k % 32;
+    int second = kk >= 16;            /* nibbles 4..7 of the word */
+    int rest = second ? kk - 16 : kk; /* 4 q + (j mod 4) */
+    int q = rest / 4, j = (rest % 4) + (second ? 4 : 0);
+    *hi = j % 2;
+    return 8 * q + 4 * h + j / 2;
+}
+
+/* Swizzled position of 16-byte chunk c (0/1) in 32-byte row `row` of a plane:
+ * the two halves are exchanged when bit 2 of the row index is set.         */
+static int swizzled_chunk(int64_t row, int c) { return ((row >> 2) & 1) ? 1 - c : c; }
+
+/* FP8 E4M3 byte of an integer c in [-8, 8], from the format's definition:
+ * sign bit, 4-bit exponent with bias 7, 3-bit mantissa (normal numbers
+ * 1.mmm x 2^(e-7)); 0 is 0x00.                                               */
+static uint8_t e4m3_byte(int c) {
+    if (c == 0) return 0;
+    int a = c < 0 ? -c : c, e = 0;
+    while ((a >> (e + 1)) != 0) ++e;               /* a in [2^e, 2^(e+1)) */
+    int mant = ((a << 3) >> e) - 8;                /* a / 2^e = 1 + mant / 8, exact for a <= 8 */
+    return (uint8_t)((c < 0 ? 0x80 : 0) | ((e + 7) << 3) | mant);
+}
+
+uint8_t oracle_e4m3_of_int(int c) { return e4m3_byte(c); }
+
+/* Packed weights, version 1.  qW int8 [N, K] (codes -8..7), sW fp16 bits
+ * [N, K/64], Ld fp16 bits [K, r], Lup fp16 bits [r, N]; out / def of
+ * oracle_packed_offsets()[4] bytes, zeroed by the caller.                   */
+void oracle_pack_weights_v1(const int8_t* qW, const uint16_t* sW, const uint16_t* Ld, const uint16_t* Lup,
+                            int64_t N, int64_t K, int64_t r, uint8_t* out, uint8_t* def) {
+    int64_t off[5];
+    oracle_packed_offsets(N, K, r, off);
+    int64_t G = K / OR_GROUP;
+    /* L_down in MMA fragment order: [K/16][r/8][32 lanes][2 words]; lane L,
+     * word w of (k-step s, tile t) holds the pair
+     * L_down[16 s + 2 (L % 4) + 8 w + {0, 1}][8 t + L / 4].                 */
+    for (int64_t s = 0; s < K / 16; ++s)
+        for (int64_t t = 0; t < r / 8; ++t)
+            for (int L = 0; L < 32; ++L)
+                for (int w = 0; w < 2; ++w)
+                    for (int e = 0; e < 2; ++e) {
+                        int64_t k = 16 * s + 2 * (L % 4) + 8 * w + e, j = 8 * t + L / 4;
+                        size_t at = (size_t)off[0] + ((((size_t)s * (size_t)(r / 8) + (size_t)t) * 32 + (size_t)L) * 2 +
+                                                      (size_t)w) * 4 + (size_t)e * 2;
+                        put_u16(out, def, at, Ld[k * r + j]);
+                    }
+    /* codes: [G][N][32-byte record], nibble = code + 8 */
+    for (int64_t g = 0; g < G; ++g)
+        for (int64_t n = 0; n < N; ++n) {
+            size_t rec = (size_t)off[1] + ((size_t)g * (size_t)N + (size_t)n) * 32;
+            for (int k = 0; k < OR_GROUP; ++k) {
+                int hi;
+                size_t at = rec + (size_t)record_position(k, &hi);
+                uint8_t nib = (uint8_t)(qW[n * K + g * OR_GROUP + k] + 8);
+                out[at] = hi ? (uint8_t)((out[at] & 0x0f) | (nib << 4)) : (uint8_t)((out[at] & 0xf0) | nib);
+                def[at] = 1;
+            }
+        }
+    /* scales: fp16 [G][N] */
+    for (int64_t g = 0; g < G; ++g)
+        for (int64_t n = 0; n < N; ++n)
+            put_u16(out, def, (size_t)off[2] + ((size_t)g * (size_t)N + (size_t)n) * 2, sW[n * G + g]);
+    /* L_up: [r/16][N][32 bytes], row n of plane p = L_up[16 p .. 16 p + 15][n],
+     * halves swapped by the 32-byte swizzle of row n                         */
+    for (int64_t p = 0; p < r / 16; ++p)
+        for (int64_t n = 0; n < N; ++n)
+            for (int i = 0; i < 16; ++i) {
+                size_t at = (size_t)off[3] + ((size_t)p * (size_t)N + (size_t)n) * 32 +
+                            (size_t)swizzled_chunk(n, i / 8) * 16 + (size_t)(i % 8) * 2;
+                put_u16(out, def, at, Lup[(16 * p + i) * N + n]);
+            }
+}
+
+/* Activation workspace, version 1, for rows m < M.  qA int8 [M, K], sA fp32
+ * [M, K/64], La fp16 bits [M, r] (lora_act rounded to fp16; may be NULL when
+ * r == 0); out / def of oracle_act_offsets()[4] bytes, zeroed by the caller.
+ * The stream-K flags (160 x 16 uint32) are zero after the activation step.  */
+void oracle_pack_act_v1(const int8_t* qA, const float* sA, const uint16_t* La, int64_t M, int64_t K, int64_t r,
+                        uint8_t* out, uint8_t* def) {
+    int64_t off[5];
+    oracle_act_offsets(M, K, r, off);
+    int64_t G = K / OR_GROUP;
+    for (int64_t m = 0; m < M; ++m) {
+        int64_t mt = m / 128, rr = m % 128;
+        for (int64_t g = 0; g < G; ++g) {
+            /* codes: plane (k % 64) / 32, row m % 128, byte k % 32 (swizzled) */
+            int64_t sum = 0;
+            for (int k = 0; k < OR_GROUP; ++k) {
+                int8_t c = qA[m * K + g * OR_GROUP + k];
+                sum += c;
+                size_t plane = (size_t)off[0] + (((size_t)mt * (size_t)G + (size_t)g) * 2 + (size_t)(k / 32)) * 128 * 32;
+                int b = k % 32;
+                size_t at = plane + (size_t)rr * 32 + (size_t)swizzled_chunk(rr, b / 16) * 16 + (size_t)(b % 16);
+                put_byte(out, def, at, e4m3_byte(c));
+            }
+            /* (sA, SA) fp32 pair per row and group */
+            float pair[2] = {sA[m * G + g], (float)sum};
+            size_t at = (size_t)off[1] + (((size_t)mt * (size_t)G + (size_t)g) * 128 + (size_t)rr) * 8;
+            for (int i = 0; i < 8; ++i) put_byte(out, def, at + (size_t)i, ((const uint8_t*)pair)[i]);
+        }
+        /* lora_act: [MT][r/16][128][32 bytes], column j in plane j / 16 */
+        for (int64_t j = 0; j < r; ++j) {
+            int64_t p = j / 16, jj = j % 16;
+            size_t at = (size_t)off[2] + (((size_t)mt * (size_t)(r / 16) + (size_t)p) * 128 + (size_t)rr) * 32 +
+                        (size_t)swizzled_chunk(rr, (int)(jj / 8)) * 16 + (size_t)(jj % 8) * 2;
+            put_u16(out, def, at, La[m * r + j]);
+        }
+    }
+    for (size_t i = 0; i < 160 * 16 * 4; ++i) put_byte(out, def, (size_t)off[3] + i, 0);
+}

@@ -100,9 +100,12 @@ def test_argument_checks_precede_any_launch(L):
     assert lin(64, 1024, 1024, 32, y=_vp(0x10008)) == 3
     assert lin(64, 1024, 1024, 32, wsb=100) == 4
     assert lin(64, 1024, 1024, 32, pkb=100) == 4
-    assert L.w4a4_quantize_act(A, A, 64, 100, 32, A, big, None) == 2
-    assert L.w4a4_quantize_act(_vp(0x10002), A, 64, 128, 32, A, big, None) == 3
-    assert L.w4a4_quantize_act(A, A, 64, 128, 32, A, 10, None) == 4
+    assert L.w4a4_quantize_act(A, A, big, 64, 100, 32, A, big, None) == 2
+    assert L.w4a4_quantize_act(_vp(0x10002), A, big, 64, 128, 32, A, big, None) == 3
+    assert L.w4a4_quantize_act(A, A, big, 64, 128, 32, A, 10, None) == 4
+    # the activation kernel reads L_down (K r 2 bytes) from the packed buffer
+    assert L.w4a4_quantize_act(A, A, 128 * 32 * 2 - 1, 64, 128, 32, A, big, None) == 4
+    assert L.w4a4_quantize_act(A, None, 0, 64, 128, 32, A, big, None) == 1   # r > 0 needs L_down
     assert L.w4a4_pack_weights(None, A, A, 64, 128, 32, A, big, None) == 1
     assert L.w4a4_pack_weights(A, None, A, 64, 128, 32, A, big, None) == 1  # r > 0 needs LoRA factors
     assert L.w4a4_linear_select(A, big, A, big, A, None, 64, 1024, 1024, 32, A, 7, None) == 1
@@ -113,14 +116,15 @@ def test_argument_checks_precede_any_launch(L):
     assert L.w4a4_rmsnorm_f16(A, 0, 1024, 1024, A, None) == 0     # M == 0: no-op
     assert L.w4a4_rmsnorm_f16(A, 4, 16392, 16392, A, None) == 2   # K > 16384
     big = 1 << 40
-    assert L.w4a4_quantize_act_rmsnorm(A, 1000, A, 64, 1024, 32, A, big, None) == 1  # ld_y < K
-    assert L.w4a4_quantize_act_rmsnorm(A, 1028, A, 64, 1024, 32, A, big, None) == 2  # ld_y % 8 != 0
-    assert L.w4a4_quantize_act_rmsnorm(A, 1024, A, 64, 1000, 32, A, big, None) == 2  # K % 64 != 0
-    assert L.w4a4_quantize_act_rmsnorm(A, 1024, A, 64, 1024, 24, A, big, None) == 2  # r % 16 != 0
-    assert L.w4a4_quantize_act_rmsnorm(A, 1024, None, 64, 1024, 32, A, big, None) == 1  # r > 0 needs L_down
-    assert L.w4a4_quantize_act_rmsnorm(_vp(0x10008), 1024, A, 64, 1024, 32, A, big, None) == 3
-    assert L.w4a4_quantize_act_rmsnorm(A, 1024, A, 64, 1024, 32, A, 16, None) == 4  # workspace too small
-    assert L.w4a4_quantize_act_rmsnorm(A, 1024, A, 0, 1024, 32, A, big, None) == 0  # M == 0: no-op
+    assert L.w4a4_quantize_act_rmsnorm(A, 1000, A, big, 64, 1024, 32, A, big, None) == 1  # ld_y < K
+    assert L.w4a4_quantize_act_rmsnorm(A, 1028, A, big, 64, 1024, 32, A, big, None) == 2  # ld_y % 8 != 0
+    assert L.w4a4_quantize_act_rmsnorm(A, 1024, A, big, 64, 1000, 32, A, big, None) == 2  # K % 64 != 0
+    assert L.w4a4_quantize_act_rmsnorm(A, 1024, A, big, 64, 1024, 24, A, big, None) == 2  # r % 16 != 0
+    assert L.w4a4_quantize_act_rmsnorm(A, 1024, None, big, 64, 1024, 32, A, big, None) == 1  # r > 0 needs L_down
+    assert L.w4a4_quantize_act_rmsnorm(_vp(0x10008), 1024, A, big, 64, 1024, 32, A, big, None) == 3
+    assert L.w4a4_quantize_act_rmsnorm(A, 1024, A, big, 64, 1024, 32, A, 16, None) == 4  # workspace too small
+    assert L.w4a4_quantize_act_rmsnorm(A, 1024, A, big, 0, 1024, 32, A, big, None) == 0  # M == 0: no-op
+    assert L.w4a4_quantize_act_rmsnorm(A, 1024, A, 100, 64, 1024, 32, A, big, None) == 4  # packed below L_down
 
 
 def test_argument_checks_of_the_variant_entry_points(L):
@@ -169,11 +173,40 @@ def test_argument_checks_of_the_variant_entry_points(L):
     assert L.w4a4_svd_lora_scratch_bytes(1024, 1024, 0) == 0
     assert L.w4a4_svd_lora_scratch_bytes(1024, 1000, 32) == 0
     assert L.w4a4_svd_lora_scratch_bytes(1024, 1024, 32) > 0
-    na = lambda M, N, K, r: L.w4a4_linear_noalloc(A, A, big, A, None, M, N, K, r, A, None)
+    # every check of both steps comes before any launch and before the device check: on a
+    # machine without a GPU a bad call gets its own error, never W4A4_ERR_NO_DEVICE
+    na = lambda M, N, K, r, X=A, pkb=big, cs=A, y=A, b=None: L.w4a4_linear_noalloc(
+        X, A, pkb, cs, b, M, N, K, r, y, None)
     assert na(-1, 1024, 1024, 32) == 1
     assert na(0, 1024, 1024, 32) == 0
     assert na(64, 1024, 1000, 32) == 2 and na(64, 1024, 1024, 24) == 2
+    assert na(64, 1000, 1024, 32) == 2 and na(64, 8, 1024, 32) == 2     # N % 16, N < 16
+    assert na(64, 1024, 1024, 32, X=None) == 1
+    assert na(64, 1024, 1024, 32, X=_vp(0x10004)) == 3
+    assert na(64, 1024, 1024, 32, cs=None) == 1                          # null colscale
+    assert na(64, 1024, 1024, 32, y=None) == 1
+    assert na(64, 1024, 1024, 32, cs=_vp(0x10008)) == 3
+    assert na(64, 1024, 1024, 32, b=_vp(0x10008)) == 3
+    assert na(64, 1024, 1024, 32, y=_vp(0x10002)) == 3
+    assert na(64, 1024, 1024, 32, pkb=w4.packed_weights_bytes(1024, 1024, 32) - 16) == 4  # packed too small
     assert na(8192, 1024, 4096, 32) == 4        # the workspace would not fit the library's array
+
+
+def test_noalloc_size_limit_is_the_minimum_workspace(L):
+    """The array bounds w4a4_act_workspace_min_bytes, not the size with the stream-K area:
+    the largest M that fits is accepted up to the device check, the next one refused."""
+    A = _vp(0x10000)
+    lim = w4.NOALLOC_WORKSPACE_BYTES
+    K, N, r = 4096, 1024, 32
+    M = 1
+    while w4.act_workspace_min_bytes(M + 1, K, r) <= lim:
+        M += 1
+    assert w4.act_workspace_min_bytes(M, K, r) <= lim < w4.act_workspace_min_bytes(M + 1, K, r)
+    assert w4.act_workspace_bytes(M, K, r) > lim  # (the stream-K area alone is 10 MiB)
+    call = lambda m: L.w4a4_linear_noalloc(A, A, 1 << 40, A, None, m, N, K, r, A, None)
+    assert call(M + 1) == 4
+    if not torch.cuda.is_available():
+        assert call(M) == 7   # every argument check passed; only the device is missing
 
 
 def test_stream_k_switch(L):

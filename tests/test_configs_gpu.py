@@ -1,9 +1,13 @@
 """Parity at the full sizes of the workloads, in the dispatch the benchmark uses.
 
 Whole-output comparison where the oracle finishes in seconds (single linear,
-decoder-layer linears at M = 700, the small-M sweep at K = N = 4096); sampled
-outputs for the M = 8192 prefill shapes.  Bit-exact partial sums for the qkv
-linear at M = 700.
+decoder-layer linears at M = 700, the small-M sweep at K = N = 4096); for the
+M = 8192 prefill shapes, whole output rows (every column) at the first and the
+last row of every 128-row tile, so that every output tile is compared.
+Bit-exact per-group partial sums from the kernel and schedule AUTO runs: the
+four decoder-layer linears (round-robin tiles and split-K clusters), the
+small-M sweep at M <= 32 (the tcgen05 small-M kernel), and the stream-K
+schedule on the qkv linear.
 """
 import numpy as np
 import pytest
@@ -44,15 +48,42 @@ def test_decoder_layer_linears_m700(name):
     _full_check(DECODER_LAYER_M700[name], list(DECODER_LAYER_M700).index(name))
 
 
-def test_qkv_m700_partials_bitexact():
-    s = DECODER_LAYER_M700["qkv"]
-    c = make_linear_case(seed=0, **s)
+def _partials_check(shape, seed, stream_k=False):
+    c = make_linear_case(seed=seed, **shape)
     t = to_dev(c)
     packed = pack(c, t)
     ws = quantize(c, t, packed)
-    P = w4.w4a4_debug_group_partials(ws, packed, c.M, c.N, c.K, c.r, w4.KERNEL_TC).cpu().numpy()
-    ref = oracle.Reference(c.X, c.W, None, None, c.colscale, c.bias)
-    assert np.array_equal(P, oracle.group_partials(ref.qA, ref.qW))
+    was = w4.w4a4_stream_k()
+    w4.w4a4_set_stream_k(stream_k)
+    try:
+        P = w4.w4a4_debug_group_partials(ws, packed, c.M, c.N, c.K, c.r, w4.KERNEL_AUTO)
+        dispatch = w4.w4a4_last_dispatch()
+    finally:
+        w4.w4a4_set_stream_k(was)
+    assert w4.w4a4_device_status() == 0
+    qA, _ = oracle.quantize_act(c.X)
+    qW, _ = oracle.quantize_weights(c.W)
+    assert np.array_equal(P.cpu().numpy(), oracle.group_partials(qA, qW)), dispatch
+    return dispatch
+
+
+@pytest.mark.parametrize("name", list(DECODER_LAYER_M700))
+def test_decoder_layer_partials_bitexact(name):
+    d = _partials_check(DECODER_LAYER_M700[name], list(DECODER_LAYER_M700).index(name))
+    assert "gemm_tc" in d
+    if name in ("o", "down"):
+        assert "split-K=" in d, d  # N = 1024: the cluster split-K schedule
+
+
+def test_qkv_m700_stream_k_partials_bitexact():
+    d = _partials_check(DECODER_LAYER_M700["qkv"], 0, stream_k=True)
+    assert "stream-K" in d, d
+
+
+@pytest.mark.parametrize("shape", [s for s in SMALL_M_SWEEP if s["M"] <= 32], ids=lambda s: f"M{s['M']}")
+def test_small_m_partials_bitexact(shape):
+    d = _partials_check(shape, shape["M"])
+    assert "gemm_smallm_tc" in d, d
 
 
 @pytest.mark.parametrize("shape", SMALL_M_SWEEP, ids=lambda s: f"M{s['M']}")
@@ -61,22 +92,23 @@ def test_small_m_sweep(shape):
 
 
 @pytest.mark.parametrize("name", list(PREFILL))
-def test_prefill_m8192_sampled(name):
+def test_prefill_m8192_every_tile(name):
     s = PREFILL[name]
     c = make_linear_case(seed=5, **s)
     t = to_dev(c)
     packed = pack(c, t)
     ws = quantize(c, t, packed)
     Y = run_linear(c, t, packed, ws, w4.KERNEL_AUTO)
-    rng = np.random.default_rng(1)
-    rows = np.concatenate([rng.integers(0, c.M, 1500), [0, c.M - 1, 127, 128, 8191]])
-    cols = np.concatenate([rng.integers(0, c.N, 1500), [0, c.N - 1, 127, 128, c.N - 128]])
-    y = oracle.linear_sampled(c.X, c.W, c.L_down, c.L_up, c.colscale, c.bias, rows, cols)
-    Ys = Y[torch.from_numpy(rows).cuda(), torch.from_numpy(cols).cuda()]
+    assert w4.w4a4_device_status() == 0
+    # first and last row of every 128-row tile, every column: every (M tile, N tile) pair
+    rows = np.unique(np.r_[np.arange(0, c.M, 128), np.minimum(np.arange(127, c.M + 127, 128), c.M - 1)])
+    y = oracle.linear_rows(c.X, c.W, c.L_down, c.L_up, c.colscale, c.bias, rows)
+    Ys = Y[torch.from_numpy(rows).cuda()]
     check_tol(Ys, y, name)
-    # codes of sampled rows are bit-exact at full size
+    mt_hit = np.unique(rows // 128)
+    assert mt_hit.size == -(-c.M // 128)
+    # codes and scales of those rows are bit-exact at full size
     codes, sA, _, _ = w4.w4a4_debug_unpack_act(ws, c.M, c.K, c.r)
-    sel = np.unique(rows[:64])
-    qA, sA_ref = oracle.quantize_act(c.X[sel])
-    assert np.array_equal(codes.cpu().numpy()[sel], qA)
-    assert np.array_equal(sA.cpu().numpy()[sel], sA_ref)
+    qA, sA_ref = oracle.quantize_act(c.X[rows])
+    assert np.array_equal(codes.cpu().numpy()[rows], qA)
+    assert np.array_equal(sA.cpu().numpy()[rows], sA_ref)

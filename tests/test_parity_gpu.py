@@ -15,9 +15,9 @@ from tests.helpers import check_tol, pack, quantize, run_linear, to_dev
 
 pytestmark = pytest.mark.gpu
 
-KERNELS = [w4.KERNEL_SMALLM, w4.KERNEL_TC]
-YKERNELS = KERNELS + [w4.KERNEL_SMALLM_TC]  # (the tcgen05 small-M kernel has no partials dump)
-KNAMES = {w4.KERNEL_SMALLM: "smallm", w4.KERNEL_TC: "tc", w4.KERNEL_SMALLM_TC: "smallm_tc"}
+KERNELS = [w4.KERNEL_SMALLM, w4.KERNEL_TC, w4.KERNEL_SMALLM_TC, w4.KERNEL_AUTO]  # every one has a partials dump
+YKERNELS = [w4.KERNEL_SMALLM, w4.KERNEL_TC, w4.KERNEL_SMALLM_TC]
+KNAMES = {w4.KERNEL_SMALLM: "smallm", w4.KERNEL_TC: "tc", w4.KERNEL_SMALLM_TC: "smallm_tc", w4.KERNEL_AUTO: "auto"}
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -107,13 +107,17 @@ def test_quantize_act_zero_and_outlier_rows():
 
 # ------------------------------------------------------------ exact partials
 @pytest.mark.parametrize("kernel", KERNELS, ids=lambda k: KNAMES[k])
-@pytest.mark.parametrize("M,N,K", [(1, 16, 64), (7, 48, 128), (33, 144, 192), (130, 256, 256), (300, 400, 128)])
-def test_group_partials_bitexact(kernel, M, N, K):
-    c = make_linear_case(M, K, N, 0, seed=M + N)
+@pytest.mark.parametrize("M,N,K,r", [(1, 16, 64, 0), (7, 48, 128, 16), (33, 144, 192, 32), (130, 256, 256, 0),
+                                     (300, 400, 128, 32), (64, 1024, 1024, 128), (20, 272, 4096, 32)])
+def test_group_partials_bitexact(kernel, M, N, K, r):
+    """Each kernel's dump comes from the schedule its output would use (split-K
+    clusters, ragged tiles, the 3-stage variant at rank 128, the LoRA planes)."""
+    c = make_linear_case(M, K, N, r, seed=M + N)
     t = to_dev(c)
     packed = pack(c, t)
     ws = quantize(c, t, packed)
-    P = w4.w4a4_debug_group_partials(ws, packed, M, N, K, 0, kernel).cpu().numpy()
+    P = w4.w4a4_debug_group_partials(ws, packed, M, N, K, r, kernel).cpu().numpy()
+    assert "partials dump" in w4.w4a4_last_dispatch(), w4.w4a4_last_dispatch()
     ref = oracle.Reference(c.X, c.W, None, None, c.colscale, c.bias)
     assert np.array_equal(P, oracle.group_partials(ref.qA, ref.qW))
 
@@ -302,6 +306,14 @@ def _stream_k_case(M, N, K, r):
     # a second call on the same workspace finds the flags cleared: the same bits
     Y2 = run_linear(c, t, packed, ws, w4.KERNEL_TC)
     assert torch.equal(Y, Y2)
+    # the stream-K schedule's own integer partials, on the sampled rows
+    if M * N * K <= 1 << 31:
+        P = w4.w4a4_debug_group_partials(ws, packed, M, N, K, r, w4.KERNEL_TC)
+        assert "stream-K" in w4.w4a4_last_dispatch() and "partials dump" in w4.w4a4_last_dispatch()
+        qA, _ = oracle.quantize_act(c.X[rows])
+        qW, _ = oracle.quantize_weights(c.W)
+        assert np.array_equal(P.cpu().numpy()[rows], oracle.group_partials(qA, qW))
+        assert w4.w4a4_device_status() == 0
     # without the hand-over area the GEMM takes another schedule, within tolerance too
     ws_min = ws[: w4.act_workspace_min_bytes(M, K, r)]
     Y3 = torch.full((M, N), float("nan"), dtype=torch.float16, device="cuda")

@@ -45,12 +45,12 @@ SIGNATURES = {
     "w4a4_act_workspace_min_bytes": (Z, [I, I, I]),
     "w4a4_pack_weights": (I, [P, P, P, I, I, I, P, Z, P]),
     "w4a4_pack_weight_codes": (I, [P, P, P, P, I, I, I, P, Z, P]),
-    "w4a4_quantize_act": (I, [P, P, I, I, I, P, Z, P]),
+    "w4a4_quantize_act": (I, [P, P, Z, I, I, I, P, Z, P]),
     "w4a4_linear": (I, [P, Z, P, Z, P, P, I, I, I, I, P, P]),
     "w4a4_linear_select": (I, [P, Z, P, Z, P, P, I, I, I, I, P, I, P]),
     "w4a4_linear_noalloc": (I, [P, P, Z, P, P, I, I, I, I, P, P]),
     "w4a4_rmsnorm_f16": (I, [P, I, I, I, P, P]),
-    "w4a4_quantize_act_rmsnorm": (I, [P, I, P, I, I, I, P, Z, P]),
+    "w4a4_quantize_act_rmsnorm": (I, [P, I, P, Z, I, I, I, P, Z, P]),
     "w4a16_linear": (I, [P, P, Z, P, P, I, I, I, I, P, P]),
     "w4a16_pack_weights_asym": (I, [P, P, P, I, I, I, P, Z, P]),
     "w4a4_pack_weights_gate_up": (I, [P, P, P, I, I, I, P, Z, P]),
@@ -61,7 +61,7 @@ SIGNATURES = {
     "w4a16_linear_asym": (I, [P, P, Z, P, P, I, I, I, I, P, P]),
     "w4a4_debug_unpack_weights": (I, [P, I, I, I, P, P, P, P, P]),
     "w4a4_debug_unpack_act": (I, [P, I, I, I, P, P, P, P, P]),
-    "w4a4_debug_group_partials": (I, [P, P, I, I, I, I, I, P, P]),
+    "w4a4_debug_group_partials": (I, [P, Z, P, Z, I, I, I, I, I, P, P]),
     "w4a4_device_status": (I, []),
     "w4a4_status_string": (ctypes.c_char_p, [I]),
     "w4a4_last_dispatch": (ctypes.c_char_p, []),
@@ -149,7 +149,8 @@ def w4a4_pack_weight_codes(codes, scales, L_down, L_up, packed, r: int, stream=N
 
 def w4a4_quantize_act(X, packed, act_ws, r: int, stream=None):
     M, K = X.shape
-    _check(lib().w4a4_quantize_act(_ptr(X), _ptr(packed), M, K, r, _ptr(act_ws), _nbytes(act_ws),
+    _check(lib().w4a4_quantize_act(_ptr(X), _ptr(packed), _nbytes(packed) if packed is not None else 0, M, K, r,
+                                   _ptr(act_ws), _nbytes(act_ws),
                                    _stream(stream)), "w4a4_quantize_act")
 
 
@@ -233,7 +234,8 @@ def w4a4_quantize_act_rmsnorm(Y, K: int, packed, act_ws, r: int, stream=None):
     """RMSNorm of the first K columns of each row of Y [M, ld], then the
     activation step of the next linear on the normalised values."""
     M, ld = Y.shape
-    _check(lib().w4a4_quantize_act_rmsnorm(_ptr(Y), ld, _ptr(packed), M, K, r, _ptr(act_ws), _nbytes(act_ws),
+    _check(lib().w4a4_quantize_act_rmsnorm(_ptr(Y), ld, _ptr(packed), _nbytes(packed) if packed is not None else 0,
+                                           M, K, r, _ptr(act_ws), _nbytes(act_ws),
                                            _stream(stream)), "w4a4_quantize_act_rmsnorm")
 
 
@@ -287,8 +289,8 @@ def w4a4_debug_unpack_act(act_ws, M: int, K: int, r: int, stream=None):
 
 def w4a4_debug_group_partials(act_ws, packed, M: int, N: int, K: int, r: int, kernel: int, stream=None):
     P_ = torch.empty((M, N, K // GROUP), dtype=torch.int32, device=act_ws.device)
-    _check(lib().w4a4_debug_group_partials(_ptr(act_ws), _ptr(packed), M, N, K, r, kernel, _ptr(P_),
-                                           _stream(stream)), "w4a4_debug_group_partials")
+    _check(lib().w4a4_debug_group_partials(_ptr(act_ws), _nbytes(act_ws), _ptr(packed), _nbytes(packed), M, N, K,
+                                           r, kernel, _ptr(P_), _stream(stream)), "w4a4_debug_group_partials")
     return P_
 
 

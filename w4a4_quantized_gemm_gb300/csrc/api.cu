@@ -123,6 +123,20 @@ int device_sm_count() {
     return g_sm_count[dev];
 }
 
+// The checks of w4a4_linear on everything but the activation workspace.
+w4a4_status linear_checks_no_ws(const void* packed, size_t packed_bytes, const uint16_t* colscale,
+                                const uint16_t* bias, int M, int N, int K, int r, const void* out) {
+    if (M < 0) return W4A4_ERR_INVALID_ARG;
+    w4a4_status st = check_kn(N, K, r);
+    if (st != W4A4_OK) return st;
+    if (M == 0) return W4A4_OK;
+    if (!packed || !colscale || !out) return W4A4_ERR_INVALID_ARG;
+    if (!aligned16(packed) || !aligned16(colscale) || (bias && !aligned16(bias)) || !aligned16(out))
+        return W4A4_ERR_MISALIGNED;
+    if (packed_bytes < packed_layout(N, K, r).total) return W4A4_ERR_WORKSPACE;
+    return check_device();
+}
+
 }  // namespace w4a4
 
 using namespace w4a4;
@@ -259,8 +273,11 @@ w4a4_status w4a4_pack_weight_codes(const int8_t* codes, const uint16_t* scales, 
     return pack_common(nullptr, codes, scales, L_down, L_up, N, K, r, packed, packed_bytes, stream);
 }
 
-w4a4_status w4a4_quantize_act(const uint16_t* X, const void* packed, int M, int K, int r, void* act_ws,
-                              size_t act_ws_bytes, cudaStream_t stream) {
+// Bytes of the packed buffer the activation kernel reads: its L_down section.
+static size_t ldown_bytes(int K, int r) { return size_t(K) * size_t(r) * 2; }
+
+w4a4_status w4a4_quantize_act(const uint16_t* X, const void* packed, size_t packed_bytes, int M, int K, int r,
+                              void* act_ws, size_t act_ws_bytes, cudaStream_t stream) {
     if (M < 0) return W4A4_ERR_INVALID_ARG;
     w4a4_status st = check_kn(16, K, r);
     if (st != W4A4_OK) return st;
@@ -268,13 +285,14 @@ w4a4_status w4a4_quantize_act(const uint16_t* X, const void* packed, int M, int 
     if (!X || !act_ws || (r > 0 && !packed)) return W4A4_ERR_INVALID_ARG;
     if (!aligned16(X) || !aligned16(act_ws) || (packed && !aligned16(packed))) return W4A4_ERR_MISALIGNED;
     if (act_ws_bytes < act_layout(M, K, r).total) return W4A4_ERR_WORKSPACE;
+    if (r > 0 && packed_bytes < ldown_bytes(K, r)) return W4A4_ERR_WORKSPACE;
     if ((st = check_device()) != W4A4_OK) return st;
     return launch_quantize_act(X, static_cast<const uint8_t*>(packed), M, K, r, static_cast<uint8_t*>(act_ws),
                                stream);
 }
 
-w4a4_status w4a4_quantize_act_rmsnorm(const uint16_t* Y, int ld_y, const void* packed, int M, int K, int r,
-                                      void* act_ws, size_t act_ws_bytes, cudaStream_t stream) {
+w4a4_status w4a4_quantize_act_rmsnorm(const uint16_t* Y, int ld_y, const void* packed, size_t packed_bytes, int M,
+                                      int K, int r, void* act_ws, size_t act_ws_bytes, cudaStream_t stream) {
     if (M < 0 || ld_y < K) return W4A4_ERR_INVALID_ARG;
     w4a4_status st = check_kn(16, K, r);
     if (st != W4A4_OK) return st;
@@ -283,6 +301,7 @@ w4a4_status w4a4_quantize_act_rmsnorm(const uint16_t* Y, int ld_y, const void* p
     if (!Y || !act_ws || (r > 0 && !packed)) return W4A4_ERR_INVALID_ARG;
     if (!aligned16(Y) || !aligned16(act_ws) || (packed && !aligned16(packed))) return W4A4_ERR_MISALIGNED;
     if (act_ws_bytes < act_layout(M, K, r).total) return W4A4_ERR_WORKSPACE;
+    if (r > 0 && packed_bytes < ldown_bytes(K, r)) return W4A4_ERR_WORKSPACE;
     if ((st = check_device()) != W4A4_OK) return st;
     return launch_quantize_act_rmsnorm(Y, ld_y, static_cast<const uint8_t*>(packed), M, K, r,
                                        static_cast<uint8_t*>(act_ws), stream);
@@ -290,14 +309,14 @@ w4a4_status w4a4_quantize_act_rmsnorm(const uint16_t* Y, int ld_y, const void* p
 
 // AUTO: up to the small-M threshold the tcgen05 weight-streaming kernel (it
 // beats the warp-MMA one from M = 1 on), above it the tcgen05 tiles (measured
-// crossovers on the decoder-layer and K = N = 4096 shapes).  The partials dump,
-// which the tcgen05 weight-streaming kernel does not have, takes the warp-MMA
-// kernel at small M.
-static int pick_kernel(int M, int kernel, bool dump = false) {
+// crossovers on the decoder-layer and K = N = 4096 shapes).  The partials dump
+// goes through the same choice.
+static int pick_kernel(int M, int kernel) {
     if (kernel == W4A4_KERNEL_TC || kernel == W4A4_KERNEL_SMALLM || kernel == W4A4_KERNEL_SMALLM_TC) return kernel;
     if (M > w4a4_small_m_threshold()) return W4A4_KERNEL_TC;
-    return dump ? W4A4_KERNEL_SMALLM : W4A4_KERNEL_SMALLM_TC;
+    return W4A4_KERNEL_SMALLM_TC;
 }
+
 
 static w4a4_status linear_checks(const void* act_ws, size_t act_ws_bytes, const void* packed, size_t packed_bytes,
                                  const uint16_t* colscale, const uint16_t* bias, int M, int N, int K, int r,
@@ -306,13 +325,10 @@ static w4a4_status linear_checks(const void* act_ws, size_t act_ws_bytes, const 
     w4a4_status st = check_kn(N, K, r);
     if (st != W4A4_OK) return st;
     if (M == 0) return W4A4_OK;
-    if (!act_ws || !packed || !colscale || !out) return W4A4_ERR_INVALID_ARG;
-    if (!aligned16(act_ws) || !aligned16(packed) || !aligned16(colscale) || (bias && !aligned16(bias)) ||
-        !aligned16(out))
-        return W4A4_ERR_MISALIGNED;
-    if (act_ws_bytes < act_layout(M, K, r).total || packed_bytes < packed_layout(N, K, r).total)
-        return W4A4_ERR_WORKSPACE;
-    return check_device();
+    if (!act_ws) return W4A4_ERR_INVALID_ARG;
+    if (!aligned16(act_ws)) return W4A4_ERR_MISALIGNED;
+    if (act_ws_bytes < act_layout(M, K, r).total) return W4A4_ERR_WORKSPACE;
+    return linear_checks_no_ws(packed, packed_bytes, colscale, bias, M, N, K, r, out);
 }
 
 w4a4_status w4a4_linear_select(const void* act_ws, size_t act_ws_bytes, const void* packed, size_t packed_bytes,
@@ -329,7 +345,8 @@ w4a4_status w4a4_linear_select(const void* act_ws, size_t act_ws_bytes, const vo
         const bool sk_room = AL.full > AL.total && act_ws_bytes >= AL.full;
         return launch_gemm_tc(ws, pk, colscale, bias, M, N, K, r, Y, nullptr, sk_room, 0, stream);
     }
-    if (k == W4A4_KERNEL_SMALLM_TC) return launch_gemm_smallm_tc(ws, pk, colscale, bias, M, N, K, r, Y, 0, stream);
+    if (k == W4A4_KERNEL_SMALLM_TC)
+        return launch_gemm_smallm_tc(ws, pk, colscale, bias, M, N, K, r, Y, nullptr, 0, stream);
     return launch_gemm_smallm(ws, pk, colscale, bias, M, N, K, r, Y, nullptr, stream);
 }
 
@@ -349,7 +366,8 @@ w4a4_status w4a4_linear_silu_mul(const void* act_ws, size_t act_ws_bytes, const 
     const uint8_t* ws = static_cast<const uint8_t*>(act_ws);
     const uint8_t* pk = static_cast<const uint8_t*>(packed);
     // up to the small-M threshold the tcgen05 weight-streaming kernel, above it the tiles
-    if (M <= w4a4_small_m_threshold()) return launch_gemm_smallm_tc(ws, pk, colscale, bias, M, N, K, r, H, N / 2, stream);
+    if (M <= w4a4_small_m_threshold())
+        return launch_gemm_smallm_tc(ws, pk, colscale, bias, M, N, K, r, H, nullptr, N / 2, stream);
     const ActLayout AL = act_layout(M, K, r);
     const bool sk_room = AL.full > AL.total && act_ws_bytes >= AL.full;
     return launch_gemm_tc(ws, pk, colscale, bias, M, N, K, r, H, nullptr, sk_room, N / 2, stream);
@@ -437,22 +455,31 @@ w4a4_status w4a4_debug_unpack_act(const void* act_ws, int M, int K, int r, int8_
     return sync_status(stream);
 }
 
-w4a4_status w4a4_debug_group_partials(const void* act_ws, const void* packed, int M, int N, int K, int r,
-                                      int kernel, int32_t* P, cudaStream_t stream) {
+w4a4_status w4a4_debug_group_partials(const void* act_ws, size_t act_ws_bytes, const void* packed,
+                                      size_t packed_bytes, int M, int N, int K, int r, int kernel, int32_t* P,
+                                      cudaStream_t stream) {
+    if (kernel < W4A4_KERNEL_AUTO || kernel > W4A4_KERNEL_SMALLM_TC) return W4A4_ERR_INVALID_ARG;
     if (M < 0) return W4A4_ERR_INVALID_ARG;
     w4a4_status st = check_kn(N, K, r);
     if (st != W4A4_OK) return st;
     if (M == 0) return W4A4_OK;
     if (!act_ws || !packed || !P) return W4A4_ERR_INVALID_ARG;
-    if (kernel == W4A4_KERNEL_SMALLM_TC) return W4A4_ERR_UNSUPPORTED_SHAPE;  // (no partials dump)
     if (!aligned16(act_ws) || !aligned16(packed)) return W4A4_ERR_MISALIGNED;
+    const ActLayout AL = act_layout(M, K, r);
+    if (act_ws_bytes < AL.total || packed_bytes < packed_layout(N, K, r).total) return W4A4_ERR_WORKSPACE;
     if ((st = check_device()) != W4A4_OK) return st;
     const uint8_t* ws = static_cast<const uint8_t*>(act_ws);
     const uint8_t* pk = static_cast<const uint8_t*>(packed);
-    if (pick_kernel(M, kernel, true) == W4A4_KERNEL_TC)
-        st = launch_gemm_tc(ws, pk, nullptr, nullptr, M, N, K, r, nullptr, P, false, 0, stream);
-    else
+    // the kernel and schedule w4a4_linear_select would run, with the dump on and no output
+    const int k = pick_kernel(M, kernel);
+    if (k == W4A4_KERNEL_TC) {
+        const bool sk_room = AL.full > AL.total && act_ws_bytes >= AL.full;
+        st = launch_gemm_tc(ws, pk, nullptr, nullptr, M, N, K, r, nullptr, P, sk_room, 0, stream);
+    } else if (k == W4A4_KERNEL_SMALLM_TC) {
+        st = launch_gemm_smallm_tc(ws, pk, nullptr, nullptr, M, N, K, r, nullptr, P, 0, stream);
+    } else {
         st = launch_gemm_smallm(ws, pk, nullptr, nullptr, M, N, K, r, nullptr, P, stream);
+    }
     if (st != W4A4_OK) return st;
     if ((st = sync_status(stream)) != W4A4_OK) return st;
     return device_status_words();

@@ -77,10 +77,13 @@ __host__ __device__ inline TcPlan tc_plan(int tokn, int r, int ks) {
     return p;
 }
 
-template <int TOKN>
+// DUMP: the debug variant, which also writes every group's exact integer product to
+// P and stores no Y (colscale and bias are not read).
+template <int TOKN, bool DUMP>
 __global__ void __launch_bounds__(kThreads, TOKN >= 64 ? 1 : 2) gemm_smallm_tc_kernel(
     const uint8_t* __restrict__ ws, const uint8_t* __restrict__ packed, const uint16_t* __restrict__ colscale,
-    const uint16_t* __restrict__ bias, int M, int N, int K, int r, uint16_t* __restrict__ Y, int KS, int silu_I) {
+    const uint16_t* __restrict__ bias, int M, int N, int K, int r, uint16_t* __restrict__ Y,
+    int32_t* __restrict__ P, int KS, int silu_I) {
     constexpr int BLK = TOKN / 4;  // 4-token blocks
     constexpr int kS = stages_for(TOKN);
     extern __shared__ uint8_t smdyn[];
@@ -331,6 +334,14 @@ __global__ void __launch_bounds__(kThreads, TOKN >= 64 ? 1 : 2) gemm_smallm_tc_k
                 for (int c = 0; c < TOKN / 32; ++c) tmem_ld32_at(tl + uint32_t(s * TOKN + 32 * c), d + 32 * c);
             }
             tmem_wait_ld();
+            if (DUMP && nbase + row < N) {
+                // partials dump: P = D - 8 SA, exact in fp32 (|D| < 2^13), SA read from the workspace
+                const int g = g_begin + e, n = nbase + row;
+                const float* ssg = reinterpret_cast<const float*>(ws + AL.sS + ((size_t)(mt * G + g) * kTileM + rt0) * 8);
+#pragma unroll
+                for (int c = 0; c < TOKN; ++c)
+                    if (tok0 + c < M) P[((size_t)(tok0 + c) * N + n) * G + g] = int32_t(d[c] - 8.f * ssg[2 * c + 1]);
+            }
             const float sw = __half2float(__ushort_as_half(
                 reinterpret_cast<const uint16_t*>(smraw + PLN.sw + s * (kRows * 2))[row]));
             const uint64_t sw2 = f2_pack(sw, sw);
@@ -411,7 +422,8 @@ __global__ void __launch_bounds__(kThreads, TOKN >= 64 ? 1 : 2) gemm_smallm_tc_k
     // ---- affine of the owned token blocks, staged as rows [token][128 + 8] over the weight planes
     uint16_t* ys = reinterpret_cast<uint16_t*>(smraw + PLN.wexp);
     constexpr int LDY = kRows + 8;
-    if (is_epi && !*abort && silu_I > 0) {
+    constexpr bool store = !DUMP;
+    if (is_epi && !*abort && store && silu_I > 0) {
         // fused gate|up weights (gate_up_row order): lanes 0..15 of the warp on lane quarter q
         // hold the gates of outputs j = 64 t + 16 q + lane, lanes 16..31 the matching ups;
         // h = silu(g) u is staged as [token][64 + 8] at column 16 q + lane
@@ -435,7 +447,7 @@ __global__ void __launch_bounds__(kThreads, TOKN >= 64 ? 1 : 2) gemm_smallm_tc_k
                         __half_as_ushort(__float2half_rn(__fdividef(y, 1.0f + __expf(-y)) * u));
             }
         }
-    } else if (is_epi && !*abort) {
+    } else if (is_epi && !*abort && store) {
         const int n = nbase + row;
         const float cs = n < N ? __half2float(__ushort_as_half(colscale[n])) : 0.f;
         const float bs = (bias && n < N) ? __half2float(__ushort_as_half(bias[n])) : 0.f;
@@ -450,7 +462,7 @@ __global__ void __launch_bounds__(kThreads, TOKN >= 64 ? 1 : 2) gemm_smallm_tc_k
         }
     }
     __syncthreads();
-    if (!*abort && silu_I > 0) {
+    if (!*abort && store && silu_I > 0) {
         for (int c = threadIdx.x; c < TOKN * (kRows / 16); c += kThreads) {
             const int t = c / (kRows / 16), ch = c % (kRows / 16);
             const int m = tok0 + t, j = (nbase >> 1) + ch * 8;
@@ -459,7 +471,7 @@ __global__ void __launch_bounds__(kThreads, TOKN >= 64 ? 1 : 2) gemm_smallm_tc_k
                 *reinterpret_cast<uint4*>(Y + (size_t)m * silu_I + j) =
                     *reinterpret_cast<const uint4*>(&ys[t * LDY + ch * 8]);
         }
-    } else if (!*abort) {
+    } else if (!*abort && store) {
         for (int c = threadIdx.x; c < TOKN * (kRows / 8); c += kThreads) {
             const int t = c / (kRows / 8), ch = c % (kRows / 8);
             const int m = tok0 + t, n = nbase + ch * 8;
@@ -482,9 +494,9 @@ int smtc_split(int M, int N, int K, int TOKN) {
     return ks;
 }
 
-template <int TOKN>
+template <int TOKN, bool DUMP>
 w4a4_status launch_t(const uint8_t* ws, const uint8_t* packed, const uint16_t* cs, const uint16_t* bias, int M,
-                     int N, int K, int r, uint16_t* Y, int silu_I, cudaStream_t s) {
+                     int N, int K, int r, uint16_t* Y, int32_t* P, int silu_I, cudaStream_t s) {
     const int KS = smtc_split(M, N, K, TOKN);
     const TcPlan plan = tc_plan(TOKN, r, KS);
     const int smem_max = int(tc_plan(TOKN, W4A4_MAX_RANK, kMaxKS).total) + 1024;
@@ -492,7 +504,7 @@ w4a4_status launch_t(const uint8_t* ws, const uint8_t* packed, const uint16_t* c
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev >= 0 && dev < 64 && !attr_done[dev]) {
-        if (cudaFuncSetAttribute(gemm_smallm_tc_kernel<TOKN>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_max) !=
+        if (cudaFuncSetAttribute(gemm_smallm_tc_kernel<TOKN, DUMP>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_max) !=
             cudaSuccess)
             return W4A4_ERR_CUDA;
         attr_done[dev] = 1;
@@ -510,13 +522,13 @@ w4a4_status launch_t(const uint8_t* ws, const uint8_t* packed, const uint16_t* c
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = plan.total + 1024;  // (the dynamic region is aligned up to 1024 bytes inside)
     cfg.stream = s;
-    if (cudaLaunchKernelEx(&cfg, gemm_smallm_tc_kernel<TOKN>, ws, packed, cs, bias, M, N, K, r, Y, KS, silu_I) !=
+    if (cudaLaunchKernelEx(&cfg, gemm_smallm_tc_kernel<TOKN, DUMP>, ws, packed, cs, bias, M, N, K, r, Y, P, KS, silu_I) !=
         cudaSuccess) {
         cudaGetLastError();
         return W4A4_ERR_CUDA;
     }
-    set_dispatch("gemm_smallm_tc tcgen05.f8f6f4 swap-AB N=%d split-K=%d (cluster) grid=%ux%u%s", TOKN, KS, grid.x,
-                 grid.y, silu_I ? " silu(gate)*up" : "");
+    set_dispatch("gemm_smallm_tc tcgen05.f8f6f4 swap-AB N=%d split-K=%d (cluster) grid=%ux%u%s%s", TOKN, KS, grid.x,
+                 grid.y, silu_I ? " silu(gate)*up" : "", DUMP ? " (partials dump)" : "");
     return launch_status();
 }
 
@@ -537,11 +549,16 @@ w4a4_status smtc_read_and_clear_status() {
 }
 
 w4a4_status launch_gemm_smallm_tc(const uint8_t* ws, const uint8_t* packed, const uint16_t* colscale,
-                                  const uint16_t* bias, int M, int N, int K, int r, uint16_t* Y, int silu_I,
-                                  cudaStream_t s) {
-    if (M <= 16) return launch_t<16>(ws, packed, colscale, bias, M, N, K, r, Y, silu_I, s);
-    if (M <= 32) return launch_t<32>(ws, packed, colscale, bias, M, N, K, r, Y, silu_I, s);
-    return launch_t<64>(ws, packed, colscale, bias, M, N, K, r, Y, silu_I, s);
+                                  const uint16_t* bias, int M, int N, int K, int r, uint16_t* Y, int32_t* P_dump,
+                                  int silu_I, cudaStream_t s) {
+    if (P_dump) {  // the same token block and split, in the DUMP variant
+        if (M <= 16) return launch_t<16, true>(ws, packed, nullptr, nullptr, M, N, K, r, nullptr, P_dump, 0, s);
+        if (M <= 32) return launch_t<32, true>(ws, packed, nullptr, nullptr, M, N, K, r, nullptr, P_dump, 0, s);
+        return launch_t<64, true>(ws, packed, nullptr, nullptr, M, N, K, r, nullptr, P_dump, 0, s);
+    }
+    if (M <= 16) return launch_t<16, false>(ws, packed, colscale, bias, M, N, K, r, Y, nullptr, silu_I, s);
+    if (M <= 32) return launch_t<32, false>(ws, packed, colscale, bias, M, N, K, r, Y, nullptr, silu_I, s);
+    return launch_t<64, false>(ws, packed, colscale, bias, M, N, K, r, Y, nullptr, silu_I, s);
 }
 
 }  // namespace w4a4

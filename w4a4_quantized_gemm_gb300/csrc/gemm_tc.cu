@@ -116,7 +116,9 @@ static_assert(smem_map(4, 2, false).total <= 227 * 1024, "4 stages must fit at r
 static_assert(smem_map(3, 8, false).total <= 227 * 1024, "3 stages must fit at rank 128");
 static_assert(smem_map(3, 2, true).total <= 227 * 1024, "3 stages + the reduction buffer must fit at rank 32");
 
-template <int S, bool DUMP, bool SPLIT, bool SK>
+// DUMP: the debug variant of a schedule, which also writes every group's exact
+// integer product to P and stores no Y (colscale and bias are not read).
+template <int S, bool SPLIT, bool SK, bool DUMP>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_tc_kernel(const uint8_t* __restrict__ ws, const uint8_t* __restrict__ packed,
                    const uint16_t* __restrict__ colscale, const uint16_t* __restrict__ bias, int M, int N, int K,
@@ -135,7 +137,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (!SPLIT) KS = 1;
     const int cid = int(blockIdx.x) / KS, ncl = int(gridDim.x) / KS;
     const int j0 = kr * J / KS, j1 = (kr + 1) * J / KS;
-    const int RPB = DUMP ? 0 : r / 16;  // LoRA operand planes held in shared memory
+    const int RPB = r / 16;  // LoRA operand planes held in shared memory
+    constexpr bool has_y = !DUMP;
     const ActLayout AL = act_layout(M, K, r);
     const PackedLayout PL = packed_layout(N, K, r);
     const int MT = AL.MT, NT = (N + BN - 1) / BN;
@@ -222,7 +225,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     // overlaps the previous kernel; so does warming L2 with the weight records of
     // the first jobs (a prefetch only fills the cache, the copies proper come
     // after the wait).  Global data the previous kernel may write is read after it.
-    if (warp == WARP_PRODUCER_W && lane == 0 && u_begin < u_end && !DUMP) {
+    if (warp == WARP_PRODUCER_W && lane == 0 && u_begin < u_end) {
         int t0, a0, b0;
         seg_at(u_begin, t0, a0, b0);
         const int n0 = (t0 / MT) * BN, rows = min(BN, N - n0);
@@ -451,7 +454,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             // [cs gate 0..15 | cs up | bias gate | bias up]
             uint8_t* const cbw = gbase + mp.CB + uint32_t(warp) * kCB;
             // (only warps that store this segment: not a stream-K hand-over, not a split-K sender)
-            const bool stores = !DUMP && !(SK && a > 0) && !(SPLIT && ((warp >> 2) % KS) != kr);
+            const bool stores = has_y && !(SK && a > 0) && !(SPLIT && ((warp >> 2) % KS) != kr);
             if (stores && lane < 8) {
                 const uint16_t* src = nullptr;
                 if (silu_I > 0) {
@@ -519,18 +522,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         __syncwarp();
                         if (lane == 0) mbar_arrive(tempty(bf));
                     }
-                    if constexpr (DUMP) {
-                        if (m < M) {
+                    if (DUMP && m < M) {
+                        // partials dump: P = D - 8 SA, exact in fp32 (|D| < 2^13)
 #pragma unroll
-                            for (int c = 0; c < 16; ++c) {
-                                const int n = n0 + c0 + ch * 16 + c;
-                                if (n < N) {
-                                    P[(size_t(m) * N + n) * G + g0] = int32_t(d0[c] - 8.f * sv0.y);
-                                    if (two) P[(size_t(m) * N + n) * G + g0 + 1] = int32_t(d1[c] - 8.f * sv1.y);
-                                }
+                        for (int c = 0; c < 16; ++c) {
+                            const int n = n0 + c0 + ch * 16 + c;
+                            if (n < N) {
+                                P[(size_t(m) * N + n) * G + g0] = int32_t(d0[c] - 8.f * sv0.y);
+                                if (two) P[(size_t(m) * N + n) * G + g0 + 1] = int32_t(d1[c] - 8.f * sv1.y);
                             }
                         }
-                    } else {
+                    }
+                    {
                         // t = sA D - 8 SA sA, acc += sW t, two columns per instruction
                         uint64_t* a = acc + ch * 8;
                         const ulonglong2* w0 = reinterpret_cast<const ulonglong2*>(sc0 + (c0 + ch * 16) * 4);
@@ -604,7 +607,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     if (!ok) break;
                 }
             }
-            if constexpr (SPLIT && !DUMP) {
+            if constexpr (SPLIT) {
                 const int sl = warp >> 2, owner = sl % KS;
                 if (owner != kr) {
                     // send this slice's sums to its owner once it has consumed the previous ones
@@ -661,7 +664,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
             }
             ++tc;
-            if constexpr (!DUMP) {
+            if constexpr (has_y) {
                 cp_async_wait<0>();  // this warp's colscale / bias chunks
                 __syncwarp();
                 if (m < M && silu_I > 0) {
@@ -735,26 +738,26 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 }
 
 // Registers per thread the kernel was compiled for (cached per instantiation).
-template <int S, bool DUMP, bool SPLIT, bool SK>
+template <int S, bool SPLIT, bool SK, bool DUMP>
 int launch_regs() {
     static int regs = -1;
     if (regs < 0) {
         cudaFuncAttributes fa{};
-        if (cudaFuncGetAttributes(&fa, gemm_tc_kernel<S, DUMP, SPLIT, SK>) != cudaSuccess) return 0;
+        if (cudaFuncGetAttributes(&fa, gemm_tc_kernel<S, SPLIT, SK, DUMP>) != cudaSuccess) return 0;
         regs = fa.numRegs;
     }
     return regs;
 }
 
-template <int S, bool DUMP, bool SPLIT, bool SK = false>
+template <int S, bool SPLIT, bool SK, bool DUMP>
 w4a4_status launch_impl(const uint8_t* ws, const uint8_t* packed, const uint16_t* cs, const uint16_t* bias, int M,
                         int N, int K, int r, uint16_t* Y, int32_t* P, int KS, cudaStream_t s, int sk_ctas = 0,
                         int silu_I = 0) {
-    auto kern = gemm_tc_kernel<S, DUMP, SPLIT, SK>;
+    auto kern = gemm_tc_kernel<S, SPLIT, SK, DUMP>;
     static int attr_done[64] = {0};
     int dev = 0;
     cudaGetDevice(&dev);
-    const int rp = DUMP ? 0 : r / 16;
+    const int rp = r / 16;
     const uint32_t smem_max = smem_map(S, S == 4 ? 2 : (SPLIT ? 2 : 8), SPLIT).total;
     if (dev >= 0 && dev < 64 && !attr_done[dev]) {
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem_max)) != cudaSuccess)
@@ -762,7 +765,7 @@ w4a4_status launch_impl(const uint8_t* ws, const uint8_t* packed, const uint16_t
         attr_done[dev] = 1;
     }
     // the setmaxnreg split needs the launch-time register pool to cover it
-    if (launch_regs<S, DUMP, SPLIT, SK>() * NUM_THREADS <
+    if (launch_regs<S, SPLIT, SK, DUMP>() * NUM_THREADS <
         NUM_EPI_WARPS * 32 * EPI_REGS + (NUM_THREADS - NUM_EPI_WARPS * 32) * OTHER_REGS)
         return W4A4_ERR_CUDA;
     const int MT = (M + BM - 1) / BM, NT = (N + BN - 1) / BN;
@@ -827,7 +830,7 @@ static int resident_clusters(int ks) {
     cudaGetDevice(&dev);
     if (dev < 0 || dev >= 64) return 0;
     if (cache[dev][ks] == 0) {
-        auto kern = gemm_tc_kernel<3, false, true, false>;
+        auto kern = gemm_tc_kernel<3, true, false, false>;
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  int(smem_map(3, 2, true).total)) != cudaSuccess) {
             cudaGetLastError();
@@ -889,22 +892,31 @@ static TcSchedule tc_schedule(int M, int N, int K, int r, bool sk_room) {
     return best_s;
 }
 
-w4a4_status launch_gemm_tc(const uint8_t* ws, const uint8_t* packed, const uint16_t* colscale, const uint16_t* bias,
-                           int M, int N, int K, int r, uint16_t* Y, int32_t* P_dump, bool sk_room, int silu_I,
-                           cudaStream_t s) {
-    if (P_dump) return launch_impl<4, true, false>(ws, packed, colscale, bias, M, N, K, r, Y, P_dump, 1, s);
+template <bool DUMP>
+static w4a4_status dispatch_tc(const uint8_t* ws, const uint8_t* packed, const uint16_t* colscale,
+                               const uint16_t* bias, int M, int N, int K, int r, uint16_t* Y, int32_t* P, bool sk_room,
+                               int silu_I, cudaStream_t s) {
     const TcSchedule sc = tc_schedule(M, N, K, r, sk_room && tc_stream_k_enabled());
     if (sc.sk_ctas > 0) {
         if (r > 32)
-            return launch_impl<3, false, false, true>(ws, packed, colscale, bias, M, N, K, r, Y, nullptr, 1, s,
-                                                      sc.sk_ctas, silu_I);
-        return launch_impl<4, false, false, true>(ws, packed, colscale, bias, M, N, K, r, Y, nullptr, 1, s,
-                                                  sc.sk_ctas, silu_I);
+            return launch_impl<3, false, true, DUMP>(ws, packed, colscale, bias, M, N, K, r, Y, P, 1, s, sc.sk_ctas,
+                                                     silu_I);
+        return launch_impl<4, false, true, DUMP>(ws, packed, colscale, bias, M, N, K, r, Y, P, 1, s, sc.sk_ctas,
+                                                 silu_I);
     }
     if (sc.ks > 1)
-        return launch_impl<3, false, true>(ws, packed, colscale, bias, M, N, K, r, Y, nullptr, sc.ks, s, 0, silu_I);
-    if (r > 32) return launch_impl<3, false, false>(ws, packed, colscale, bias, M, N, K, r, Y, nullptr, 1, s, 0, silu_I);
-    return launch_impl<4, false, false>(ws, packed, colscale, bias, M, N, K, r, Y, nullptr, 1, s, 0, silu_I);
+        return launch_impl<3, true, false, DUMP>(ws, packed, colscale, bias, M, N, K, r, Y, P, sc.ks, s, 0, silu_I);
+    if (r > 32)
+        return launch_impl<3, false, false, DUMP>(ws, packed, colscale, bias, M, N, K, r, Y, P, 1, s, 0, silu_I);
+    return launch_impl<4, false, false, DUMP>(ws, packed, colscale, bias, M, N, K, r, Y, P, 1, s, 0, silu_I);
+}
+
+w4a4_status launch_gemm_tc(const uint8_t* ws, const uint8_t* packed, const uint16_t* colscale, const uint16_t* bias,
+                           int M, int N, int K, int r, uint16_t* Y, int32_t* P_dump, bool sk_room, int silu_I,
+                           cudaStream_t s) {
+    // the partials dump runs the schedule the call would run, in its DUMP variant
+    if (P_dump) return dispatch_tc<true>(ws, packed, colscale, bias, M, N, K, r, nullptr, P_dump, sk_room, 0, s);
+    return dispatch_tc<false>(ws, packed, colscale, bias, M, N, K, r, Y, nullptr, sk_room, silu_I, s);
 }
 
 w4a4_status tc_read_and_clear_status() {

@@ -5,6 +5,11 @@
 
 namespace w4a4 {
 
+// api.cu: every check of w4a4_linear except those on the activation workspace
+// (null and misaligned pointers, shapes, packed_bytes, the current device)
+w4a4_status linear_checks_no_ws(const void* packed, size_t packed_bytes, const uint16_t* colscale,
+                                const uint16_t* bias, int M, int N, int K, int r, const void* out);
+
 // pack.cu
 // silu_I > 0: W is a fused gate|up weight (I gate rows, then I up rows), packed in gate_up_row order
 void launch_pack_weights(const float* W, const int8_t* codes, const uint16_t* scales, int N, int K, int r,
@@ -30,6 +35,8 @@ w4a4_status launch_gemm_smallm(const uint8_t* ws, const uint8_t* packed, const u
 // gemm_tc.cu (tcgen05 + TMEM)
 // sk_room: the workspace holds the stream-K hand-over area (act_layout().full bytes)
 // silu_I > 0: weights packed by w4a4_pack_weights_gate_up; Y receives silu(gate) * up [M, silu_I]
+// P_dump != nullptr: the same schedule also writes the exact per-group partials
+// (Y == nullptr: no output; colscale and bias are then not read)
 w4a4_status launch_gemm_tc(const uint8_t* ws, const uint8_t* packed, const uint16_t* colscale,
                            const uint16_t* bias, int M, int N, int K, int r, uint16_t* Y, int32_t* P_dump,
                            bool sk_room, int silu_I, cudaStream_t s);
@@ -37,9 +44,11 @@ w4a4_status launch_gemm_tc(const uint8_t* ws, const uint8_t* packed, const uint1
 // rmsnorm.cu (stack glue between linears)
 w4a4_status launch_quantize_act_rmsnorm(const uint16_t* Y, int ld_y, const uint8_t* packed, int M, int K, int r,
                                         uint8_t* ws, cudaStream_t s);
+// gemm_smallm_tc.cu (tcgen05, weights as the 128-row operand); P_dump != nullptr also
+// writes the exact per-group partials (Y == nullptr: no output)
 w4a4_status launch_gemm_smallm_tc(const uint8_t* ws, const uint8_t* packed, const uint16_t* colscale,
-                                  const uint16_t* bias, int M, int N, int K, int r, uint16_t* Y, int silu_I,
-                                  cudaStream_t s);
+                                  const uint16_t* bias, int M, int N, int K, int r, uint16_t* Y, int32_t* P_dump,
+                                  int silu_I, cudaStream_t s);
 w4a4_status launch_gemm_w4a16(const uint16_t* X, const uint8_t* packed, const uint16_t* colscale,
                               const uint16_t* bias, int M, int N, int K, int r, uint16_t* Y, bool asym,
                               cudaStream_t s);

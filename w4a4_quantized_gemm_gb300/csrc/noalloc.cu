@@ -51,16 +51,25 @@ w4a4_status noalloc_workspace(void** out) {
 extern "C" w4a4_status w4a4_linear_noalloc(const uint16_t* X, const void* packed, size_t packed_bytes,
                                            const uint16_t* colscale, const uint16_t* bias, int M, int N, int K,
                                            int r, uint16_t* Y, cudaStream_t stream) {
+    // Every argument is checked before anything is launched or looked up: the
+    // shapes, the pointers of both steps, packed_bytes, and the array's size.
+    // The device is checked last, so that a bad call is refused the same way
+    // with or without a usable GPU.
     if (M < 0 || N < 0 || K < 0 || r < 0) return W4A4_ERR_INVALID_ARG;
-    if (M == 0) return W4A4_OK;
-    if (K < w4a4::kGroup || K % w4a4::kGroup != 0 || r % 16 != 0 || r > W4A4_MAX_RANK)
+    if (K < w4a4::kGroup || K % w4a4::kGroup != 0 || N < 16 || N % 16 != 0 || r % 16 != 0 || r > W4A4_MAX_RANK)
         return W4A4_ERR_UNSUPPORTED_SHAPE;
-    // refuse before touching the device when the workspace would not fit the array
+    if (M == 0) return W4A4_OK;
+    if (!X) return W4A4_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(X) & 15u) != 0) return W4A4_ERR_MISALIGNED;
+    // the workspace every call needs must fit the array; the GEMM's optional
+    // stream-K hand-over area never does, so that schedule is not used here
     if (w4a4::act_layout(M, K, r).total > size_t(W4A4_NOALLOC_WORKSPACE_BYTES)) return W4A4_ERR_WORKSPACE;
-    void* ws = nullptr;
-    w4a4_status st = w4a4::noalloc_workspace(&ws);
+    w4a4_status st = w4a4::linear_checks_no_ws(packed, packed_bytes, colscale, bias, M, N, K, r, Y);
     if (st != W4A4_OK) return st;
-    st = w4a4_quantize_act(X, packed, M, K, r, ws, W4A4_NOALLOC_WORKSPACE_BYTES, stream);
+    void* ws = nullptr;
+    st = w4a4::noalloc_workspace(&ws);
+    if (st != W4A4_OK) return st;
+    st = w4a4_quantize_act(X, packed, packed_bytes, M, K, r, ws, W4A4_NOALLOC_WORKSPACE_BYTES, stream);
     if (st != W4A4_OK) return st;
     return w4a4_linear(ws, W4A4_NOALLOC_WORKSPACE_BYTES, packed, packed_bytes, colscale, bias, M, N, K, r, Y, stream);
 }
