@@ -55,7 +55,8 @@
  *   offset 0                 qA  [MT][G][2][128][32 bytes]: the code of row m,
  *       column k is stored as an FP8 E4M3 byte (every integer in [-8, 7] is exact
  *       in E4M3) in plane (k % 64) / 32, row m % 128, byte k % 32, with the two
- *       16-byte halves of a row swapped when ((m % 128) >> 2) & 1.
+ *       16-byte halves of a row swapped when ((m % 128) >> 2) & 1.  Code 0 is
+ *       E4M3 zero of either sign (0x00, or 0x80 where x / sA rounds to -0).
  *   next align256            sS  [MT][G][128][2] fp32: (sA, SA) per row and group,
  *       SA = sum of the group's 64 codes (exact integer in fp32).
  *   next align256            La  [MT][r/16][128][32 bytes]: lora_act = X L_down
