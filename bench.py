@@ -279,7 +279,23 @@ def kernel_source_hash(name: str) -> str:
 # of one step, from the ncu capture summarised under profiles/, keyed by the
 # hash of the kernel source they were taken on: once the kernel changes, the
 # counters no longer describe it and traffic is reported as null.
-NCU_TRAFFIC = {}
+NCU_TRAFFIC = {
+    # the four decoder-layer GEMM launches (qkv, o, gate_up, down) at M = 700, one launch each,
+    # read from HBM (24 input replicas cycled): 3,495,168 + 3,071,232 + 4,770,560 + 4,513,024 bytes;
+    # Y stays in L2 within a launch, so the write counter is near zero (profiles/gemm_tc_traffic_decoder_layer_m700.md)
+    (WORKLOAD, "9ed4a39ebb1a337f"): {
+        "bytes_per_pass": 15849984,
+        "per_linear": {"qkv": 3495168, "o": 3071232, "gate_up": 4770560, "down": 4513024},
+        "source": "ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum, one launch per linear "
+                  "(profiles/gemm_tc_traffic_decoder_layer_m700.md)"},
+    # the M = 8192, 4096 -> 14336 GEMM launch: 76.22 MB read + 199.38 MB written
+    # (profiles/gemm_tc_prefill_m8192.md); the 14336 -> 4096 launch was not captured
+    (PREFILL_WORKLOAD, "9ed4a39ebb1a337f"): {
+        "bytes_per_pass": None,
+        "per_linear": {"gate_up_style": 275602432, "down_style": None},
+        "source": "ncu --section SpeedOfLight --metrics dram__bytes_read.sum,dram__bytes_write.sum, one launch "
+                  "(profiles/gemm_tc_prefill_m8192.md)"},
+}
 
 
 def ncu_traffic(workload: str, source: str = "gemm_tc.cu"):
@@ -1192,8 +1208,12 @@ def run_prefill(args, rank, world, local_rank):
         bf16, peak_src = 1900.0, "fallback"
     fp8_peak = 2.0 * bf16  # FP8 tensor kind: measured bf16 burst x nominal fp8/bf16 ratio (4.5/2.25)
     achieved = ops / gemm_s / 1e12
+    traffic = ncu_traffic(PREFILL_WORKLOAD)
     roofline = {"bound": "tensor", "achieved": achieved, "peak": fp8_peak, "unit": "TFLOP/s",
-                "frac": achieved / fp8_peak, "traffic": None,
+                "frac": achieved / fp8_peak, "traffic": traffic["bytes_per_pass"] if traffic else None,
+                "traffic_per_linear": traffic["per_linear"] if traffic else None,
+                "traffic_source": traffic["source"] if traffic else
+                "null: no ncu capture of the current gemm_tc.cu source",
                 "kernel": "w4a4_linear (GEMM + LoRA up + affine), 2 launches per step",
                 "peak_source": f"{peak_src} bf16 burst x 2 (fp8 kind)",
                 "per_linear_gemm_us": g_us, "per_linear_quantize_us": q_us,

@@ -92,3 +92,17 @@ def test_workload_totals():
     assert bench.stack_ops() == 640_968_294_400
     assert metrics.weight_bytes(4096, 4096) == 8_912_896     # the small-M sweep's packed weights + scales
     assert metrics.weight_bytes(1024, 1024) == 524_288 + 32_768
+
+
+def test_bench_traffic_is_tied_to_the_kernel_source_it_was_measured_on():
+    """roofline.traffic comes from an ncu capture of a given gemm_tc.cu: reported only while the
+    source still hashes to the key it was recorded under, null once the kernel changes."""
+    import bench
+    key = bench.kernel_source_hash("gemm_tc.cu")
+    rec = bench.NCU_TRAFFIC.get((bench.WORKLOAD, key))
+    got = bench.ncu_traffic(bench.WORKLOAD)
+    if rec is None:
+        assert got is None
+    else:
+        assert got["bytes_per_pass"] == sum(rec["per_linear"].values())
+    assert bench.ncu_traffic("no such workload") is None
