@@ -6,8 +6,9 @@
 // dimension is N; "W4A4 CUDA Kernel for Voice Clone", 3.7: exact per-group
 // products, scaled per group, LoRA up into the same accumulator).
 //
-// Per group g, D[n, m] = sum_k E4M3(cW[n,k] + 8) * E4M3(cA[m,k]) exactly in its
-// own tensor-memory buffer, and the epilogue adds sW[n,g] (sA[m,g] D - 8 SA sA)
+// Per group g, D[n, m] = 2^-9 sum_k (cW[n,k] + 8) * cA[m,k] exactly in its own
+// tensor-memory buffer (the weight bytes are the offset codes themselves, which
+// E4M3 reads as u * 2^-9), and the epilogue adds sW[n,g] (2^9 sA[m,g] D - 8 SA sA)
 // to fp32 sums held in registers (one thread per weight row, one column pair
 // per two tokens).
 //
@@ -251,19 +252,23 @@ __global__ void __launch_bounds__(kThreads, TOKN >= 64 ? 1 : 2) gemm_smallm_tc_k
             const uint8_t* wr = smraw + PLN.wraw + s * (kRows * 32) + row * 32;
             const uint4 w01 = *reinterpret_cast<const uint4*>(wr);
             const uint4 w23 = *reinterpret_cast<const uint4*>(wr + 16);
-            const uint4 p0c0 = make_uint4(expand4(w01.x), expand4(w01.z), expand4(w23.x), expand4(w23.z));
-            const uint4 p0c1 =
-                make_uint4(expand4(w01.x >> 16), expand4(w01.z >> 16), expand4(w23.x >> 16), expand4(w23.z >> 16));
-            const uint4 p1c0 = make_uint4(expand4(w01.y), expand4(w01.w), expand4(w23.y), expand4(w23.w));
-            const uint4 p1c1 =
-                make_uint4(expand4(w01.y >> 16), expand4(w01.w >> 16), expand4(w23.y >> 16), expand4(w23.w >> 16));
+            uint4 p0c0, p0c1, p1c0, p1c1;  // (the bytes are the codes + 8, as E4M3 values scaled by 2^-9)
+            expand8(w01.x, p0c0.x, p0c1.x);
+            expand8(w01.z, p0c0.y, p0c1.y);
+            expand8(w23.x, p0c0.z, p0c1.z);
+            expand8(w23.z, p0c0.w, p0c1.w);
+            expand8(w01.y, p1c0.x, p1c1.x);
+            expand8(w01.w, p1c0.y, p1c1.y);
+            expand8(w23.y, p1c0.z, p1c1.z);
+            expand8(w23.w, p1c0.w, p1c1.w);
             uint8_t* ep = smraw + PLN.wexp + s * (2 * kRows * 32);
             *reinterpret_cast<uint4*>(ep + row * 32 + swz32(row, 0) * 16) = p0c0;
             *reinterpret_cast<uint4*>(ep + row * 32 + swz32(row, 1) * 16) = p0c1;
             *reinterpret_cast<uint4*>(ep + kRows * 32 + row * 32 + swz32(row, 0) * 16) = p1c0;
             *reinterpret_cast<uint4*>(ep + kRows * 32 + row * 32 + swz32(row, 1) * 16) = p1c1;
             if (warp == 0) {
-                // (sA, SA) pairs -> sA[] and cc[] = -8 SA sA, in place (the pairs' 8 bytes per token)
+                // (sA, SA) pairs -> 2^9 sA[] (undoing the 2^-9 of the expanded weights) and
+                // cc[] = -8 SA sA, in place (the pairs' 8 bytes per token)
                 float* sp = reinterpret_cast<float*>(smraw + PLN.sa + s * (TOKN * 8));
                 float v0[TOKN / 32 + 1], v1[TOKN / 32 + 1];
 #pragma unroll
@@ -279,7 +284,7 @@ __global__ void __launch_bounds__(kThreads, TOKN >= 64 ? 1 : 2) gemm_smallm_tc_k
                 for (int u = 0; u * 32 < TOKN; ++u) {
                     const int m = u * 32 + lane;
                     if (m < TOKN) {
-                        sp[m] = v0[u];
+                        sp[m] = v0[u] * kExpand8Scale;
                         sp[TOKN + m] = (-8.f * v1[u]) * v0[u];
                     }
                 }
@@ -335,12 +340,12 @@ __global__ void __launch_bounds__(kThreads, TOKN >= 64 ? 1 : 2) gemm_smallm_tc_k
             }
             tmem_wait_ld();
             if (DUMP && nbase + row < N) {
-                // partials dump: P = D - 8 SA, exact in fp32 (|D| < 2^13), SA read from the workspace
+                // partials dump: P = 2^9 D - 8 SA, exact in fp32 (|2^9 D| < 2^13), SA read from the workspace
                 const int g = g_begin + e, n = nbase + row;
                 const float* ssg = reinterpret_cast<const float*>(ws + AL.sS + ((size_t)(mt * G + g) * kTileM + rt0) * 8);
 #pragma unroll
                 for (int c = 0; c < TOKN; ++c)
-                    if (tok0 + c < M) P[((size_t)(tok0 + c) * N + n) * G + g] = int32_t(d[c] - 8.f * ssg[2 * c + 1]);
+                    if (tok0 + c < M) P[((size_t)(tok0 + c) * N + n) * G + g] = int32_t(d[c] * kExpand8Scale - 8.f * ssg[2 * c + 1]);
             }
             const float sw = __half2float(__ushort_as_half(
                 reinterpret_cast<const uint16_t*>(smraw + PLN.sw + s * (kRows * 2))[row]));

@@ -3,8 +3,9 @@
 //
 // Computes, per 128 x 128 output tile ("W4A4 CUDA Kernel for Voice Clone",
 // 3.7; "High-Performance Kernel Design for W4A4 ... on Blackwell", 1):
-//   acc = lora_act . L_up  +  sum_g sW[n,g] (sA[m,g] D_g - 8 SA[m,g] sA[m,g])
-//   D_g = sum_{k in g} E4M3(cA) * E4M3(cW + 8)     (exact, one group per TMEM buffer)
+//   acc = lora_act . L_up  +  sum_g sW[n,g] (2^9 sA[m,g] D_g - 8 SA[m,g] sA[m,g])
+//   D_g = 2^-9 sum_{k in g} cA * (cW + 8)     (exact, one group per TMEM buffer: the
+//         weight bytes are the offset codes, which E4M3 reads as u * 2^-9)
 //   Y   = fp16(colscale * acc + bias)
 //
 // Structure (the warp-specialised persistent design of the Blackwell W4A4
@@ -19,7 +20,7 @@
 //   warp 21     MMA issuer (one thread) + tensor-memory owner: per tile a
 //               kind::f16 LoRA-up chain, per group two kind::f8f6f4 MMAs
 //               (M = N = 128, K = 32) into its 128 columns of a job buffer;
-//   warps 16-19 nibble -> E4M3 expansion of the weight tiles into the
+//   warps 16-19 nibble -> byte expansion of the weight tiles into the
 //               32-byte-swizzled B operand (32 rows each, one warp per SM
 //               sub-partition) and the groups' scales as fp32 into a scale
 //               ring that outlives the stage;
@@ -405,12 +406,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     const uint4 w01 = *reinterpret_cast<const uint4*>(wp + row * 32);
                     const uint4 w23 = *reinterpret_cast<const uint4*>(wp + row * 32 + 16);
                     // words: w01 = (q0h0, q0h1, q1h0, q1h1), w23 = (q2h0, q2h1, q3h0, q3h1)
-                    const uint4 p0c0 = make_uint4(expand4(w01.x), expand4(w01.z), expand4(w23.x), expand4(w23.z));
-                    const uint4 p0c1 = make_uint4(expand4(w01.x >> 16), expand4(w01.z >> 16), expand4(w23.x >> 16),
-                                                  expand4(w23.z >> 16));
-                    const uint4 p1c0 = make_uint4(expand4(w01.y), expand4(w01.w), expand4(w23.y), expand4(w23.w));
-                    const uint4 p1c1 = make_uint4(expand4(w01.y >> 16), expand4(w01.w >> 16), expand4(w23.y >> 16),
-                                                  expand4(w23.w >> 16));
+                    // (the bytes are the codes + 8, as E4M3 values scaled by 2^-9)
+                    uint4 p0c0, p0c1, p1c0, p1c1;
+                    expand8(w01.x, p0c0.x, p0c1.x);
+                    expand8(w01.z, p0c0.y, p0c1.y);
+                    expand8(w23.x, p0c0.z, p0c1.z);
+                    expand8(w23.z, p0c0.w, p0c1.w);
+                    expand8(w01.y, p1c0.x, p1c1.x);
+                    expand8(w01.w, p1c0.y, p1c1.y);
+                    expand8(w23.y, p1c0.z, p1c1.z);
+                    expand8(w23.w, p1c0.w, p1c1.w);
                     uint8_t* bp = sp + ST_B + uint32_t(j) * kB;
                     *reinterpret_cast<uint4*>(bp + row * 32 + swz32(row, 0) * 16) = p0c0;
                     *reinterpret_cast<uint4*>(bp + row * 32 + swz32(row, 1) * 16) = p0c1;
@@ -508,8 +513,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 const float2 sv0 = reinterpret_cast<const float2*>(sc0 + BN * 4)[row];
                 const float2 sv1 = two ? reinterpret_cast<const float2*>(sc1 + BN * 4)[row] : make_float2(0.f, 0.f);
                 const float cm0 = (-8.f * sv0.y) * sv0.x, cm1 = (-8.f * sv1.y) * sv1.x;
-                const uint64_t sa0 = f2_pack(sv0.x, sv0.x), cc0 = f2_pack(cm0, cm0);
-                const uint64_t sa1 = f2_pack(sv1.x, sv1.x), cc1 = f2_pack(cm1, cm1);
+                // (2^9 sA: the tensor memory holds 2^-9 D)
+                const float sx0 = sv0.x * kExpand8Scale, sx1 = sv1.x * kExpand8Scale;
+                const uint64_t sa0 = f2_pack(sx0, sx0), cc0 = f2_pack(cm0, cm0);
+                const uint64_t sa1 = f2_pack(sx1, sx1), cc1 = f2_pack(cm1, cm1);
                 const uint32_t tb = tl + bf * (GPJ * BN);
 #pragma unroll
                 for (int ch = 0; ch < EPI_COLS / 16; ++ch) {
@@ -523,13 +530,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         if (lane == 0) mbar_arrive(tempty(bf));
                     }
                     if (DUMP && m < M) {
-                        // partials dump: P = D - 8 SA, exact in fp32 (|D| < 2^13)
+                        // partials dump: P = 2^9 (2^-9 D) - 8 SA, exact in fp32 (|D| < 2^13)
 #pragma unroll
                         for (int c = 0; c < 16; ++c) {
                             const int n = n0 + c0 + ch * 16 + c;
                             if (n < N) {
-                                P[(size_t(m) * N + n) * G + g0] = int32_t(d0[c] - 8.f * sv0.y);
-                                if (two) P[(size_t(m) * N + n) * G + g0 + 1] = int32_t(d1[c] - 8.f * sv1.y);
+                                P[(size_t(m) * N + n) * G + g0] = int32_t(d0[c] * kExpand8Scale - 8.f * sv0.y);
+                                if (two)
+                                    P[(size_t(m) * N + n) * G + g0 + 1] = int32_t(d1[c] * kExpand8Scale - 8.f * sv1.y);
                             }
                         }
                     }
