@@ -104,8 +104,9 @@ typedef enum {
     W4A4_KERNEL_AUTO = 0,   /* by M: M <= threshold the tcgen05 small-M kernel, else tensor-core tiles */
     W4A4_KERNEL_TC = 1,     /* tcgen05 (TMEM accumulators, bulk-copy pipeline) */
     W4A4_KERNEL_SMALLM = 2, /* weight-streaming kernel (warp-level MMA, split over K) */
-    W4A4_KERNEL_SMALLM_TC = 3 /* weight-streaming kernel on tcgen05 (weights as the 128-row operand, tokens
-                                 as N; split over K) */
+    W4A4_KERNEL_SMALLM_TC = 3, /* weight-streaming kernel on tcgen05 (weights as the 128-row operand, tokens
+                                  as N; split over K) */
+    W4A4_KERNEL_FUSED = 4   /* w4a4_forward only: the whole linear in one kernel for small M (see there) */
 } w4a4_kernel;
 
 /* ---- size queries (bytes of caller-allocated device buffers) ---- */
@@ -150,6 +151,31 @@ w4a4_status w4a4_quantize_act(const uint16_t* X, const void* packed, size_t pack
 w4a4_status w4a4_linear(const void* act_ws, size_t act_ws_bytes, const void* packed,
                         size_t packed_bytes, const uint16_t* colscale, const uint16_t* bias,
                         int M, int N, int K, int r, uint16_t* Y, cudaStream_t stream);
+
+/* ---- the whole linear from fp16 activations ([VC] 3.6-3.7; [INT4] "One token
+ * versus a thousand": at decode sizes the call is a weight stream)
+ * Y = the layer of w4a4_linear applied to X fp16 [M, K] row-major, i.e.
+ * w4a4_quantize_act followed by w4a4_linear, in one call.  Arguments as for
+ * those two; X must be 16-byte aligned.
+ * kernel W4A4_KERNEL_AUTO: for 1 <= M <= w4a4_small_m_threshold() and the shapes
+ * the fused kernel takes (r <= 32; K / 64 groups split over at most 8 CTAs with
+ * at most 8 groups each, i.e. K <= 4096 at N >= 1024; the shared-memory plan
+ * fits two CTAs per SM), one kernel does everything: quantisation and LoRA down
+ * of X (the same codes, scales and SA as w4a4_quantize_act, bit for bit; the
+ * LoRA-down sums in another fixed order, so lora_act may differ in its last
+ * fp16 bit), the exact per-group products, LoRA up and the affine.  act_ws may
+ * then be NULL; if it is given (act_ws_bytes >= w4a4_act_workspace_min_bytes),
+ * the kernel also writes the codes, (sA, SA) pairs and lora_act there in the
+ * workspace layout.  Otherwise the call runs w4a4_quantize_act and w4a4_linear
+ * on act_ws, which is then required.
+ * kernel W4A4_KERNEL_FUSED: the fused kernel, W4A4_ERR_UNSUPPORTED_SHAPE where
+ * it does not apply.  TC, SMALLM, SMALLM_TC: the two-call path with that GEMM.
+ * Every argument check runs before anything is launched. */
+w4a4_status w4a4_forward(const uint16_t* X, const void* packed, size_t packed_bytes, const uint16_t* colscale,
+                         const uint16_t* bias, int M, int N, int K, int r, uint16_t* Y, void* act_ws,
+                         size_t act_ws_bytes, int kernel, cudaStream_t stream);
+/* Whether w4a4_forward's AUTO choice for these sizes is the fused kernel. */
+int w4a4_forward_is_fused(int M, int N, int K, int r);
 
 /* ---- fused gate|up linear with the SiLU(gate) * up epilogue ([VC] 1: the
  * decoder MLP's SiLU(gate_proj x) * up_proj x feeding down_proj).
@@ -302,6 +328,13 @@ w4a4_status w4a4_debug_unpack_act(const void* act_ws, int M, int K, int r, int8_
 w4a4_status w4a4_debug_group_partials(const void* act_ws, size_t act_ws_bytes, const void* packed,
                                       size_t packed_bytes, int M, int N, int K, int r, int kernel, int32_t* P,
                                       cudaStream_t stream);
+/* The same partials from the fused kernel of w4a4_forward (kernel
+ * W4A4_KERNEL_FUSED) on X fp16 [M, K]: no Y is written.  act_ws may be NULL or
+ * receive the codes, scales and lora_act as in w4a4_forward.
+ * W4A4_ERR_UNSUPPORTED_SHAPE where the fused kernel does not apply. */
+w4a4_status w4a4_debug_forward_partials(const uint16_t* X, const void* packed, size_t packed_bytes, int M, int N,
+                                        int K, int r, void* act_ws, size_t act_ws_bytes, int32_t* P,
+                                        cudaStream_t stream);
 /* Reads and clears the device status word written by bounded waits
  * (W4A4_OK or W4A4_ERR_TIMEOUT); synchronises the device. */
 w4a4_status w4a4_device_status(void);

@@ -20,7 +20,7 @@ LIB_PATH = os.path.join(_HERE, "libw4a4.so")
 
 W4A4_OK = 0
 W4A4_ERR_TIMEOUT = 6
-KERNEL_AUTO, KERNEL_TC, KERNEL_SMALLM, KERNEL_SMALLM_TC = 0, 1, 2, 3
+KERNEL_AUTO, KERNEL_TC, KERNEL_SMALLM, KERNEL_SMALLM_TC, KERNEL_FUSED = 0, 1, 2, 3, 4
 GROUP = 64
 
 _STATUS = {
@@ -49,6 +49,9 @@ SIGNATURES = {
     "w4a4_linear": (I, [P, Z, P, Z, P, P, I, I, I, I, P, P]),
     "w4a4_linear_select": (I, [P, Z, P, Z, P, P, I, I, I, I, P, I, P]),
     "w4a4_linear_noalloc": (I, [P, P, Z, P, P, I, I, I, I, P, P]),
+    "w4a4_forward": (I, [P, P, Z, P, P, I, I, I, I, P, P, Z, I, P]),
+    "w4a4_forward_is_fused": (I, [I, I, I, I]),
+    "w4a4_debug_forward_partials": (I, [P, P, Z, I, I, I, I, P, Z, P, P]),
     "w4a4_rmsnorm_f16": (I, [P, I, I, I, P, P]),
     "w4a4_quantize_act_rmsnorm": (I, [P, I, P, Z, I, I, I, P, Z, P]),
     "w4a16_linear": (I, [P, P, Z, P, P, I, I, I, I, P, P]),
@@ -245,6 +248,20 @@ def w4a4_linear(act_ws, packed, colscale, bias, Y, K: int, r: int, kernel: int =
                                     _ptr(bias), M, N, K, r, _ptr(Y), kernel, _stream(stream)), "w4a4_linear")
 
 
+def w4a4_forward(X, packed, colscale, bias, Y, r: int, act_ws=None, kernel: int = KERNEL_AUTO, stream=None):
+    """The whole layer from fp16 X [M, K] into Y [M, N] in one call (one fused
+    kernel at small M, else quantise + GEMM on act_ws; see include/w4a4.h)."""
+    M, K = X.shape
+    N = Y.shape[1]
+    _check(lib().w4a4_forward(_ptr(X), _ptr(packed), _nbytes(packed), _ptr(colscale), _ptr(bias), M, N, K, r,
+                              _ptr(Y), _ptr(act_ws), 0 if act_ws is None else _nbytes(act_ws), kernel,
+                              _stream(stream)), "w4a4_forward")
+
+
+def w4a4_forward_is_fused(M: int, N: int, K: int, r: int) -> bool:
+    return bool(lib().w4a4_forward_is_fused(M, N, K, r))
+
+
 def w4a4_linear_noalloc(X, packed, colscale, bias, Y, r: int, stream=None):
     """Quantise X and run the layer with the library's built-in workspace (no
     allocation anywhere; see include/w4a4.h for its size limit and sharing rules)."""
@@ -291,6 +308,15 @@ def w4a4_debug_group_partials(act_ws, packed, M: int, N: int, K: int, r: int, ke
     P_ = torch.empty((M, N, K // GROUP), dtype=torch.int32, device=act_ws.device)
     _check(lib().w4a4_debug_group_partials(_ptr(act_ws), _nbytes(act_ws), _ptr(packed), _nbytes(packed), M, N, K,
                                            r, kernel, _ptr(P_), _stream(stream)), "w4a4_debug_group_partials")
+    return P_
+
+
+def w4a4_debug_forward_partials(X, packed, N: int, r: int, act_ws=None, stream=None):
+    M, K = X.shape
+    P_ = torch.empty((M, N, K // GROUP), dtype=torch.int32, device=X.device)
+    _check(lib().w4a4_debug_forward_partials(_ptr(X), _ptr(packed), _nbytes(packed), M, N, K, r, _ptr(act_ws),
+                                             0 if act_ws is None else _nbytes(act_ws), _ptr(P_), _stream(stream)),
+           "w4a4_debug_forward_partials")
     return P_
 
 

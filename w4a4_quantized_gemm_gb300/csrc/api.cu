@@ -69,7 +69,8 @@ w4a4_status device_status_words() {
     const w4a4_status c = w4a16_read_and_clear_status();
     const w4a4_status d = smtc_read_and_clear_status();
     const w4a4_status e = q_read_and_clear_status();
-    return a != W4A4_OK ? a : b != W4A4_OK ? b : c != W4A4_OK ? c : d != W4A4_OK ? d : e;
+    const w4a4_status f = fused_read_and_clear_status();
+    return a != W4A4_OK ? a : b != W4A4_OK ? b : c != W4A4_OK ? c : d != W4A4_OK ? d : e != W4A4_OK ? e : f;
 }
 }  // namespace
 
@@ -357,6 +358,33 @@ w4a4_status w4a4_linear(const void* act_ws, size_t act_ws_bytes, const void* pac
                               W4A4_KERNEL_AUTO, stream);
 }
 
+int w4a4_forward_is_fused(int M, int N, int K, int r) {
+    if (check_kn(N, K, r) != W4A4_OK || M < 1 || M > w4a4_small_m_threshold()) return 0;
+    return fused_eligible(M, N, K, r) ? 1 : 0;
+}
+
+w4a4_status w4a4_forward(const uint16_t* X, const void* packed, size_t packed_bytes, const uint16_t* colscale,
+                         const uint16_t* bias, int M, int N, int K, int r, uint16_t* Y, void* act_ws,
+                         size_t act_ws_bytes, int kernel, cudaStream_t stream) {
+    if (kernel < W4A4_KERNEL_AUTO || kernel > W4A4_KERNEL_FUSED) return W4A4_ERR_INVALID_ARG;
+    w4a4_status st = linear_checks_no_ws(packed, packed_bytes, colscale, bias, M, N, K, r, Y);
+    if (st != W4A4_OK || M == 0) return st;
+    if (!X) return W4A4_ERR_INVALID_ARG;
+    if (!aligned16(X) || (act_ws && !aligned16(act_ws))) return W4A4_ERR_MISALIGNED;
+    const bool fused = kernel == W4A4_KERNEL_FUSED || (kernel == W4A4_KERNEL_AUTO && w4a4_forward_is_fused(M, N, K, r));
+    if (fused && !fused_eligible(M, N, K, r)) return W4A4_ERR_UNSUPPORTED_SHAPE;
+    const size_t need = act_layout(M, K, r).total;
+    if (act_ws ? act_ws_bytes < need : !fused) return act_ws ? W4A4_ERR_WORKSPACE : W4A4_ERR_INVALID_ARG;
+    const uint8_t* pk = static_cast<const uint8_t*>(packed);
+    if (fused)
+        return launch_linear_fused(X, pk, colscale, bias, M, N, K, r, Y, static_cast<uint8_t*>(act_ws), nullptr,
+                                   stream);
+    st = launch_quantize_act(X, pk, M, K, r, static_cast<uint8_t*>(act_ws), stream);
+    if (st != W4A4_OK) return st;
+    return w4a4_linear_select(act_ws, act_ws_bytes, packed, packed_bytes, colscale, bias, M, N, K, r, Y, kernel,
+                              stream);
+}
+
 w4a4_status w4a4_linear_silu_mul(const void* act_ws, size_t act_ws_bytes, const void* packed, size_t packed_bytes,
                                  const uint16_t* colscale, const uint16_t* bias, int M, int N, int K, int r,
                                  uint16_t* H, cudaStream_t stream) {
@@ -480,6 +508,26 @@ w4a4_status w4a4_debug_group_partials(const void* act_ws, size_t act_ws_bytes, c
     } else {
         st = launch_gemm_smallm(ws, pk, nullptr, nullptr, M, N, K, r, nullptr, P, stream);
     }
+    if (st != W4A4_OK) return st;
+    if ((st = sync_status(stream)) != W4A4_OK) return st;
+    return device_status_words();
+}
+
+w4a4_status w4a4_debug_forward_partials(const uint16_t* X, const void* packed, size_t packed_bytes, int M, int N,
+                                        int K, int r, void* act_ws, size_t act_ws_bytes, int32_t* P,
+                                        cudaStream_t stream) {
+    if (M < 0) return W4A4_ERR_INVALID_ARG;
+    w4a4_status st = check_kn(N, K, r);
+    if (st != W4A4_OK) return st;
+    if (M == 0) return W4A4_OK;
+    if (!X || !packed || !P) return W4A4_ERR_INVALID_ARG;
+    if (!aligned16(X) || !aligned16(packed) || (act_ws && !aligned16(act_ws))) return W4A4_ERR_MISALIGNED;
+    if (packed_bytes < packed_layout(N, K, r).total) return W4A4_ERR_WORKSPACE;
+    if (act_ws && act_ws_bytes < act_layout(M, K, r).total) return W4A4_ERR_WORKSPACE;
+    if (!fused_eligible(M, N, K, r)) return W4A4_ERR_UNSUPPORTED_SHAPE;
+    if ((st = check_device()) != W4A4_OK) return st;
+    st = launch_linear_fused(X, static_cast<const uint8_t*>(packed), nullptr, nullptr, M, N, K, r, nullptr,
+                             static_cast<uint8_t*>(act_ws), P, stream);
     if (st != W4A4_OK) return st;
     if ((st = sync_status(stream)) != W4A4_OK) return st;
     return device_status_words();

@@ -182,6 +182,14 @@ __device__ __forceinline__ void pdl_launch_dependents() {
     asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
 }
 
+// Read-only 16-byte load that does not allocate in L1 (data read once).
+__device__ __forceinline__ uint4 ldg_stream_v4(const void* p) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];\n"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
 __device__ __forceinline__ uint4 ldg_nc_v4(const void* p) {
     uint4 v;
     asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];\n"
@@ -207,4 +215,5 @@ w4a4_status smallm_read_and_clear_status();  // bounded-wait status of the small
 w4a4_status w4a16_read_and_clear_status();   // bounded-wait status of the W4A16 kernel
 w4a4_status smtc_read_and_clear_status();    // bounded-wait status of the tcgen05 small-M kernel
 w4a4_status q_read_and_clear_status();       // bounded-wait status of the activation kernel
+w4a4_status fused_read_and_clear_status();   // bounded-wait status of the fused small-M linear
 }  // namespace w4a4

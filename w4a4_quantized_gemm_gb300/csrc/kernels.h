@@ -49,6 +49,13 @@ w4a4_status launch_quantize_act_rmsnorm(const uint16_t* Y, int ld_y, const uint8
 w4a4_status launch_gemm_smallm_tc(const uint8_t* ws, const uint8_t* packed, const uint16_t* colscale,
                                   const uint16_t* bias, int M, int N, int K, int r, uint16_t* Y, int32_t* P_dump,
                                   int silu_I, cudaStream_t s);
+// linear_fused.cu (the whole linear for small M in one kernel): ws may be nullptr
+// (else it also receives codes, (sA, SA) and lora_act); P_dump != nullptr: the
+// partials variant (no Y)
+bool fused_eligible(int M, int N, int K, int r);
+w4a4_status launch_linear_fused(const uint16_t* X, const uint8_t* packed, const uint16_t* colscale,
+                                const uint16_t* bias, int M, int N, int K, int r, uint16_t* Y, uint8_t* ws,
+                                int32_t* P_dump, cudaStream_t s);
 w4a4_status launch_gemm_w4a16(const uint16_t* X, const uint8_t* packed, const uint16_t* colscale,
                               const uint16_t* bias, int M, int N, int K, int r, uint16_t* Y, bool asym,
                               cudaStream_t s);

@@ -37,6 +37,7 @@
 
 #include "kernels.h"
 #include "norm.cuh"
+#include "quant.cuh"
 #include "tc_ptx.cuh"
 
 namespace cg = cooperative_groups;
@@ -65,13 +66,6 @@ __device__ __forceinline__ void ldmatrix_x4(uint32_t (&r)[4], const void* p) {
     asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
                  : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
                  : "r"(smem_u32(p)));
-}
-
-// Two integer-valued floats -> E4M3 bytes: lo -> bits 0-7, hi -> bits 8-15.
-__device__ __forceinline__ uint32_t cvt_e4m3x2(float lo, float hi) {
-    uint16_t r;
-    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;\n" : "=h"(r) : "f"(hi), "f"(lo));
-    return r;
 }
 
 template <int R, bool NORM>  // LoRA rank, multiple of 16 (0 = no LoRA branch); RMSNorm on the way in
@@ -210,58 +204,9 @@ __global__ void __launch_bounds__(kWarps * 32) quantize_act_kernel(const uint16_
 #pragma unroll
             for (int i = 0; i < 4; ++i) xv[i] = scale_to_f16(xv[i], inv, inva, invb);
         }
-        float x[32];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const uint32_t w[4] = {xv[i].x, xv[i].y, xv[i].z, xv[i].w};
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[j]));
-                x[8 * i + 2 * j] = f.x;
-                x[8 * i + 2 * j + 1] = f.y;
-            }
-        }
-        float amax = 0.f;
-#pragma unroll
-        for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(x[i]));
-        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-        // scale = max(absmax / 7, 1e-10) with IEEE division.  Codes lie in [-7, 7]:
-        // |x| <= absmax and scale >= fl(absmax / 7), so |x / scale| <= 7 (1 + 2^-23)
-        // rounds to at most 7 and the clamp to [-8, 7] never acts.
-        const float s = fmaxf(__fdiv_rn(amax, 7.0f), 1e-10f);
-        const float inv = __frcp_rn(s);
-        // codes on the reciprocal path, branch-free; elements within 2^-18 of a
-        // rounding boundary are flagged and redone with the IEEE quotient below
-        // (x[] is overwritten by the codes; the fp16 inputs stay in xv)
-        float* c = x;
-        bool near_tie = false;
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-            const float y = x[i] * inv;
-            c[i] = rintf(y);
-            near_tie |= fabsf(y - c[i]) >= 0.5f - 3.814697265625e-06f;
-        }
-        // (rare) rint(fl(x / s)) with the IEEE quotient where the reciprocal product
-        // lies within 2^-18 of k + 1/2: y is within 2^-20 of x/s and fl(x/s) within
-        // 2^-21, so everywhere else both round alike
-        if (__any_sync(0xffffffffu, near_tie)) {
-#pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                const uint32_t wv = (&xv[i >> 3].x)[(i & 7) >> 1];
-                const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&wv));
-                const float xi = (i & 1) ? f.y : f.x;
-                const float y = xi * inv;
-                if (fabsf(y - c[i]) >= 0.5f - 3.814697265625e-06f) c[i] = rintf(__fdiv_rn(xi, s));
-            }
-        }
-        float csum = 0.f;
+        float s, csum;
         uint32_t packed[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            csum += (c[4 * i] + c[4 * i + 1]) + (c[4 * i + 2] + c[4 * i + 3]);
-            packed[i] = cvt_e4m3x2(c[4 * i], c[4 * i + 1]) | (cvt_e4m3x2(c[4 * i + 2], c[4 * i + 3]) << 16);
-        }
-        csum += __shfl_xor_sync(0xffffffffu, csum, 1);
+        quantize_half_group(xv, s, csum, packed);
         uint8_t* plane = ws + AL.qA + ((size_t)(mt * G + g) * 2 + qhalf) * (kTileM * 32);
         *reinterpret_cast<uint4*>(plane + rr * 32 + swz32(rr, 0) * 16) =
             make_uint4(packed[0], packed[1], packed[2], packed[3]);

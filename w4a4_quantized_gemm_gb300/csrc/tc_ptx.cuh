@@ -140,6 +140,20 @@ __device__ __forceinline__ void st_async_v4(uint32_t remote_addr, float4 v, uint
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
     asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(nthreads) : "memory");
 }
+// Named barrier over `nthreads` threads with an OR reduction: every
+// participant receives the OR of the participants' predicates, so all of them
+// take the same branch after it.
+__device__ __forceinline__ bool named_bar_red_or(uint32_t id, uint32_t nthreads, bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n.reg .pred p, q;\nsetp.ne.u32 p, %1, 0;\n"
+        "bar.red.or.pred q, %2, %3, p;\n"
+        "selp.u32 %0, 1, 0, q;\n}\n"
+        : "=r"(r)
+        : "r"(uint32_t(pred)), "r"(id), "r"(nthreads)
+        : "memory");
+    return r != 0;
+}
 // Arrive on an mbarrier of another CTA of the cluster, releasing this thread's
 // earlier (distributed) shared-memory writes to whoever acquires the phase.
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t remote_bar) {
@@ -226,6 +240,12 @@ __device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;\n" ::"l"(src), "r"(bytes) : "memory");
 }
 
+// 16-byte cp.async global -> shared that copies src_bytes (16 or 0) and fills
+// the rest of the 16 bytes with zeros.
+__device__ __forceinline__ void cp_async16_zfill(uint32_t dst, const void* src, uint32_t src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
+
 // 1-D bulk copy global -> shared, completing `bytes` of transaction count on bar.
 __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
     asm volatile(
@@ -279,6 +299,16 @@ __device__ __forceinline__ void mma_f8(uint32_t d_tmem, uint64_t a, uint64_t b, 
         "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
         "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
         "l"(a), "l"(b), "r"(idesc), "r"(acc)
+        : "memory");
+}
+// Same, with the A operand in tensor memory (lane = row, byte k % 4 of column
+// k / 4 for the 32 k of one MMA) and B in shared memory.
+__device__ __forceinline__ void mma_f8_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc,
+                                              uint32_t acc) {
+    asm volatile(
+        "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc)
         : "memory");
 }
 __device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
@@ -357,6 +387,15 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const float (&v)[16]) 
         "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
         "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
         "r"(__float_as_uint(v[15]))
+        : "memory");
+}
+// 16 raw 32-bit words -> 32 lanes x 16 consecutive columns.
+__device__ __forceinline__ void tmem_st16_b32(uint32_t taddr, const uint32_t (&v)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+        "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};\n" ::"r"(taddr),
+        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]),
+        "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
         : "memory");
 }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory"); }
