@@ -311,8 +311,9 @@ def step_stats(ms):
 
 
 def decode_sweep(w4, dev, steps: int, warmup: int, Ms=(1, 4, 16, 32), R: int = 20, hbm: float = 6800.0):
-    """The small-M calls (K = N = 4096, r = 32): per M, the whole call (the
-    activation kernel and the GEMM, back to back) and the GEMM alone, each in a
+    """The small-M calls (K = N = 4096, r = 32): per M, the whole call through
+    w4a4_forward (from fp16 X to Y: the fused kernel up to M = 8, quantise + GEMM
+    above), the same two steps as separate calls, and the GEMM alone, each in a
     CUDA graph over R weight replicas (> L2), so the weights come from HBM.
     GB/s = packed weights + scales (the bytes every call must stream) / time."""
     import torch
@@ -336,8 +337,13 @@ def decode_sweep(w4, dev, steps: int, warmup: int, Ms=(1, 4, 16, 32), R: int = 2
         w4.w4a4_quantize_act(X, packs[0], ws, base.r)
         w4.w4a4_linear(ws, packs[0], cs, b, Y, base.K, base.r)
         disp = w4.w4a4_last_dispatch()
+        w4.w4a4_forward(X, packs[0], cs, b, Y, base.r, act_ws=ws)
+        disp_f = w4.w4a4_last_dispatch()
         torch.cuda.synchronize()
-        gw, gg = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+        gf, gw, gg = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gf):
+            for p_ in packs:
+                w4.w4a4_forward(X, p_, cs, b, Y, base.r, act_ws=ws, stream=torch.cuda.current_stream())
         with torch.cuda.graph(gw):
             for p_ in packs:
                 st = torch.cuda.current_stream()
@@ -360,13 +366,15 @@ def decode_sweep(w4, dev, steps: int, warmup: int, Ms=(1, 4, 16, 32), R: int = 2
             torch.cuda.synchronize()
             return e0.elapsed_time(e1) * 1e3 / (steps * R)
 
-        uw, ug = tm(gw), tm(gg)
-        out[M] = {"whole_call_us": uw, "whole_call_gbs": wbytes / (uw * 1e-6) / 1e9,
+        uf, uw, ug = tm(gf), tm(gw), tm(gg)
+        out[M] = {"whole_call_us": uf, "whole_call_gbs": wbytes / (uf * 1e-6) / 1e9, "whole_call_dispatch": disp_f,
+                  "two_calls_us": uw, "two_calls_gbs": wbytes / (uw * 1e-6) / 1e9,
                   "gemm_us": ug, "gemm_gbs": wbytes / (ug * 1e-6) / 1e9, "dispatch": disp}
     low = min(out, key=lambda m: out[m]["whole_call_gbs"])
     return {"per_M": out, "min_whole_call_gbs": out[low]["whole_call_gbs"], "at_M": low,
             "frac_hbm": out[low]["whole_call_gbs"] / hbm, "hbm_gbs": hbm, "weight_bytes_per_call": wbytes,
-            "what": "whole call = w4a4_quantize_act + w4a4_linear (K = N = 4096, r = 32) per weight replica; "
+            "what": "whole call = one w4a4_forward from fp16 X (K = N = 4096, r = 32) per weight replica "
+                    "(two_calls: w4a4_quantize_act + w4a4_linear); "
                     f"{R} replicas, {R * wbytes / 2**20:.0f} MiB > L2; min over M <= 32 is the headline"}
 
 
@@ -1044,8 +1052,7 @@ def run_decode(args, rank, world, local_rank):
                         arrived.append(ev)
                 for j, p_ in enumerate(packs):
                     st.wait_event(arrived[j])
-                    w4.w4a4_quantize_act(Xd[j], p_, ws, base.r, st)
-                    w4.w4a4_linear(ws, p_, cs, b, Yd[j], base.K, base.r, w4.KERNEL_AUTO, st)
+                    w4.w4a4_forward(Xd[j], p_, cs, b, Yd[j], base.r, act_ws=ws, stream=st)
                     done = torch.cuda.Event()
                     done.record(st)
                     s_out.wait_event(done)
@@ -1057,7 +1064,7 @@ def run_decode(args, rank, world, local_rank):
             ue = max_over_ranks(tm(ge), dev, world)
             e2e = {"value": job_rate(world, wbytes, ue * 1e-3) / 1e9, "unit": "GB/s", "h2d_bytes_per_step": M * base.K * 2,
                    "d2h_bytes_per_step": M * base.N * 2, "us_per_call": ue, "M": M,
-                   "how": "per call: H2D of X from pinned host (copy stream), quantize + linear through the C-ABI, "
+                   "how": "per call: H2D of X from pinned host (copy stream), w4a4_forward through the C-ABI, "
                           "D2H of Y (second copy stream, overlapping the next call); CUDA graph over the weight "
                           "replicas"}
     # whole calls (activation kernel + GEMM back to back): the headline
@@ -1067,7 +1074,8 @@ def run_decode(args, rank, world, local_rank):
         v["whole_call_us"] = max_over_ranks(v["whole_call_us"], dev, world)
         v["whole_call_gbs"] = job_rate(world, wbytes, v["whole_call_us"] * 1e-3) / 1e9
         results[m_].update(whole_call_us=v["whole_call_us"], whole_call_gbs=v["whole_call_gbs"],
-                           frac_hbm_whole_call=v["whole_call_gbs"] / (world * hbm))
+                           frac_hbm_whole_call=v["whole_call_gbs"] / (world * hbm),
+                           whole_call_dispatch=v["whole_call_dispatch"], two_calls_us=v["two_calls_us"])
     if world > 1:
         dist.barrier()
         dist.destroy_process_group()
@@ -1087,7 +1095,9 @@ def run_decode(args, rank, world, local_rank):
                    "svd_lora": {"seconds_per_layer": svd_s, "rounds": 3, "power_iters": 16,
                                 "residual_per_round": svd_errs,
                                 "what": "w4a4_pack_weights_svd on the K=N=4096 weights, r=32 (offline)"}},
-        "gpu_launches": args.steps * R * len(results) * 2, "e2e": e2e, "clocks": sampler.summary(),
+        "gpu_launches": args.steps * R * sum(1 if "linear_fused" in v.get("whole_call_dispatch", "") else 2
+                                             for v in results.values()),
+        "e2e": e2e, "clocks": sampler.summary(),
         "roofline": {"bound": "hbm", "achieved": low_gemm / world, "peak": hbm, "unit": "GB/s",
                      "frac": low_gemm / world / hbm, "traffic": None,
                      "kernel": "w4a4_linear (small-M weight-streaming kernel; the value above is the whole call)",

@@ -157,10 +157,10 @@ w4a4_status w4a4_linear(const void* act_ws, size_t act_ws_bytes, const void* pac
  * Y = the layer of w4a4_linear applied to X fp16 [M, K] row-major, i.e.
  * w4a4_quantize_act followed by w4a4_linear, in one call.  Arguments as for
  * those two; X must be 16-byte aligned.
- * kernel W4A4_KERNEL_AUTO: for 1 <= M <= w4a4_small_m_threshold() and the shapes
- * the fused kernel takes (r <= 32; K / 64 groups split over at most 8 CTAs with
- * at most 8 groups each, i.e. K <= 4096 at N >= 1024; the shared-memory plan
- * fits two CTAs per SM), one kernel does everything: quantisation and LoRA down
+ * kernel W4A4_KERNEL_AUTO: for 1 <= M <= 8 and the shapes the fused kernel takes
+ * (M <= 32; r <= 32; K / 64 groups split over at most 8 CTAs with at most 8
+ * groups each, i.e. K <= 4096 at N >= 1024; the shared-memory plan fits two CTAs
+ * per SM), one kernel does everything: quantisation and LoRA down
  * of X (the same codes, scales and SA as w4a4_quantize_act, bit for bit; the
  * LoRA-down sums in another fixed order, so lora_act may differ in its last
  * fp16 bit), the exact per-group products, LoRA up and the affine.  act_ws may
@@ -168,8 +168,10 @@ w4a4_status w4a4_linear(const void* act_ws, size_t act_ws_bytes, const void* pac
  * the kernel also writes the codes, (sA, SA) pairs and lora_act there in the
  * workspace layout.  Otherwise the call runs w4a4_quantize_act and w4a4_linear
  * on act_ws, which is then required.
- * kernel W4A4_KERNEL_FUSED: the fused kernel, W4A4_ERR_UNSUPPORTED_SHAPE where
- * it does not apply.  TC, SMALLM, SMALLM_TC: the two-call path with that GEMM.
+ * (Above M = 8 the two-call path is faster: each 128-row weight tile repeats the
+ * quantisation and LoRA down of the X slice it reads.)
+ * kernel W4A4_KERNEL_FUSED: the fused kernel (M <= 32), W4A4_ERR_UNSUPPORTED_SHAPE
+ * where it does not apply.  TC, SMALLM, SMALLM_TC: the two-call path with that GEMM.
  * Every argument check runs before anything is launched. */
 w4a4_status w4a4_forward(const uint16_t* X, const void* packed, size_t packed_bytes, const uint16_t* colscale,
                          const uint16_t* bias, int M, int N, int K, int r, uint16_t* Y, void* act_ws,

@@ -358,8 +358,16 @@ w4a4_status w4a4_linear(const void* act_ws, size_t act_ws_bytes, const void* pac
                               W4A4_KERNEL_AUTO, stream);
 }
 
+// AUTO takes the fused kernel up to this M.  Every 128-row weight tile's cluster
+// repeats the quantisation and LoRA down of the whole X slice it reads, so that
+// work grows with M times the tile count: measured at K = N = 4096, r = 32 (a CUDA
+// graph of back-to-back calls), the fused call against quantise + GEMM is
+// 9.3 vs 11.0 us at M = 1, 9.6 vs 11.5 at M = 4, 11.5 vs 11.4 at M = 16 and
+// 14.9 vs 13.0 at M = 32.
+constexpr int kFusedMaxM = 8;
+
 int w4a4_forward_is_fused(int M, int N, int K, int r) {
-    if (check_kn(N, K, r) != W4A4_OK || M < 1 || M > w4a4_small_m_threshold()) return 0;
+    if (check_kn(N, K, r) != W4A4_OK || M < 1 || M > kFusedMaxM || M > w4a4_small_m_threshold()) return 0;
     return fused_eligible(M, N, K, r) ? 1 : 0;
 }
 

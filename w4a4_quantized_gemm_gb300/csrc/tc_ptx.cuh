@@ -140,6 +140,11 @@ __device__ __forceinline__ void st_async_v4(uint32_t remote_addr, float4 v, uint
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
     asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(nthreads) : "memory");
 }
+// Arrive on a named barrier without waiting (producer side of a handoff whose
+// consumer calls named_bar_sync with the same id and count).
+__device__ __forceinline__ void named_bar_arrive(uint32_t id, uint32_t nthreads) {
+    asm volatile("bar.arrive %0, %1;\n" ::"r"(id), "r"(nthreads) : "memory");
+}
 // Named barrier over `nthreads` threads with an OR reduction: every
 // participant receives the OR of the participants' predicates, so all of them
 // take the same branch after it.
