@@ -65,10 +65,9 @@ static_assert(NPB * GPJ * BN <= int(TMEM_COLS), "job buffers must fit in tensor 
 constexpr int SS = 4;  // scale-ring depth (jobs)
 constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;
 constexpr uint64_t DRAIN_LIMIT_NS = 200000000ull;
-// Sleep between barrier polls, per role: the producers and the expansion run
-// stages ahead and can wake late; the MMA issuer and the epilogue are on the
-// critical path.
-constexpr uint32_t BACKOFF_PRODUCER = 256, BACKOFF_EXPAND = 128, BACKOFF_MMA = 32, BACKOFF_EPI = 64;
+// Waiting warps are suspended in the barrier unit until the phase completes (woken at once,
+// no issue slots spent), re-checking the abort flag and the clock every SUSPEND_NS at most
+constexpr uint32_t SUSPEND_NS = 20000;
 
 // Stage (one job = GPJ groups): activation codes (per group 2 planes x 128 rows
 // x 32 B), weight nibbles (per group 128 rows x 32 B), the expanded B operand
@@ -93,6 +92,26 @@ constexpr int MAX_KS = 4;
 constexpr uint32_t kRedBlock = 32 * EPI_COLS * 4;
 constexpr uint32_t kRed = 64 * 1024;  // max over KS of (KS - 1) * ceil(4 / KS) * 4 blocks
 __host__ __device__ constexpr int owned_slices(int KS) { return (4 + KS - 1) / KS; }
+
+// Tile order.  Tile t -> (M tile, N tile): M tiles vary fastest, so the CTAs at
+// work at one time share a few weight tiles and sweep all of A -- unless A (the
+// activation codes, M x K bytes) is large and larger than the packed weights:
+// then N tiles vary fastest, so that A is read from DRAM once and the weights
+// (which then fit in L2) are the operand read again (at M = 8192, K = 14336 the
+// M-fastest order read 3.5 GB from DRAM for 0.15 GB of operands).
+__host__ __device__ inline bool n_fastest(int M, int N, int K) {
+    const size_t a = size_t(M) * size_t(K), w = size_t(N) * size_t(K) / 2;
+    return a > (size_t(64) << 20) && a > w;
+}
+__host__ __device__ inline void tile_coords(int t, int MT, int NT, bool nf, int& mt, int& nt) {
+    if (nf) {
+        mt = t / NT;
+        nt = t % NT;
+    } else {
+        mt = t % MT;
+        nt = t / MT;
+    }
+}
 static_assert((2 - 1) * 2 * 4 * kRedBlock <= kRed && (3 - 1) * 2 * 4 * kRedBlock <= kRed &&
                   (4 - 1) * 1 * 4 * kRedBlock <= kRed, "reduction buffer too small");
 
@@ -144,6 +163,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const PackedLayout PL = packed_layout(N, K, r);
     const int MT = AL.MT, NT = (N + BN - 1) / BN;
     const int tiles = MT * NT;
+    const bool nf = n_fastest(M, N, K);
     // Work is walked as segments (tile t, jobs [a, b)).  Round-robin: CTA (or
     // cluster) cid takes tiles cid, cid + ncl, ... with jobs [j0, j1).  Stream-K:
     // the tiles x J jobs, tile-major, are cut into gridDim.x equal runs, CTA p
@@ -229,7 +249,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (warp == WARP_PRODUCER_W && lane == 0 && u_begin < u_end) {
         int t0, a0, b0;
         seg_at(u_begin, t0, a0, b0);
-        const int n0 = (t0 / MT) * BN, rows = min(BN, N - n0);
+        int mt0, nt0;
+        tile_coords(t0, MT, NT, nf, mt0, nt0);
+        const int n0 = nt0 * BN, rows = min(BN, N - n0);
         for (int g = a0 * GPJ; g < min(G, (a0 + S) * GPJ); ++g)
             prefetch_l2(packed + PL.qW + (size_t(g) * N + n0) * 32, uint32_t(rows) * 32);
     }
@@ -256,10 +278,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         for (int u = u_begin; u < u_end && ok; u = seg_next(u, a, b)) {
             seg_at(u, t, a, b);
             const int RP = lora_planes(a);
-            const int mt = t % MT, n0 = (t / MT) * BN;
+            int mt, nt;
+            tile_coords(t, MT, NT, nf, mt, nt);
+            const int n0 = nt * BN;
             const int rows = min(BN, N - n0);
             if (RP > 0 && role < 2) {
-                if (!warp_wait_parity(lempty, lp ^ 1u, abort_flag, WAIT_LIMIT_NS, BACKOFF_PRODUCER)) {
+                if (!warp_wait_parity_suspend(lempty, lp ^ 1u, abort_flag, WAIT_LIMIT_NS, SUSPEND_NS)) {
                     ok = false;
                     break;
                 }
@@ -283,7 +307,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 const int g0 = jb * GPJ, ng = min(GPJ, G - g0);
                 const int s = int(it % S);
                 const uint32_t ph = (it / S) & 1u;
-                if (!warp_wait_parity(empty(s), ph ^ 1u, abort_flag, WAIT_LIMIT_NS, BACKOFF_PRODUCER)) {
+                if (!warp_wait_parity_suspend(empty(s), ph ^ 1u, abort_flag, WAIT_LIMIT_NS, SUSPEND_NS)) {
                     ok = false;
                     break;
                 }
@@ -329,8 +353,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             if (RP > 0) {
                 // the LoRA product takes a job buffer of its own (first 128 columns)
                 const uint32_t bf = jc % NPB, tph = (jc / NPB) & 1u;
-                if (!warp_wait_parity(tempty(bf), tph ^ 1u, abort_flag, WAIT_LIMIT_NS, BACKOFF_MMA) ||
-                    !warp_wait_parity(lfull, lp, abort_flag, WAIT_LIMIT_NS, BACKOFF_MMA)) {
+                if (!warp_wait_parity_suspend(tempty(bf), tph ^ 1u, abort_flag, WAIT_LIMIT_NS, SUSPEND_NS) ||
+                    !warp_wait_parity_suspend(lfull, lp, abort_flag, WAIT_LIMIT_NS, SUSPEND_NS)) {
                     ok = false;
                     break;
                 }
@@ -351,9 +375,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 const int s = int(it % S);
                 const uint32_t ph = (it / S) & 1u;
                 const uint32_t bf = jc % NPB, tph = (jc / NPB) & 1u;
-                if (!warp_wait_parity(full(s), ph, abort_flag, WAIT_LIMIT_NS, BACKOFF_MMA) ||
-                    !warp_wait_parity(bready(s), ph, abort_flag, WAIT_LIMIT_NS, BACKOFF_MMA) ||
-                    !warp_wait_parity(tempty(bf), tph ^ 1u, abort_flag, WAIT_LIMIT_NS, BACKOFF_MMA)) {
+                if (!warp_wait_parity_suspend(full(s), ph, abort_flag, WAIT_LIMIT_NS, SUSPEND_NS) ||
+                    !warp_wait_parity_suspend(bready(s), ph, abort_flag, WAIT_LIMIT_NS, SUSPEND_NS) ||
+                    !warp_wait_parity_suspend(tempty(bf), tph ^ 1u, abort_flag, WAIT_LIMIT_NS, SUSPEND_NS)) {
                     ok = false;
                     break;
                 }
@@ -394,8 +418,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 const int ng = min(GPJ, G - jb * GPJ);
                 const int s = int(it % S), q = int(it % SS);
                 const uint32_t ph = (it / S) & 1u, sph = (it / SS) & 1u;
-                if (!warp_wait_parity(full(s), ph, abort_flag, WAIT_LIMIT_NS, BACKOFF_EXPAND) ||
-                    !warp_wait_parity(sempty(q), sph ^ 1u, abort_flag, WAIT_LIMIT_NS, BACKOFF_EXPAND)) {
+                if (!warp_wait_parity_suspend(full(s), ph, abort_flag, WAIT_LIMIT_NS, SUSPEND_NS) ||
+                    !warp_wait_parity_suspend(sempty(q), sph ^ 1u, abort_flag, WAIT_LIMIT_NS, SUSPEND_NS)) {
                     ok = false;
                     break;
                 }
@@ -451,7 +475,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         for (int u = u_begin; u < u_end && ok; u = seg_next(u, a, b)) {
             seg_at(u, t, a, b);
             const int RP = lora_planes(a);
-            const int mt = t % MT, n0 = (t / MT) * BN;
+            int mt, nt;
+            tile_coords(t, MT, NT, nf, mt, nt);
+            const int n0 = nt * BN;
             const int m = mt * BM + row;
             uint64_t acc[EPI_COLS / 2];  // running sums as packed column pairs
             // this warp's colscale / bias for the tile's store, fetched while the jobs run:
@@ -478,7 +504,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             if (stores) cp_async_commit();
             if (RP > 0) {
                 const uint32_t bf = jc % NPB, tph = (jc / NPB) & 1u;
-                if (!warp_wait_parity(tfull(bf), tph, abort_flag, WAIT_LIMIT_NS, BACKOFF_EPI)) {
+                if (!warp_wait_parity_suspend(tfull(bf), tph, abort_flag, WAIT_LIMIT_NS, SUSPEND_NS)) {
                     ok = false;
                     break;
                 }
@@ -502,8 +528,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 const int q = int(it % SS);
                 const uint32_t sph = (it / SS) & 1u;
                 const uint32_t bf = jc % NPB, tph = (jc / NPB) & 1u;
-                if (!warp_wait_parity(tfull(bf), tph, abort_flag, WAIT_LIMIT_NS, BACKOFF_EPI) ||
-                    !warp_wait_parity(sfull(q), sph, abort_flag, WAIT_LIMIT_NS, BACKOFF_EPI)) {
+                if (!warp_wait_parity_suspend(tfull(bf), tph, abort_flag, WAIT_LIMIT_NS, SUSPEND_NS) ||
+                    !warp_wait_parity_suspend(sfull(q), sph, abort_flag, WAIT_LIMIT_NS, SUSPEND_NS)) {
                     ok = false;
                     break;
                 }
@@ -639,7 +665,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 // owner: one thread posts the bytes this CTA receives for the tile
                 if (sl == kr && lq == 0 && lane == 0)
                     mbar_expect_tx(red_full, uint32_t(own * 4 * (KS - 1)) * kRedBlock);
-                if (!warp_wait_parity(red_full, tc & 1u, abort_flag, WAIT_LIMIT_NS, BACKOFF_EPI)) {
+                if (!warp_wait_parity_suspend(red_full, tc & 1u, abort_flag, WAIT_LIMIT_NS, SUSPEND_NS)) {
                     ok = false;
                     break;
                 }
@@ -662,7 +688,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 __syncwarp();
                 if (lane == 0) mbar_arrive(own_done);
                 if (sl == kr && lq == 0) {
-                    if (!warp_wait_parity(own_done, tc & 1u, abort_flag, WAIT_LIMIT_NS, BACKOFF_EPI)) {
+                    if (!warp_wait_parity_suspend(own_done, tc & 1u, abort_flag, WAIT_LIMIT_NS, SUSPEND_NS)) {
                         ok = false;
                         break;
                     }
@@ -823,9 +849,9 @@ w4a4_status launch_impl(const uint8_t* ws, const uint8_t* packed, const uint16_t
         cudaGetLastError();
         return W4A4_ERR_CUDA;
     }
-    set_dispatch("gemm_tc tcgen05.f8f6f4 tile=%dx%d groups/job=%d stages=%d split-K=%d (cluster) tiles=%d grid=%d%s%s",
-                 BM, BN, GPJ, S, KS, tiles, clusters * KS, silu_I ? " silu(gate)*up" : "",
-                 DUMP ? " (partials dump)" : "");
+    set_dispatch("gemm_tc tcgen05.f8f6f4 tile=%dx%d groups/job=%d stages=%d split-K=%d (cluster) tiles=%d grid=%d%s%s%s",
+                 BM, BN, GPJ, S, KS, tiles, clusters * KS, n_fastest(M, N, K) ? " N-tiles-fastest" : "",
+                 silu_I ? " silu(gate)*up" : "", DUMP ? " (partials dump)" : "");
     return launch_status();
 }
 

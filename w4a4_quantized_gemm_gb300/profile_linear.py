@@ -2,8 +2,11 @@
 
     python -m w4a4_quantized_gemm_gb300.profile_linear <qkv|o|gate_up|down|prefill_up|prefill_down|m1|m16|m32> [iters]
     python -m w4a4_quantized_gemm_gb300.profile_linear norm_gate_up [iters]
+    python -m w4a4_quantized_gemm_gb300.profile_linear fwd_<m1|m16|m32> [iters]
 
-The last form runs the stack's RMSNorm glue alone: the gate_up output
+The fwd_ forms call w4a4_forward instead (the whole layer from fp16 X in one
+call: the fused small-M kernel up to M = 8).  The norm_gate_up form runs the
+stack's RMSNorm glue alone: the gate_up output
 [700, 6144] normalised over its first 3072 columns into the down linear's
 input, on replicas of the buffers.
 
@@ -56,7 +59,8 @@ def main() -> int:
         torch.cuda.synchronize()
         print(f"{name}: M=700 ld=6144 K=3072 replicas={R} iters={iters} dispatch={w4.w4a4_last_dispatch()}")
         return 0
-    s = SHAPES[name]
+    fwd = name.startswith("fwd_")
+    s = SHAPES[name[4:] if fwd else name]
     M, K, N, r = s["M"], s["K"], s["N"], s["r"]
     c = make_linear_case(M=M, K=K, N=N, r=r, seed=0)
     dev = torch.device("cuda", 0)
@@ -77,8 +81,11 @@ def main() -> int:
     Ys = [torch.empty((M, N), dtype=torch.float16, device=dev) for _ in range(R)]
     for i in range(iters):
         j = i % R
-        w4.w4a4_quantize_act(Xs[j], Ps[j], WS[j], r)
-        w4.w4a4_linear(WS[j], Ps[j], cs, b, Ys[j], K, r)
+        if fwd:
+            w4.w4a4_forward(Xs[j], Ps[j], cs, b, Ys[j], r, act_ws=WS[j])
+        else:
+            w4.w4a4_quantize_act(Xs[j], Ps[j], WS[j], r)
+            w4.w4a4_linear(WS[j], Ps[j], cs, b, Ys[j], K, r)
     torch.cuda.synchronize()
     print(f"{name}: M={M} K={K} N={N} r={r} replicas={R} iters={iters} dispatch={w4.w4a4_last_dispatch()}")
     return 0
