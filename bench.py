@@ -281,19 +281,19 @@ def kernel_source_hash(name: str) -> str:
 # counters no longer describe it and traffic is reported as null.
 NCU_TRAFFIC = {
     # the four decoder-layer GEMM launches (qkv, o, gate_up, down) at M = 700, one launch each,
-    # read from HBM (24 input replicas cycled): 3,495,168 + 3,071,232 + 4,770,560 + 4,513,024 bytes;
+    # read from HBM (24 input replicas cycled): 3,494,400 + 3,066,368 + 4,747,264 + 4,508,160 bytes;
     # Y stays in L2 within a launch, so the write counter is near zero (profiles/gemm_tc_traffic_decoder_layer_m700.md)
-    (WORKLOAD, "9ed4a39ebb1a337f"): {
-        "bytes_per_pass": 15849984,
-        "per_linear": {"qkv": 3495168, "o": 3071232, "gate_up": 4770560, "down": 4513024},
+    (WORKLOAD, "5a739d4976ca8da5"): {
+        "bytes_per_pass": 15816192,
+        "per_linear": {"qkv": 3494400, "o": 3066368, "gate_up": 4747264, "down": 4508160},
         "source": "ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum, one launch per linear "
                   "(profiles/gemm_tc_traffic_decoder_layer_m700.md)"},
-    # the M = 8192, 4096 -> 14336 GEMM launch: 76.22 MB read + 199.38 MB written
-    # (profiles/gemm_tc_prefill_m8192.md); the 14336 -> 4096 launch was not captured
-    (PREFILL_WORKLOAD, "9ed4a39ebb1a337f"): {
-        "bytes_per_pass": None,
-        "per_linear": {"gate_up_style": 275602432, "down_style": None},
-        "source": "ncu --section SpeedOfLight --metrics dram__bytes_read.sum,dram__bytes_write.sum, one launch "
+    # the two M = 8192 GEMM launches: 4096 -> 14336 73.65 MB read + 198.39 MB written, 14336 -> 4096
+    # 165.79 MB read + 56.01 MB written (profiles/gemm_tc_prefill_m8192.md)
+    (PREFILL_WORKLOAD, "5a739d4976ca8da5"): {
+        "bytes_per_pass": 272034304 + 221797888,
+        "per_linear": {"gate_up_style": 272034304, "down_style": 221797888},
+        "source": "ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum, one launch per linear "
                   "(profiles/gemm_tc_prefill_m8192.md)"},
 }
 

@@ -1,8 +1,8 @@
 """Profiling driver: one W4A4 linear of the M=700 decoder layer, called in a loop.
 
-    python -m w4a4_quantized_gemm_gb300.profile_linear <qkv|o|gate_up|down|prefill_up|prefill_down|m1|m16|m32> [iters]
+    python -m w4a4_quantized_gemm_gb300.profile_linear <qkv|o|gate_up|down|prefill_up|prefill_down|m1|m4|m16|m32> [iters]
     python -m w4a4_quantized_gemm_gb300.profile_linear norm_gate_up [iters]
-    python -m w4a4_quantized_gemm_gb300.profile_linear fwd_<m1|m16|m32> [iters]
+    python -m w4a4_quantized_gemm_gb300.profile_linear fwd_<m1|m4|m16|m32> [iters]
 
 The fwd_ forms call w4a4_forward instead (the whole layer from fp16 X in one
 call: the fused small-M kernel up to M = 8).  The norm_gate_up form runs the
@@ -33,6 +33,7 @@ SHAPES.update({
     "prefill_up": dict(M=8192, K=4096, N=14336, r=32),
     "prefill_down": dict(M=8192, K=14336, N=4096, r=32),
     "m1": dict(M=1, K=4096, N=4096, r=32),
+    "m4": dict(M=4, K=4096, N=4096, r=32),
     "m16": dict(M=16, K=4096, N=4096, r=32),
     "m32": dict(M=32, K=4096, N=4096, r=32),
 })
