@@ -69,7 +69,7 @@ __device__ __forceinline__ void ldmatrix_x4(uint32_t (&r)[4], const void* p) {
 }
 
 template <int R, bool NORM>  // LoRA rank, multiple of 16 (0 = no LoRA branch); RMSNorm on the way in
-__global__ void __launch_bounds__(kWarps * 32) quantize_act_kernel(const uint16_t* __restrict__ X, int ld_x,
+__global__ void __launch_bounds__(kWarps * 32, 2) quantize_act_kernel(const uint16_t* __restrict__ X, int ld_x,
                                                                    const uint2* __restrict__ Ldp, int M,
                                                                    int K, uint8_t* __restrict__ ws) {
     extern __shared__ __align__(16) uint8_t qsm[];
