@@ -3,8 +3,13 @@
     python -m w4a4_quantized_gemm_gb300.profile_linear <qkv|o|gate_up|down|prefill_up|prefill_down|m1|m4|m16|m32> [iters]
     python -m w4a4_quantized_gemm_gb300.profile_linear norm_gate_up [iters]
     python -m w4a4_quantized_gemm_gb300.profile_linear fwd_<m1|m4|m16|m32> [iters]
+    python -m w4a4_quantized_gemm_gb300.profile_linear single [iters]
+    python -m w4a4_quantized_gemm_gb300.profile_linear stack [forwards]
 
-The fwd_ forms call w4a4_forward instead (the whole layer from fp16 X in one
+`single` is the single linear M=64, K=N=1024.  `stack` builds the 28-layer
+stack (112 linears, RMSNorm folded into each next activation kernel) and runs
+that many eager forward passes (336 launches each).  The fwd_ forms call
+w4a4_forward instead (the whole layer from fp16 X in one
 call: the fused small-M kernel up to M = 8).  The norm_gate_up form runs the
 stack's RMSNorm glue alone: the gate_up output
 [700, 6144] normalised over its first 3072 columns into the down linear's
@@ -26,10 +31,11 @@ import numpy as np
 
 sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
 
-from synthetic import DECODER_LAYER_M700, make_linear_case  # noqa: E402
+from synthetic import DECODER_LAYER_M700, SINGLE_LINEAR, make_linear_case  # noqa: E402
 
 SHAPES = dict(DECODER_LAYER_M700)
 SHAPES.update({
+    "single": dict(SINGLE_LINEAR),
     "prefill_up": dict(M=8192, K=4096, N=14336, r=32),
     "prefill_down": dict(M=8192, K=14336, N=4096, r=32),
     "m1": dict(M=1, K=4096, N=4096, r=32),
@@ -48,6 +54,19 @@ def main() -> int:
 
     name = sys.argv[1] if len(sys.argv) > 1 else "qkv"
     iters = int(sys.argv[2]) if len(sys.argv) > 2 else 30
+    if name == "stack":
+        from synthetic import STACK_LAYERS, STACK_LINEARS, make_stack_input, make_stack_linear
+        from w4a4_quantized_gemm_gb300.stack import W4A4Stack
+        dev = torch.device("cuda", 0)
+        nl = len(STACK_LINEARS)
+        stack = W4A4Stack((make_stack_linear(l, j) for l in range(STACK_LAYERS) for j in range(nl)), 700, dev)
+        stack.X0.copy_(torch.from_numpy(make_stack_input(700).view(np.float16).copy()).to(dev))
+        for _ in range(iters):
+            stack.forward()
+        torch.cuda.synchronize()
+        print(f"stack: {len(stack.layers)} linears, {stack.launches_per_forward()} launches per forward, "
+              f"forwards={iters} status={w4.w4a4_device_status()}")
+        return 0
     if name == "norm_gate_up":
         dev = torch.device("cuda", 0)
         g = torch.Generator(device="cpu").manual_seed(0)
