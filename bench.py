@@ -281,21 +281,27 @@ def kernel_source_hash(name: str) -> str:
 # counters no longer describe it and traffic is reported as null.
 NCU_TRAFFIC = {
     # the four decoder-layer GEMM launches (qkv, o, gate_up, down) at M = 700, one launch each,
-    # read from HBM (24 input replicas cycled): 3,494,400 + 3,066,368 + 4,747,264 + 4,508,160 bytes;
+    # read from HBM (24 input replicas cycled): 3,494,144 + 3,066,368 + 4,747,520 + 4,508,416 bytes;
     # Y stays in L2 within a launch, so the write counter is near zero (profiles/gemm_tc_traffic_decoder_layer_m700.md)
-    (WORKLOAD, "5a739d4976ca8da5"): {
-        "bytes_per_pass": 15816192,
-        "per_linear": {"qkv": 3494400, "o": 3066368, "gate_up": 4747264, "down": 4508160},
+    (WORKLOAD, "860c8d9177f66133"): {
+        "bytes_per_pass": 15817728,
+        "per_linear": {"qkv": 3495168, "o": 3066368, "gate_up": 4747776, "down": 4508416},
         "source": "ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum, one launch per linear "
                   "(profiles/gemm_tc_traffic_decoder_layer_m700.md)"},
-    # the two M = 8192 GEMM launches: 4096 -> 14336 73.65 MB read + 198.39 MB written, 14336 -> 4096
-    # 165.79 MB read + 56.01 MB written (profiles/gemm_tc_prefill_m8192.md)
-    (PREFILL_WORKLOAD, "5a739d4976ca8da5"): {
-        "bytes_per_pass": 272034304 + 221797888,
-        "per_linear": {"gate_up_style": 272034304, "down_style": 221797888},
-        "source": "ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum, one launch per linear "
+    # the M = 8192 GEMMs, two launches per linear (the full rounds, then the last round split over K):
+    # 4096 -> 14336 74.41 + 14.70 MB read, 197.75 MB written; 14336 -> 4096 160.56 + 37.76 MB read,
+    # 51.39 MB written (profiles/gemm_tc_prefill_m8192.md)
+    (PREFILL_WORKLOAD, "860c8d9177f66133"): {
+        "bytes_per_pass": 286869760 + 249710080,
+        "per_linear": {"gate_up_style": 286869760, "down_style": 249710080},
+        "source": "ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum, both launches of each linear "
                   "(profiles/gemm_tc_prefill_m8192.md)"},
 }
+
+
+def gemm_launches(dispatch: str) -> int:
+    """GEMM launches one w4a4_linear call makes (two when its last round of tiles runs split over K)."""
+    return 2 if "round-robin, last" in dispatch else 1
 
 
 def ncu_traffic(workload: str, source: str = "gemm_tc.cu"):
@@ -717,7 +723,7 @@ def run_ours(args, rank, world, local_rank):
         "config": base_config({"replicas": R, "l2": f"inputs larger than L2: {footprint / 2**20:.0f} MiB cycled",
                                "passes_per_step": P, "dispatch": dispatch}),
         "step_ms": stats, "ms_per_pass": ms_per_step / P,
-        "gpu_launches": args.steps * P * 2 * len(names),
+        "gpu_launches": args.steps * P * sum(1 + gemm_launches(dispatch[n]) for n in names),
         "roofline": roofline, "decode": decode, "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
     }
     print(json.dumps(line), flush=True)
@@ -1276,7 +1282,8 @@ def run_prefill(args, rank, world, local_rank):
                 "traffic_per_linear": traffic["per_linear"] if traffic else None,
                 "traffic_source": traffic["source"] if traffic else
                 "null: no ncu capture of the current gemm_tc.cu source",
-                "kernel": "w4a4_linear (GEMM + LoRA up + affine), 2 launches per step",
+                "kernel": "w4a4_linear (GEMM + LoRA up + affine), "
+                          f"{sum(gemm_launches(dispatch[n]) for n in names)} launches per step",
                 "peak_source": f"{peak_src} bf16 burst x 2 (fp8 kind)",
                 "per_linear_gemm_us": g_us, "per_linear_quantize_us": q_us,
                 "per_linear_gemm_tops": {n: metrics.linear_ops(PREFILL[n]["M"], PREFILL[n]["N"], PREFILL[n]["K"],
@@ -1382,7 +1389,7 @@ def run_prefill(args, rank, world, local_rank):
         "config": {"workload": PREFILL_WORKLOAD, "M": 8192, "group": 64, "rank": 32,
                    "linears": {n: [PREFILL[n]["K"], PREFILL[n]["N"]] for n in names}, "replicas": R,
                    "l2": f"inputs larger than L2: {footprint / 2**20:.0f} MiB cycled", "dispatch": dispatch},
-        "gpu_launches": args.steps * 2 * len(names),
+        "gpu_launches": args.steps * sum(1 + gemm_launches(dispatch[n]) for n in names),
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "clocks": sampler.summary() if sampler else None,
     }
     print(json.dumps(line), flush=True)

@@ -112,3 +112,27 @@ def test_prefill_m8192_every_tile(name):
     qA, sA_ref = oracle.quantize_act(c.X[rows])
     assert np.array_equal(codes.cpu().numpy()[rows], qA)
     assert np.array_equal(sA.cpu().numpy()[rows], sA_ref)
+
+
+@pytest.mark.parametrize("M,K,N,r", [(256, 2048, 10240, 32), (1280, 1536, 2048, 16)], ids=lambda v: str(v))
+def test_thin_last_round_runs_split_over_k(M, K, N, r):
+    """A last round of tiles at most half the SMs, with enough jobs per tile, runs as a
+    launch of its own with split-K (the full rounds round-robin before it): every output
+    tile, those of both launches, on the first and last row of every 128-row tile;
+    the group partials of the same schedule bit-exact on those rows."""
+    c = make_linear_case(M, K, N, r, seed=M + N)
+    t = to_dev(c)
+    packed = pack(c, t)
+    ws = quantize(c, t, packed)
+    Y = run_linear(c, t, packed, ws, w4.KERNEL_AUTO)
+    d = w4.w4a4_last_dispatch()
+    assert w4.w4a4_device_status() == 0
+    assert "round-robin, last" in d and "split-K=" in d, d
+    rows = np.unique(np.r_[np.arange(0, c.M, 128), np.minimum(np.arange(127, c.M + 127, 128), c.M - 1)])
+    y = oracle.linear_rows(c.X, c.W, c.L_down, c.L_up, c.colscale, c.bias, rows)
+    check_tol(Y[torch.from_numpy(rows).cuda()], y, f"thin last round {M}x{K}x{N}")
+    P = w4.w4a4_debug_group_partials(ws, packed, M, N, K, r, w4.KERNEL_AUTO)
+    assert "round-robin, last" in w4.w4a4_last_dispatch()
+    qA, _ = oracle.quantize_act(c.X[rows])
+    qW, _ = oracle.quantize_weights(c.W)
+    assert np.array_equal(P.cpu().numpy()[rows], oracle.group_partials(qA, qW))

@@ -142,7 +142,8 @@ template <int S, bool SPLIT, bool SK, bool DUMP>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_tc_kernel(const uint8_t* __restrict__ ws, const uint8_t* __restrict__ packed,
                    const uint16_t* __restrict__ colscale, const uint16_t* __restrict__ bias, int M, int N, int K,
-                   int r, uint16_t* __restrict__ Y, int32_t* __restrict__ P, int KS, int silu_I) {
+                   int r, uint16_t* __restrict__ Y, int32_t* __restrict__ P, int KS, int silu_I, int t_lo,
+                   int t_hi) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -165,7 +166,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int tiles = MT * NT;
     const bool nf = n_fastest(M, N, K);
     // Work is walked as segments (tile t, jobs [a, b)).  Round-robin: CTA (or
-    // cluster) cid takes tiles cid, cid + ncl, ... with jobs [j0, j1).  Stream-K:
+    // cluster) cid takes tiles t_lo + cid, t_lo + cid + ncl, ... below t_hi with jobs
+    // [j0, j1) (a launch may cover a range of the tiles: the last, thin round of tiles
+    // can be launched on its own with split-K).  Stream-K:
     // the tiles x J jobs, tile-major, are cut into gridDim.x equal runs, CTA p
     // taking run p; a tile cut between CTAs is finished by the CTA holding its
     // first job, which adds the later CTAs' fp32 sums handed over in the workspace.
@@ -173,8 +176,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int units = tiles * J;
     const int sk_ctas = int(gridDim.x);
     auto sk_start = [&](int p) -> int { return int((long long)p * units / sk_ctas); };
-    const int u_begin = SK ? sk_start(int(blockIdx.x)) : cid;
-    const int u_end = SK ? sk_start(int(blockIdx.x) + 1) : tiles;
+    const int u_begin = SK ? sk_start(int(blockIdx.x)) : t_lo + cid;
+    const int u_end = SK ? sk_start(int(blockIdx.x) + 1) : t_hi;
     auto seg_at = [&](int u, int& t, int& a, int& b) {
         if (SK) {
             t = u / J;
@@ -786,7 +789,7 @@ int launch_regs() {
 template <int S, bool SPLIT, bool SK, bool DUMP>
 w4a4_status launch_impl(const uint8_t* ws, const uint8_t* packed, const uint16_t* cs, const uint16_t* bias, int M,
                         int N, int K, int r, uint16_t* Y, int32_t* P, int KS, cudaStream_t s, int sk_ctas = 0,
-                        int silu_I = 0) {
+                        int silu_I = 0, int t_lo = 0, int t_hi = -1) {
     auto kern = gemm_tc_kernel<S, SPLIT, SK, DUMP>;
     static int attr_done[64] = {0};
     int dev = 0;
@@ -804,9 +807,11 @@ w4a4_status launch_impl(const uint8_t* ws, const uint8_t* packed, const uint16_t
         return W4A4_ERR_CUDA;
     const int MT = (M + BM - 1) / BM, NT = (N + BN - 1) / BN;
     const int tiles = MT * NT;
+    if (t_hi < 0) t_hi = tiles;
+    const int ntl = t_hi - t_lo;  // the tiles of this launch
     const uint32_t smem = smem_map(S, rp, SPLIT).total;
     if (!SPLIT) {
-        const int grid = SK ? sk_ctas : (tiles < device_sm_count() ? tiles : device_sm_count());
+        const int grid = SK ? sk_ctas : (ntl < device_sm_count() ? ntl : device_sm_count());
         cudaLaunchConfig_t cfg{};
         cudaLaunchAttribute attr[1];
         cfg.attrs = attr;
@@ -815,7 +820,8 @@ w4a4_status launch_impl(const uint8_t* ws, const uint8_t* packed, const uint16_t
         cfg.blockDim = dim3(NUM_THREADS);
         cfg.dynamicSmemBytes = smem;
         cfg.stream = s;
-        if (cudaLaunchKernelEx(&cfg, kern, ws, packed, cs, bias, M, N, K, r, Y, P, 1, silu_I) != cudaSuccess) {
+        if (cudaLaunchKernelEx(&cfg, kern, ws, packed, cs, bias, M, N, K, r, Y, P, 1, silu_I, t_lo, t_hi) !=
+            cudaSuccess) {
             cudaGetLastError();
             return W4A4_ERR_CUDA;
         }
@@ -836,16 +842,17 @@ w4a4_status launch_impl(const uint8_t* ws, const uint8_t* packed, const uint16_t
     cfg.blockDim = dim3(NUM_THREADS);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
-    cfg.gridDim = dim3(unsigned(tiles * KS));
+    cfg.gridDim = dim3(unsigned(ntl * KS));
     int active = 0;
     if (cudaOccupancyMaxActiveClusters(&active, kern, &cfg) != cudaSuccess || active < 1) {
         cudaGetLastError();
         return W4A4_ERR_CUDA;
     }
-    const int clusters = tiles < active ? tiles : active;
+    const int clusters = ntl < active ? ntl : active;
     cfg.gridDim = dim3(unsigned(clusters * KS));
     cfg.numAttrs = add_pdl_attr(attr, 1);
-    if (cudaLaunchKernelEx(&cfg, kern, ws, packed, cs, bias, M, N, K, r, Y, P, KS, silu_I) != cudaSuccess) {
+    if (cudaLaunchKernelEx(&cfg, kern, ws, packed, cs, bias, M, N, K, r, Y, P, KS, silu_I, t_lo, t_hi) !=
+        cudaSuccess) {
         cudaGetLastError();
         return W4A4_ERR_CUDA;
     }
@@ -891,19 +898,24 @@ static int resident_clusters(int ks) {
     return cache[dev][ks];
 }
 
-// Schedule: the cheapest of round-robin tiles, split-K over clusters and
+// Schedule: the cheapest of round-robin tiles, split-K over clusters, the full
+// rounds round-robin followed by the last round alone split over K, and
 // stream-K, in units of one job's time: rounds of tiles x jobs per tile;
-// rounds x (jobs / KS + the cluster reduction, about 1.5 jobs); or the longest
-// run of jobs + the hand-over of a tile's sums (about 1 job).  Rank 128 LoRA
+// rounds x (jobs / KS + the cluster reduction, about 1.5 jobs); (rounds - 1) x
+// jobs + jobs / KS + 1.5 + a second launch (its wait for the first and a
+// tile's fixed costs, about 5 jobs: measured, a K = 1024 tile of 8 jobs lost
+// to it), for a last round at most half full; or the longest run of jobs + the
+// hand-over of a tile's sums (about 1 job).  Rank 128 LoRA
 // operands leave no room for the cluster reduction buffer; stream-K needs the
 // hand-over area of the workspace.
 struct TcSchedule {
-    int ks, sk_ctas;  // sk_ctas > 0: stream-K over that many CTAs
+    int ks, sk_ctas;       // sk_ctas > 0: stream-K over that many CTAs
+    int tail_ks, tail_lo;  // tail_ks > 1: tiles [0, tail_lo) round-robin, then the rest split over tail_ks
 };
 static TcSchedule tc_schedule(int M, int N, int K, int r, bool sk_room) {
     const int tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
     const int jobs = (K / kGroup + GPJ - 1) / GPJ;
-    TcSchedule best_s{1, 0};
+    TcSchedule best_s{1, 0, 1, 0};
     if (tiles <= 0) return best_s;
     const int sms = device_sm_count();
     double best = double((tiles + sms - 1) / sms) * jobs;
@@ -913,7 +925,18 @@ static TcSchedule tc_schedule(int M, int N, int K, int r, bool sk_room) {
         const double cost = double((tiles + cl - 1) / cl) * (double((jobs + ks - 1) / ks) + 1.5);
         if (cost < best) {
             best = cost;
-            best_s = TcSchedule{ks, 0};
+            best_s = TcSchedule{ks, 0, 1, 0};
+        }
+    }
+    const int rounds = (tiles + sms - 1) / sms, rem = tiles - (rounds - 1) * sms;
+    if (rounds >= 2 && 2 * rem <= sms && r <= 32) {
+        for (int ks = 2; ks <= MAX_KS && ks <= jobs && ks * rem <= sms; ++ks) {
+            if (resident_clusters(ks) < rem) continue;
+            const double cost = double(rounds - 1) * jobs + double((jobs + ks - 1) / ks) + 1.5 + 5.0;
+            if (cost < best) {
+                best = cost;
+                best_s = TcSchedule{1, 0, ks, (rounds - 1) * sms};
+            }
         }
     }
     if (sk_room && (long long)tiles * jobs < (1ll << 31) / kStreamKSlots) {
@@ -921,7 +944,7 @@ static TcSchedule tc_schedule(int M, int N, int K, int r, bool sk_room) {
         long long p = sms < kStreamKSlots ? sms : kStreamKSlots;
         if (p > units) p = units;
         const double cost = double((units + p - 1) / p) + 1.0;
-        if (cost < best) best_s = TcSchedule{1, int(p)};
+        if (cost < best) best_s = TcSchedule{1, int(p), 1, 0};
     }
     return best_s;
 }
@@ -937,6 +960,20 @@ static w4a4_status dispatch_tc(const uint8_t* ws, const uint8_t* packed, const u
                                                      silu_I);
         return launch_impl<4, false, true, DUMP>(ws, packed, colscale, bias, M, N, K, r, Y, P, 1, s, sc.sk_ctas,
                                                  silu_I);
+    }
+    if (sc.tail_ks > 1) {
+        // the full rounds, then the last round's tiles split over K in a launch of their own
+        w4a4_status st =
+            launch_impl<4, false, false, DUMP>(ws, packed, colscale, bias, M, N, K, r, Y, P, 1, s, 0, silu_I, 0, sc.tail_lo);
+        if (st != W4A4_OK) return st;
+        st = launch_impl<3, true, false, DUMP>(ws, packed, colscale, bias, M, N, K, r, Y, P, sc.tail_ks, s, 0, silu_I,
+                                               sc.tail_lo, -1);
+        const int tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
+        set_dispatch("gemm_tc tcgen05.f8f6f4 tile=%dx%d groups/job=%d stages=4 tiles=%d: %d round-robin, last %d "
+                     "split-K=%d (cluster)%s%s%s", BM, BN, GPJ, tiles, sc.tail_lo, tiles - sc.tail_lo, sc.tail_ks,
+                     n_fastest(M, N, K) ? " N-tiles-fastest" : "", silu_I ? " silu(gate)*up" : "",
+                     DUMP ? " (partials dump)" : "");
+        return st;
     }
     if (sc.ks > 1)
         return launch_impl<3, true, false, DUMP>(ws, packed, colscale, bias, M, N, K, r, Y, P, sc.ks, s, 0, silu_I);
