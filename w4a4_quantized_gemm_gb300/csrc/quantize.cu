@@ -322,17 +322,19 @@ template <int R, bool NORM>
 w4a4_status launch_q(const uint16_t* X, int ld_x, const uint8_t* packed, int M, int K, uint8_t* ws,
                      cudaStream_t s) {
     const int G = K / kGroup;
-    // split K over a (small) cluster: one group per warp where that takes at most
-    // two CTAs, else about two groups per warp (larger clusters cost more in
-    // their reduction than they gain)
+    // split K over a (small) cluster: one group per warp up to clusters of six (at
+    // M = 700, K = 2048 and 3072: 4.4 and 4.8 us against 4.9 and 4.9 with two groups
+    // per warp), about two groups per warp beyond
     // (with few row blocks -- decode -- the SMs are idle anyway: one group per warp
     // up to the largest cluster)
-    // (with many row blocks -- prefill -- about eight groups per warp: at M = 8192
-    // this takes K = 4096 from 82 to 51 us and K = 14336 from 258 to 176 us)
+    // (with many row blocks -- prefill -- one CTA per row block, its warps taking
+    // every eighth group: two such CTAs share an SM, and at M = 8192 this is the
+    // fastest split for K = 4096 and K = 14336: 36 and 105 us, against 42 / 110
+    // with clusters of two)
     const int row_blocks = (M + kRows - 1) / kRows;
     int CK = (G + kWarps - 1) / kWarps;
-    if (CK > 2 && row_blocks > 8) CK = (G + 2 * kWarps - 1) / (2 * kWarps);
-    if (row_blocks >= kPrefillRowBlocks) CK = (G + 8 * kWarps - 1) / (8 * kWarps);
+    if (CK > 6 && row_blocks > 8) CK = (G + 2 * kWarps - 1) / (2 * kWarps);
+    if (row_blocks >= kPrefillRowBlocks) CK = 1;
     if (CK > kMaxCluster) CK = kMaxCluster;
     if (CK < 1) CK = 1;
     cudaLaunchConfig_t cfg = {};
