@@ -281,19 +281,19 @@ def kernel_source_hash(name: str) -> str:
 # counters no longer describe it and traffic is reported as null.
 NCU_TRAFFIC = {
     # the four decoder-layer GEMM launches (qkv, o, gate_up, down) at M = 700, one launch each,
-    # read from HBM (24 input replicas cycled): 3,494,144 + 3,066,368 + 4,747,520 + 4,508,416 bytes;
-    # Y stays in L2 within a launch, so the write counter is near zero (profiles/gemm_tc_traffic_decoder_layer_m700.md)
-    (WORKLOAD, "860c8d9177f66133"): {
-        "bytes_per_pass": 15817728,
-        "per_linear": {"qkv": 3495168, "o": 3066368, "gate_up": 4747776, "down": 4508416},
+    # read from HBM (24 input replicas cycled): 3,501,824 + 3,066,112 + 4,747,520 + 4,508,416 bytes read,
+    # 512 written; Y stays in L2 within a launch (profiles/gemm_tc_traffic_decoder_layer_m700.md)
+    (WORKLOAD, "b7ecf7ca82e1c185"): {
+        "bytes_per_pass": 15824384,
+        "per_linear": {"qkv": 3502336, "o": 3066112, "gate_up": 4747520, "down": 4508416},
         "source": "ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum, one launch per linear "
                   "(profiles/gemm_tc_traffic_decoder_layer_m700.md)"},
     # the M = 8192 GEMMs, two launches per linear (the full rounds, then the last round split over K):
-    # 4096 -> 14336 74.41 + 14.70 MB read, 197.75 MB written; 14336 -> 4096 160.56 + 37.76 MB read,
-    # 51.39 MB written (profiles/gemm_tc_prefill_m8192.md)
-    (PREFILL_WORKLOAD, "860c8d9177f66133"): {
-        "bytes_per_pass": 286869760 + 249710080,
-        "per_linear": {"gate_up_style": 286869760, "down_style": 249710080},
+    # 4096 -> 14336 75.59 + 14.70 MB read, 198.38 MB written; 14336 -> 4096 160.56 + 37.77 MB read,
+    # 51.85 MB written (profiles/gemm_tc_prefill_m8192.md)
+    (PREFILL_WORKLOAD, "b7ecf7ca82e1c185"): {
+        "bytes_per_pass": 288672768 + 250180352,
+        "per_linear": {"gate_up_style": 288672768, "down_style": 250180352},
         "source": "ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum, both launches of each linear "
                   "(profiles/gemm_tc_prefill_m8192.md)"},
 }

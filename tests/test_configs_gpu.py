@@ -5,7 +5,8 @@ decoder-layer linears at M = 700, the small-M sweep at K = N = 4096); for the
 M = 8192 prefill shapes, whole output rows (every column) at the first and the
 last row of every 128-row tile, so that every output tile is compared.
 Bit-exact per-group partial sums from the kernel and schedule AUTO runs: the
-four decoder-layer linears (round-robin tiles and split-K clusters), the
+four decoder-layer linears (whole tiles with the last round split over K in
+the same launch, split-K clusters, round-robin tiles), the
 small-M sweep at M <= 32 (the tcgen05 small-M kernel), and the stream-K
 schedule on the qkv linear.
 """
@@ -73,6 +74,8 @@ def test_decoder_layer_partials_bitexact(name):
     assert "gemm_tc" in d
     if name in ("o", "down"):
         assert "split-K=" in d, d  # N = 1024: the cluster split-K schedule
+    if name == "qkv":
+        assert "split-K=2 in the same launch" in d, d  # 192 tiles: 152 whole, the last 40 split over K
 
 
 def test_qkv_m700_stream_k_partials_bitexact():
@@ -114,12 +117,16 @@ def test_prefill_m8192_every_tile(name):
     assert np.array_equal(sA.cpu().numpy()[rows], sA_ref)
 
 
-@pytest.mark.parametrize("M,K,N,r", [(256, 2048, 10240, 32), (1280, 1536, 2048, 16)], ids=lambda v: str(v))
-def test_thin_last_round_runs_split_over_k(M, K, N, r):
-    """A last round of tiles at most half the SMs, with enough jobs per tile, runs as a
-    launch of its own with split-K (the full rounds round-robin before it): every output
-    tile, those of both launches, on the first and last row of every 128-row tile;
-    the group partials of the same schedule bit-exact on those rows."""
+@pytest.mark.parametrize("M,K,N,r,mode", [(256, 1024, 10240, 32, "inline"), (1280, 1536, 2048, 16, "inline"),
+                                            (256, 4096, 10240, 32, "second")], ids=lambda v: str(v))
+def test_thin_last_round_runs_split_over_k(M, K, N, r, mode):
+    """A last round of tiles that fills at most half the SMs runs split over K after
+    the full rounds of whole tiles: in the same launch on clusters of two when the
+    tiles are short ("inline"), or as a launch of its own on larger clusters when
+    they are long ("second").  Every output tile, on the first and last row of
+    every 128-row tile; the group partials of the same schedule bit-exact on those
+    rows."""
+    expect = "split-K=2 in the same launch" if mode == "inline" else "round-robin, last"
     c = make_linear_case(M, K, N, r, seed=M + N)
     t = to_dev(c)
     packed = pack(c, t)
@@ -127,12 +134,13 @@ def test_thin_last_round_runs_split_over_k(M, K, N, r):
     Y = run_linear(c, t, packed, ws, w4.KERNEL_AUTO)
     d = w4.w4a4_last_dispatch()
     assert w4.w4a4_device_status() == 0
-    assert "round-robin, last" in d and "split-K=" in d, d
+    assert expect in d, d
     rows = np.unique(np.r_[np.arange(0, c.M, 128), np.minimum(np.arange(127, c.M + 127, 128), c.M - 1)])
     y = oracle.linear_rows(c.X, c.W, c.L_down, c.L_up, c.colscale, c.bias, rows)
     check_tol(Y[torch.from_numpy(rows).cuda()], y, f"thin last round {M}x{K}x{N}")
     P = w4.w4a4_debug_group_partials(ws, packed, M, N, K, r, w4.KERNEL_AUTO)
-    assert "round-robin, last" in w4.w4a4_last_dispatch()
+    assert expect in w4.w4a4_last_dispatch()
+    assert w4.w4a4_device_status() == 0
     qA, _ = oracle.quantize_act(c.X[rows])
     qW, _ = oracle.quantize_weights(c.W)
-    assert np.array_equal(P.cpu().numpy()[rows], oracle.group_partials(qA, qW))
+    assert np.array_equal(P[torch.from_numpy(rows).cuda()].cpu().numpy(), oracle.group_partials(qA, qW))

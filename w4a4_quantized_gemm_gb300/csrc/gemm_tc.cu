@@ -138,12 +138,13 @@ static_assert(smem_map(3, 2, true).total <= 227 * 1024, "3 stages + the reductio
 
 // DUMP: the debug variant of a schedule, which also writes every group's exact
 // integer product to P and stores no Y (colscale and bias are not read).
-template <int S, bool SPLIT, bool SK, bool DUMP>
+// MIXED (with SPLIT): tiles below t_split run whole, the rest split over K.
+template <int S, bool SPLIT, bool SK, bool DUMP, bool MIXED>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_tc_kernel(const uint8_t* __restrict__ ws, const uint8_t* __restrict__ packed,
                    const uint16_t* __restrict__ colscale, const uint16_t* __restrict__ bias, int M, int N, int K,
                    int r, uint16_t* __restrict__ Y, int32_t* __restrict__ P, int KS, int silu_I, int t_lo,
-                   int t_hi) {
+                   int t_hi, int t_split) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -156,6 +157,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     // otherwise every CTA is its own "cluster" of one
     const int kr = SPLIT ? int(cluster_ctarank()) : 0;
     if (!SPLIT) KS = 1;
+    if (MIXED) KS = 2;  // (a compile-time split keeps the epilogue within its registers)
     const int cid = int(blockIdx.x) / KS, ncl = int(gridDim.x) / KS;
     const int j0 = kr * J / KS, j1 = (kr + 1) * J / KS;
     const int RPB = r / 16;  // LoRA operand planes held in shared memory
@@ -165,10 +167,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int MT = AL.MT, NT = (N + BN - 1) / BN;
     const int tiles = MT * NT;
     const bool nf = n_fastest(M, N, K);
-    // Work is walked as segments (tile t, jobs [a, b)).  Round-robin: CTA (or
-    // cluster) cid takes tiles t_lo + cid, t_lo + cid + ncl, ... below t_hi with jobs
-    // [j0, j1) (a launch may cover a range of the tiles: the last, thin round of tiles
-    // can be launched on its own with split-K).  Stream-K:
+    // Work is walked as segments (tile t, jobs [a, b)).  Round-robin: tiles
+    // [t_lo, t_split) are whole, CTA p taking t_lo + p, t_lo + p + gridDim.x, ...;
+    // tiles [t_split, t_hi) are split over K, cluster cid taking t_split + cid,
+    // t_split + cid + ncl, ... with jobs [j0, j1) on rank kr.  A launch may cover a
+    // range of the tiles, and a split-K launch may run its full rounds whole and
+    // only the last, thin round split.  Stream-K:
     // the tiles x J jobs, tile-major, are cut into gridDim.x equal runs, CTA p
     // taking run p; a tile cut between CTAs is finished by the CTA holding its
     // first job, which adds the later CTAs' fp32 sums handed over in the workspace.
@@ -176,8 +180,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int units = tiles * J;
     const int sk_ctas = int(gridDim.x);
     auto sk_start = [&](int p) -> int { return int((long long)p * units / sk_ctas); };
-    const int u_begin = SK ? sk_start(int(blockIdx.x)) : t_lo + cid;
+    // (the host passes t_lo <= t_split <= t_hi; only MIXED reads it)
+    const int u_begin = SK       ? sk_start(int(blockIdx.x))
+                        : !MIXED ? t_lo + cid
+                                 : (t_lo + int(blockIdx.x) < t_split ? t_lo + int(blockIdx.x) : t_split + cid);
     const int u_end = SK ? sk_start(int(blockIdx.x) + 1) : t_hi;
+    // segment u: tile t, jobs [a, b); split over the cluster or whole
+    auto split_seg = [&](int u) -> bool { return SPLIT && (!MIXED || u >= t_split); };
     auto seg_at = [&](int u, int& t, int& a, int& b) {
         if (SK) {
             t = u / J;
@@ -185,13 +194,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             b = min(J, a + (u_end - u));
         } else {
             t = u;
-            a = j0;
-            b = j1;
+            a = split_seg(u) ? j0 : 0;
+            b = split_seg(u) ? j1 : J;
         }
     };
-    auto seg_next = [&](int u, int a, int b) -> int { return SK ? u + (b - a) : u + ncl; };
-    // the LoRA term is added once per tile: by split rank 0, or by the segment holding job 0
-    auto lora_planes = [&](int a) -> int { return (SK ? a == 0 : kr == 0) ? RPB : 0; };
+    auto seg_next = [&](int u, int a, int b) -> int {
+        if (SK) return u + (b - a);
+        if (!MIXED || u >= t_split) return u + ncl;
+        const int nu = u + int(gridDim.x);
+        return nu < t_split ? nu : t_split + cid;
+    };
+    // the LoRA term is added once per tile: by a whole tile's CTA, by split rank 0, or
+    // by the stream-K segment holding job 0
+    auto lora_planes = [&](int u, int a) -> int { return (SK ? a == 0 : (!split_seg(u) || kr == 0)) ? RPB : 0; };
     const Map mp = smem_map(S, RPB, SPLIT);
 
     auto full = [&](int s) { return base + mp.BAR + 8u * s; };             // copies landed (producers + tx)
@@ -280,7 +295,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         int t = 0, a = 0, b = 0;
         for (int u = u_begin; u < u_end && ok; u = seg_next(u, a, b)) {
             seg_at(u, t, a, b);
-            const int RP = lora_planes(a);
+            const int RP = lora_planes(u, a);
             int mt, nt;
             tile_coords(t, MT, NT, nf, mt, nt);
             const int n0 = nt * BN;
@@ -352,7 +367,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         int t = 0, a = 0, b = 0;
         for (int u = u_begin; u < u_end && ok; u = seg_next(u, a, b)) {
             seg_at(u, t, a, b);
-            const int RP = lora_planes(a);
+            const int RP = lora_planes(u, a);
             if (RP > 0) {
                 // the LoRA product takes a job buffer of its own (first 128 columns)
                 const uint32_t bf = jc % NPB, tph = (jc / NPB) & 1u;
@@ -477,7 +492,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         int t = 0, a = 0, b = 0;
         for (int u = u_begin; u < u_end && ok; u = seg_next(u, a, b)) {
             seg_at(u, t, a, b);
-            const int RP = lora_planes(a);
+            const int RP = lora_planes(u, a);
             int mt, nt;
             tile_coords(t, MT, NT, nf, mt, nt);
             const int n0 = nt * BN;
@@ -488,7 +503,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             // [cs gate 0..15 | cs up | bias gate | bias up]
             uint8_t* const cbw = gbase + mp.CB + uint32_t(warp) * kCB;
             // (only warps that store this segment: not a stream-K hand-over, not a split-K sender)
-            const bool stores = has_y && !(SK && a > 0) && !(SPLIT && ((warp >> 2) % KS) != kr);
+            const bool stores = has_y && !(SK && a > 0) && !(split_seg(u) && ((warp >> 2) % KS) != kr);
             if (stores && lane < 8) {
                 const uint16_t* src = nullptr;
                 if (silu_I > 0) {
@@ -644,7 +659,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     if (!ok) break;
                 }
             }
-            if constexpr (SPLIT) {
+            if (split_seg(u)) {
                 const int sl = warp >> 2, owner = sl % KS;
                 if (owner != kr) {
                     // send this slice's sums to its owner once it has consumed the previous ones
@@ -699,8 +714,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         for (int src_rank = 0; src_rank < KS; ++src_rank)
                             if (src_rank != kr) mbar_arrive_remote(mapa_shared(red_empty, uint32_t(src_rank)));
                 }
+                ++tc;  // (counts the split segments only: both ranks walk the same ones)
             }
-            ++tc;
             if constexpr (has_y) {
                 cp_async_wait<0>();  // this warp's colscale / bias chunks
                 __syncwarp();
@@ -775,22 +790,22 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 }
 
 // Registers per thread the kernel was compiled for (cached per instantiation).
-template <int S, bool SPLIT, bool SK, bool DUMP>
+template <int S, bool SPLIT, bool SK, bool DUMP, bool MIXED>
 int launch_regs() {
     static int regs = -1;
     if (regs < 0) {
         cudaFuncAttributes fa{};
-        if (cudaFuncGetAttributes(&fa, gemm_tc_kernel<S, SPLIT, SK, DUMP>) != cudaSuccess) return 0;
+        if (cudaFuncGetAttributes(&fa, gemm_tc_kernel<S, SPLIT, SK, DUMP, MIXED>) != cudaSuccess) return 0;
         regs = fa.numRegs;
     }
     return regs;
 }
 
-template <int S, bool SPLIT, bool SK, bool DUMP>
+template <int S, bool SPLIT, bool SK, bool DUMP, bool MIXED = false>
 w4a4_status launch_impl(const uint8_t* ws, const uint8_t* packed, const uint16_t* cs, const uint16_t* bias, int M,
                         int N, int K, int r, uint16_t* Y, int32_t* P, int KS, cudaStream_t s, int sk_ctas = 0,
-                        int silu_I = 0, int t_lo = 0, int t_hi = -1) {
-    auto kern = gemm_tc_kernel<S, SPLIT, SK, DUMP>;
+                        int silu_I = 0, int t_lo = 0, int t_hi = -1, int t_split = -1) {
+    auto kern = gemm_tc_kernel<S, SPLIT, SK, DUMP, MIXED>;
     static int attr_done[64] = {0};
     int dev = 0;
     cudaGetDevice(&dev);
@@ -802,7 +817,7 @@ w4a4_status launch_impl(const uint8_t* ws, const uint8_t* packed, const uint16_t
         attr_done[dev] = 1;
     }
     // the setmaxnreg split needs the launch-time register pool to cover it
-    if (launch_regs<S, SPLIT, SK, DUMP>() * NUM_THREADS <
+    if (launch_regs<S, SPLIT, SK, DUMP, MIXED>() * NUM_THREADS <
         NUM_EPI_WARPS * 32 * EPI_REGS + (NUM_THREADS - NUM_EPI_WARPS * 32) * OTHER_REGS)
         return W4A4_ERR_CUDA;
     const int MT = (M + BM - 1) / BM, NT = (N + BN - 1) / BN;
@@ -820,7 +835,7 @@ w4a4_status launch_impl(const uint8_t* ws, const uint8_t* packed, const uint16_t
         cfg.blockDim = dim3(NUM_THREADS);
         cfg.dynamicSmemBytes = smem;
         cfg.stream = s;
-        if (cudaLaunchKernelEx(&cfg, kern, ws, packed, cs, bias, M, N, K, r, Y, P, 1, silu_I, t_lo, t_hi) !=
+        if (cudaLaunchKernelEx(&cfg, kern, ws, packed, cs, bias, M, N, K, r, Y, P, 1, silu_I, t_lo, t_hi, t_hi) !=
             cudaSuccess) {
             cudaGetLastError();
             return W4A4_ERR_CUDA;
@@ -848,10 +863,15 @@ w4a4_status launch_impl(const uint8_t* ws, const uint8_t* packed, const uint16_t
         cudaGetLastError();
         return W4A4_ERR_CUDA;
     }
-    const int clusters = ntl < active ? ntl : active;
+    // t_split > t_lo: the tiles below it run whole, one per CTA and round, on every
+    // resident cluster's CTAs; the rest split over K, one per cluster and round
+    const bool mixed = MIXED && t_split > t_lo && t_split < t_hi;
+    if (!mixed) t_split = t_lo;
+    const int split_tiles = t_hi - t_split;
+    const int clusters = mixed ? active : (split_tiles < active ? split_tiles : active);
     cfg.gridDim = dim3(unsigned(clusters * KS));
     cfg.numAttrs = add_pdl_attr(attr, 1);
-    if (cudaLaunchKernelEx(&cfg, kern, ws, packed, cs, bias, M, N, K, r, Y, P, KS, silu_I, t_lo, t_hi) !=
+    if (cudaLaunchKernelEx(&cfg, kern, ws, packed, cs, bias, M, N, K, r, Y, P, KS, silu_I, t_lo, t_hi, t_split) !=
         cudaSuccess) {
         cudaGetLastError();
         return W4A4_ERR_CUDA;
@@ -871,7 +891,7 @@ static int resident_clusters(int ks) {
     cudaGetDevice(&dev);
     if (dev < 0 || dev >= 64) return 0;
     if (cache[dev][ks] == 0) {
-        auto kern = gemm_tc_kernel<3, true, false, false>;
+        auto kern = gemm_tc_kernel<3, true, false, false, false>;
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  int(smem_map(3, 2, true).total)) != cudaSuccess) {
             cudaGetLastError();
@@ -899,23 +919,32 @@ static int resident_clusters(int ks) {
 }
 
 // Schedule: the cheapest of round-robin tiles, split-K over clusters, the full
-// rounds round-robin followed by the last round alone split over K, and
-// stream-K, in units of one job's time: rounds of tiles x jobs per tile;
-// rounds x (jobs / KS + the cluster reduction, about 1.5 jobs); (rounds - 1) x
-// jobs + jobs / KS + 1.5 + a second launch (its wait for the first and a
-// tile's fixed costs, about 5 jobs: measured, a K = 1024 tile of 8 jobs lost
-// to it), for a last round at most half full; or the longest run of jobs + the
-// hand-over of a tile's sums (about 1 job).  Rank 128 LoRA
-// operands leave no room for the cluster reduction buffer; stream-K needs the
-// hand-over area of the workspace.
+// rounds round-robin followed by the last round split over K (in the same
+// launch on clusters of two, or alone in a second launch on clusters sized to
+// fill the SMs), and stream-K, in units of one job's time:
+//  - round-robin: rounds of tiles x jobs per tile;
+//  - split-K: rounds x (jobs / KS + the cluster reduction, about 1.5 jobs);
+//  - last round split in the same launch, for a last round of at most one tile
+//    per cluster: (rounds - 1) x jobs x 1.04 + jobs / 2 + 1.5 (the factor: the
+//    three-stage ring that the reduction buffer leaves room for, measured 4%
+//    slower per job on long tiles);
+//  - last round split in a second launch, for a last round at most half full:
+//    (rounds - 1) x jobs + jobs / KS + 1.5 + about 5 jobs for the second launch
+//    (its wait for the first and a tile's fixed costs: measured, a K = 1024
+//    tile of 8 jobs lost to it);
+//  - stream-K: the longest run of jobs + the hand-over of a tile's sums (about
+//    1 job).
+// Rank 128 LoRA operands leave no room for the cluster reduction buffer;
+// stream-K needs the hand-over area of the workspace.
 struct TcSchedule {
     int ks, sk_ctas;       // sk_ctas > 0: stream-K over that many CTAs
     int tail_ks, tail_lo;  // tail_ks > 1: tiles [0, tail_lo) round-robin, then the rest split over tail_ks
+    bool tail_inline;      // ... in the same launch (clusters of two), else in a second launch
 };
 static TcSchedule tc_schedule(int M, int N, int K, int r, bool sk_room) {
     const int tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
     const int jobs = (K / kGroup + GPJ - 1) / GPJ;
-    TcSchedule best_s{1, 0, 1, 0};
+    TcSchedule best_s{1, 0, 1, 0, false};
     if (tiles <= 0) return best_s;
     const int sms = device_sm_count();
     double best = double((tiles + sms - 1) / sms) * jobs;
@@ -925,7 +954,18 @@ static TcSchedule tc_schedule(int M, int N, int K, int r, bool sk_room) {
         const double cost = double((tiles + cl - 1) / cl) * (double((jobs + ks - 1) / ks) + 1.5);
         if (cost < best) {
             best = cost;
-            best_s = TcSchedule{ks, 0, 1, 0};
+            best_s = TcSchedule{ks, 0, 1, 0, false};
+        }
+    }
+    const int cl2 = r <= 32 && jobs >= 2 ? resident_clusters(2) : 0;
+    if (cl2 >= 1 && 2 * cl2 <= sms) {
+        const int grid = 2 * cl2, rounds = (tiles + grid - 1) / grid, rem = tiles - (rounds - 1) * grid;
+        if (rounds >= 2 && rem <= cl2) {
+            const double cost = 1.04 * double(rounds - 1) * jobs + double((jobs + 1) / 2) + 1.5;
+            if (cost < best) {
+                best = cost;
+                best_s = TcSchedule{1, 0, 2, (rounds - 1) * grid, true};
+            }
         }
     }
     const int rounds = (tiles + sms - 1) / sms, rem = tiles - (rounds - 1) * sms;
@@ -935,7 +975,7 @@ static TcSchedule tc_schedule(int M, int N, int K, int r, bool sk_room) {
             const double cost = double(rounds - 1) * jobs + double((jobs + ks - 1) / ks) + 1.5 + 5.0;
             if (cost < best) {
                 best = cost;
-                best_s = TcSchedule{1, 0, ks, (rounds - 1) * sms};
+                best_s = TcSchedule{1, 0, ks, (rounds - 1) * sms, false};
             }
         }
     }
@@ -944,7 +984,7 @@ static TcSchedule tc_schedule(int M, int N, int K, int r, bool sk_room) {
         long long p = sms < kStreamKSlots ? sms : kStreamKSlots;
         if (p > units) p = units;
         const double cost = double((units + p - 1) / p) + 1.0;
-        if (cost < best) best_s = TcSchedule{1, int(p), 1, 0};
+        if (cost < best) best_s = TcSchedule{1, int(p), 1, 0, false};
     }
     return best_s;
 }
@@ -960,6 +1000,17 @@ static w4a4_status dispatch_tc(const uint8_t* ws, const uint8_t* packed, const u
                                                      silu_I);
         return launch_impl<4, false, true, DUMP>(ws, packed, colscale, bias, M, N, K, r, Y, P, 1, s, sc.sk_ctas,
                                                  silu_I);
+    }
+    if (sc.tail_ks > 1 && sc.tail_inline) {
+        // one launch on clusters of two: the full rounds whole, the last round split over K
+        const w4a4_status st = launch_impl<3, true, false, DUMP, true>(ws, packed, colscale, bias, M, N, K, r, Y, P, 2,
+                                                                       s, 0, silu_I, 0, -1, sc.tail_lo);
+        const int tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
+        set_dispatch("gemm_tc tcgen05.f8f6f4 tile=%dx%d groups/job=%d stages=3 tiles=%d: %d whole, last %d "
+                     "split-K=2 in the same launch (cluster)%s%s%s", BM, BN, GPJ, tiles, sc.tail_lo, tiles - sc.tail_lo,
+                     n_fastest(M, N, K) ? " N-tiles-fastest" : "", silu_I ? " silu(gate)*up" : "",
+                     DUMP ? " (partials dump)" : "");
+        return st;
     }
     if (sc.tail_ks > 1) {
         // the full rounds, then the last round's tiles split over K in a launch of their own
