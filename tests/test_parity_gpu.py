@@ -221,6 +221,46 @@ def test_output_guard_regions_untouched(kernel):
     check_tol(Y, y, "guarded")
 
 
+@pytest.mark.parametrize("silu,N", [(False, 512), (False, 528), (True, 512)], ids=["plain", "plain-N528", "silu"])
+def test_tiled_store_alignment_same_bits(silu, N):
+    """The tiled kernel stores 32 bytes of an output row at a time when the output
+    is 32-byte aligned (rows are N x 2 bytes with N a multiple of 16, and N/2 x 2
+    bytes with N a multiple of 32 for the SiLU epilogue), else 16 bytes at a
+    time: both give the same bits, within tolerance of the oracle, and nothing
+    outside the output is written."""
+    M, K, r = 200, 256, 32
+    c = make_linear_case(M, K, N, r, seed=21 + N)
+    t = to_dev(c)
+    if silu:
+        packed = torch.empty(w4.packed_weights_bytes(N, K, r), dtype=torch.uint8, device="cuda")
+        w4.w4a4_pack_weights_gate_up(t["W"], t["L_down"], t["L_up"], packed, r)
+    else:
+        packed = pack(c, t)
+    ws = quantize(c, t, packed)
+    cols = N // 2 if silu else N
+    outs = []
+    for off in (0, 8):  # fp16 elements past a 256-byte aligned base: 0 and 16 bytes
+        buf = torch.full((off + M * cols + 64,), 0x5A5A, dtype=torch.int16, device="cuda")
+        Y = buf[off:off + M * cols].view(torch.float16).view(M, cols)
+        assert (Y.data_ptr() % 32 == 0) == (off == 0)
+        if silu:
+            w4.w4a4_linear_silu_mul(ws, packed, t["colscale"], t["bias"], Y, K, r)
+        else:
+            w4.w4a4_linear(ws, packed, t["colscale"], t["bias"], Y, K, r, w4.KERNEL_TC)
+        torch.cuda.synchronize()
+        assert "gemm_tc" in w4.w4a4_last_dispatch()
+        assert w4.w4a4_device_status() == 0
+        b = buf.cpu().numpy()
+        assert np.all(b[:off] == 0x5A5A) and np.all(b[off + M * cols:] == 0x5A5A)
+        outs.append(Y.cpu())
+    assert torch.equal(outs[0].view(torch.int16), outs[1].view(torch.int16))
+    if silu:
+        y = oracle.silu_mul_linear(c.X, c.W, c.L_down, c.L_up, c.colscale, c.bias)
+    else:
+        y = oracle.linear(c.X, c.W, c.L_down, c.L_up, c.colscale, c.bias)
+    check_tol(outs[0], y, "store alignment")
+
+
 def test_dispatch_is_logged():
     c = make_linear_case(3, 128, 32, 16, seed=1)
     t = to_dev(c)

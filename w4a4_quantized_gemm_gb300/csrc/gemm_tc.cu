@@ -162,6 +162,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int j0 = kr * J / KS, j1 = (kr + 1) * J / KS;
     const int RPB = r / 16;  // LoRA operand planes held in shared memory
     constexpr bool has_y = !DUMP;
+    // Y 32-byte aligned: every 16-column chunk of a row is a 32-byte store (rows are
+    // N x 2 bytes, N a multiple of 16); the API guarantees 16 bytes only
+    const bool y32 = (reinterpret_cast<uintptr_t>(Y) & 31u) == 0;
     const ActLayout AL = act_layout(M, K, r);
     const PackedLayout PL = packed_layout(N, K, r);
     const int MT = AL.MT, NT = (N + BN - 1) / BN;
@@ -725,13 +728,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     const int hb = (n0 >> 1) + (c0 >> 1);
                     if (hb < silu_I) {
                         const uint4* cbv = reinterpret_cast<const uint4*>(cbw);
-                        uint4* dst = reinterpret_cast<uint4*>(Y + size_t(m) * silu_I + hb);
+                        uint16_t* const dst = Y + size_t(m) * silu_I + hb;
+                        uint32_t hw[8];
 #pragma unroll
                         for (int q8 = 0; q8 < 2; ++q8) {
                             const uint4 csg = cbv[q8], csu = cbv[2 + q8], bg = cbv[4 + q8], bu = cbv[6 + q8];
                             const uint32_t w_cg[4] = {csg.x, csg.y, csg.z, csg.w}, w_cu[4] = {csu.x, csu.y, csu.z, csu.w};
                             const uint32_t w_bg[4] = {bg.x, bg.y, bg.z, bg.w}, w_bu[4] = {bu.x, bu.y, bu.z, bu.w};
-                            uint32_t hw[4];
 #pragma unroll
                             for (int j = 0; j < 4; ++j) {
                                 const float2 c2g = __half22float2(*reinterpret_cast<const __half2*>(&w_cg[j]));
@@ -745,34 +748,49 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                                 // (relative error ~1e-6; e^-g = inf gives -0)
                                 const __half2 h = __floats2half2_rn(__fdividef(g0, 1.0f + __expf(-g0)) * u0,
                                                                     __fdividef(g1, 1.0f + __expf(-g1)) * u1);
-                                hw[j] = *reinterpret_cast<const uint32_t*>(&h);
+                                hw[q8 * 4 + j] = *reinterpret_cast<const uint32_t*>(&h);
                             }
-                            dst[q8] = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+                        }
+                        if (y32) {  // (rows of H are N/2 x 2 bytes, N a multiple of 32)
+                            st_global_v8(dst, hw);
+                        } else {
+                            reinterpret_cast<uint4*>(dst)[0] = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+                            reinterpret_cast<uint4*>(dst)[1] = make_uint4(hw[4], hw[5], hw[6], hw[7]);
                         }
                     }
                 } else if (m < M) {
+                    // 16 columns (32 bytes) per store: N is a multiple of 16, so a chunk that
+                    // starts below N ends within it
                     const uint4* cbv = reinterpret_cast<const uint4*>(cbw);
 #pragma unroll
-                    for (int ch = 0; ch < EPI_COLS / 8; ++ch) {
-                        const int n = n0 + c0 + ch * 8;
+                    for (int c16 = 0; c16 < EPI_COLS / 16; ++c16) {
+                        const int n = n0 + c0 + c16 * 16;
                         if (n < N) {
-                            const uint4 csv = cbv[ch];
-                            const uint4 bsv = cbv[4 + ch];
-                            const uint32_t cw[4] = {csv.x, csv.y, csv.z, csv.w};
-                            const uint32_t bw[4] = {bsv.x, bsv.y, bsv.z, bsv.w};
-                            uint32_t out[4];
+                            uint32_t out[8];
 #pragma unroll
-                            for (int j = 0; j < 4; ++j) {
-                                const float2 cs2 = __half22float2(*reinterpret_cast<const __half2*>(&cw[j]));
-                                const float2 b2 = __half22float2(*reinterpret_cast<const __half2*>(&bw[j]));
-                                const float2 av = f2_unpack(acc[ch * 4 + j]);
-                                const float y0 = fmaf(cs2.x, av.x, b2.x);
-                                const float y1 = fmaf(cs2.y, av.y, b2.y);
-                                const __half2 h = __floats2half2_rn(y0, y1);
-                                out[j] = *reinterpret_cast<const uint32_t*>(&h);
+                            for (int q = 0; q < 2; ++q) {
+                                const uint4 csv = cbv[c16 * 2 + q];
+                                const uint4 bsv = cbv[4 + c16 * 2 + q];
+                                const uint32_t cw[4] = {csv.x, csv.y, csv.z, csv.w};
+                                const uint32_t bw[4] = {bsv.x, bsv.y, bsv.z, bsv.w};
+#pragma unroll
+                                for (int j = 0; j < 4; ++j) {
+                                    const float2 cs2 = __half22float2(*reinterpret_cast<const __half2*>(&cw[j]));
+                                    const float2 b2 = __half22float2(*reinterpret_cast<const __half2*>(&bw[j]));
+                                    const float2 av = f2_unpack(acc[(c16 * 2 + q) * 4 + j]);
+                                    const float y0 = fmaf(cs2.x, av.x, b2.x);
+                                    const float y1 = fmaf(cs2.y, av.y, b2.y);
+                                    const __half2 h = __floats2half2_rn(y0, y1);
+                                    out[q * 4 + j] = *reinterpret_cast<const uint32_t*>(&h);
+                                }
                             }
-                            *reinterpret_cast<uint4*>(Y + size_t(m) * N + n) =
-                                make_uint4(out[0], out[1], out[2], out[3]);
+                            uint16_t* const dst = Y + size_t(m) * N + n;
+                            if (y32) {
+                                st_global_v8(dst, out);
+                            } else {
+                                reinterpret_cast<uint4*>(dst)[0] = make_uint4(out[0], out[1], out[2], out[3]);
+                                reinterpret_cast<uint4*>(dst)[1] = make_uint4(out[4], out[5], out[6], out[7]);
+                            }
                         }
                     }
                 }

@@ -201,6 +201,13 @@ __device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
 __device__ __forceinline__ void st_release_gpu(uint32_t* p, uint32_t v) {
     asm volatile("st.release.gpu.global.u32 [%0], %1;\n" ::"l"(p), "r"(v) : "memory");
 }
+// One 32-byte store from a thread (p 32-byte aligned): a whole L2 sector, half the
+// store transactions of two 16-byte stores to the same bytes.
+__device__ __forceinline__ void st_global_v8(void* p, const uint32_t (&w)[8]) {
+    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};\n" ::"l"(p), "r"(w[0]), "r"(w[1]),
+                 "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+                 : "memory");
+}
 // Release-ordered increment: this thread's earlier writes are visible to whoever
 // acquires the counter's new value.
 __device__ __forceinline__ void red_add_release_gpu(uint32_t* p, uint32_t v) {
