@@ -291,105 +291,106 @@ __global__ void __launch_bounds__(kWarps * 32) gemm_smallm_kernel(
             if (!DUMP) wait_parity_suspend(aux_full, 0u, &never_abort, kWaitNs, kSuspendNs);
         }
     }
-    if constexpr (DUMP) return;
+    if constexpr (!DUMP) {  // (the partials variant ends with the dump above)
 
-    float acc[NT8][4];
-#pragma unroll
-    for (int t = 0; t < NT8; ++t) {
-        const float2 pa = f2_unpack(acc_a[t]), pb = f2_unpack(acc_b[t]);
-        acc[t][0] = pa.x, acc[t][1] = pa.y, acc[t][2] = pb.x, acc[t][3] = pb.y;
-    }
-    if (KS > 1) {
-        cluster_wait_acquire();  // every rank's barriers are initialised
-        const int orank = warp % KS, ow = warp / KS;  // owner rank, owned-warp index there
-        if (!owner) {
-            // push this warp's partial fragment to the owner of its columns
-            const int slot = (kr < orank ? kr : kr - 1) * (kWarps / KS) + ow;
-            const uint32_t dst = mapa_shared(sbase + PLN.red + uint32_t(slot * 32 + lane) * (NT8 * 16), uint32_t(orank));
-            const uint32_t rbar = mapa_shared(red_full, uint32_t(orank));
-#pragma unroll
-            for (int t = 0; t < NT8; ++t)
-                st_async_v4(dst + uint32_t(t) * 16u, make_float4(acc[t][0], acc[t][1], acc[t][2], acc[t][3]), rbar);
-        } else {
-            const bool ok = warp_wait_parity_suspend(red_full, 0u, abort, kWaitNs, kSuspendNs);
-            if (!ok) {
-                if (lane == 0) {
-                    *abort = 1;
-                    atomicExch(&g_smallm_status, int(W4A4_ERR_TIMEOUT));
-                }
+        float acc[NT8][4];
+    #pragma unroll
+        for (int t = 0; t < NT8; ++t) {
+            const float2 pa = f2_unpack(acc_a[t]), pb = f2_unpack(acc_b[t]);
+            acc[t][0] = pa.x, acc[t][1] = pa.y, acc[t][2] = pb.x, acc[t][3] = pb.y;
+        }
+        if (KS > 1) {
+            cluster_wait_acquire();  // every rank's barriers are initialised
+            const int orank = warp % KS, ow = warp / KS;  // owner rank, owned-warp index there
+            if (!owner) {
+                // push this warp's partial fragment to the owner of its columns
+                const int slot = (kr < orank ? kr : kr - 1) * (kWarps / KS) + ow;
+                const uint32_t dst = mapa_shared(sbase + PLN.red + uint32_t(slot * 32 + lane) * (NT8 * 16), uint32_t(orank));
+                const uint32_t rbar = mapa_shared(red_full, uint32_t(orank));
+    #pragma unroll
+                for (int t = 0; t < NT8; ++t)
+                    st_async_v4(dst + uint32_t(t) * 16u, make_float4(acc[t][0], acc[t][1], acc[t][2], acc[t][3]), rbar);
             } else {
-                const float4* red = reinterpret_cast<const float4*>(smraw + PLN.red);
-                for (int rk = 0; rk < KS; ++rk) {
-                    if (rk == kr) continue;
-                    const int slot = (rk < kr ? rk : rk - 1) * (kWarps / KS) + ow;
-#pragma unroll
-                    for (int t = 0; t < NT8; ++t) {
-                        const float4 v = red[(slot * 32 + lane) * NT8 + t];
-                        acc[t][0] += v.x;
-                        acc[t][1] += v.y;
-                        acc[t][2] += v.z;
-                        acc[t][3] += v.w;
+                const bool ok = warp_wait_parity_suspend(red_full, 0u, abort, kWaitNs, kSuspendNs);
+                if (!ok) {
+                    if (lane == 0) {
+                        *abort = 1;
+                        atomicExch(&g_smallm_status, int(W4A4_ERR_TIMEOUT));
+                    }
+                } else {
+                    const float4* red = reinterpret_cast<const float4*>(smraw + PLN.red);
+                    for (int rk = 0; rk < KS; ++rk) {
+                        if (rk == kr) continue;
+                        const int slot = (rk < kr ? rk : rk - 1) * (kWarps / KS) + ow;
+    #pragma unroll
+                        for (int t = 0; t < NT8; ++t) {
+                            const float4 v = red[(slot * 32 + lane) * NT8 + t];
+                            acc[t][0] += v.x;
+                            acc[t][1] += v.y;
+                            acc[t][2] += v.z;
+                            acc[t][3] += v.w;
+                        }
                     }
                 }
             }
+            cluster_arrive_release();  // this rank's part of the exchange is done
         }
-        cluster_arrive_release();  // this rank's part of the exchange is done
-    }
 
-    // fp16 output tile staged over the group slots, which no warp or copy uses any more
-    // (after a timed-out group wait copies may still land there: nothing is staged then)
-    uint16_t* ys = reinterpret_cast<uint16_t*>(smraw + PLN.wq);
-    constexpr int LDY = kTileN + 8;
-    if (owner && warp_active && !*abort) {
-        const bool ok = r == 0 || warp_wait_parity_suspend(aux_full, 0u, abort, kWaitNs, kSuspendNs);
-        if (!ok && lane == 0) {
-            *abort = 1;
-            atomicExch(&g_smallm_status, int(W4A4_ERR_TIMEOUT));
-        }
-        // LoRA up: acc[n, m] += sum_j L_up[j, n] lora[m, j] (fp16 MMA, fp32 accumulate)
-        const int na_ = n0 + gid, nb_ = n0 + gid + 8;
-        const uint8_t* lu_a = smraw + PLN.lu + (warp * 16 + gid) * 32 + 4 * q;
-        const uint8_t* lu_b = lu_a + 8 * 32;
-        for (int p = 0; ok && p < r / 16; ++p) {
-            uint32_t a[4];
-            a[0] = *reinterpret_cast<const uint32_t*>(lu_a + p * (kTileN * 32) + swz32(na_, 0) * 16);
-            a[2] = *reinterpret_cast<const uint32_t*>(lu_a + p * (kTileN * 32) + swz32(na_, 1) * 16);
-            a[1] = *reinterpret_cast<const uint32_t*>(lu_b + p * (kTileN * 32) + swz32(nb_, 0) * 16);
-            a[3] = *reinterpret_cast<const uint32_t*>(lu_b + p * (kTileN * 32) + swz32(nb_, 1) * 16);
-            const uint8_t* la = smraw + PLN.la + p * (TOK * 32);
-#pragma unroll
+        // fp16 output tile staged over the group slots, which no warp or copy uses any more
+        // (after a timed-out group wait copies may still land there: nothing is staged then)
+        uint16_t* ys = reinterpret_cast<uint16_t*>(smraw + PLN.wq);
+        constexpr int LDY = kTileN + 8;
+        if (owner && warp_active && !*abort) {
+            const bool ok = r == 0 || warp_wait_parity_suspend(aux_full, 0u, abort, kWaitNs, kSuspendNs);
+            if (!ok && lane == 0) {
+                *abort = 1;
+                atomicExch(&g_smallm_status, int(W4A4_ERR_TIMEOUT));
+            }
+            // LoRA up: acc[n, m] += sum_j L_up[j, n] lora[m, j] (fp16 MMA, fp32 accumulate)
+            const int na_ = n0 + gid, nb_ = n0 + gid + 8;
+            const uint8_t* lu_a = smraw + PLN.lu + (warp * 16 + gid) * 32 + 4 * q;
+            const uint8_t* lu_b = lu_a + 8 * 32;
+            for (int p = 0; ok && p < r / 16; ++p) {
+                uint32_t a[4];
+                a[0] = *reinterpret_cast<const uint32_t*>(lu_a + p * (kTileN * 32) + swz32(na_, 0) * 16);
+                a[2] = *reinterpret_cast<const uint32_t*>(lu_a + p * (kTileN * 32) + swz32(na_, 1) * 16);
+                a[1] = *reinterpret_cast<const uint32_t*>(lu_b + p * (kTileN * 32) + swz32(nb_, 0) * 16);
+                a[3] = *reinterpret_cast<const uint32_t*>(lu_b + p * (kTileN * 32) + swz32(nb_, 1) * 16);
+                const uint8_t* la = smraw + PLN.la + p * (TOK * 32);
+    #pragma unroll
+                for (int t = 0; t < NT8; ++t) {
+                    const int rr = t * 8 + gid;  // rr % 8 == (rt0 + rr) % 8
+                    const uint32_t b0 = *reinterpret_cast<const uint32_t*>(la + rr * 32 + swz32(rr, 0) * 16 + 4 * q);
+                    const uint32_t b1 = *reinterpret_cast<const uint32_t*>(la + rr * 32 + swz32(rr, 1) * 16 + 4 * q);
+                    mma_f16_16816(acc[t], a, b0, b1);
+                }
+            }
+            // column affine, fp16
+            const int nl = warp * 16 + gid;
+    #pragma unroll
             for (int t = 0; t < NT8; ++t) {
-                const int rr = t * 8 + gid;  // rr % 8 == (rt0 + rr) % 8
-                const uint32_t b0 = *reinterpret_cast<const uint32_t*>(la + rr * 32 + swz32(rr, 0) * 16 + 4 * q);
-                const uint32_t b1 = *reinterpret_cast<const uint32_t*>(la + rr * 32 + swz32(rr, 1) * 16 + 4 * q);
-                mma_f16_16816(acc[t], a, b0, b1);
+                const int m0 = t * 8 + 2 * q;
+                ys[m0 * LDY + nl] = __half_as_ushort(__float2half_rn(fmaf(csa, acc[t][0], ba)));
+                ys[(m0 + 1) * LDY + nl] = __half_as_ushort(__float2half_rn(fmaf(csa, acc[t][1], ba)));
+                ys[m0 * LDY + nl + 8] = __half_as_ushort(__float2half_rn(fmaf(csb, acc[t][2], bb)));
+                ys[(m0 + 1) * LDY + nl + 8] = __half_as_ushort(__float2half_rn(fmaf(csb, acc[t][3], bb)));
             }
         }
-        // column affine, fp16
-        const int nl = warp * 16 + gid;
-#pragma unroll
-        for (int t = 0; t < NT8; ++t) {
-            const int m0 = t * 8 + 2 * q;
-            ys[m0 * LDY + nl] = __half_as_ushort(__float2half_rn(fmaf(csa, acc[t][0], ba)));
-            ys[(m0 + 1) * LDY + nl] = __half_as_ushort(__float2half_rn(fmaf(csa, acc[t][1], ba)));
-            ys[m0 * LDY + nl + 8] = __half_as_ushort(__float2half_rn(fmaf(csb, acc[t][2], bb)));
-            ys[(m0 + 1) * LDY + nl + 8] = __half_as_ushort(__float2half_rn(fmaf(csb, acc[t][3], bb)));
+        __syncthreads();
+        // store the columns of the warps this rank owns, 16 bytes at a time
+        if (!*abort) {
+            for (int c = threadIdx.x; c < TOK * (kTileN / 8); c += NT) {
+                const int t = c / (kTileN / 8), ch = c % (kTileN / 8);
+                const int m = tok0 + t, n = nbase + ch * 8;
+                if ((ch >> 1) % KS != kr) continue;  // chunk ch belongs to warp ch / 2
+                if (m < M && n < N)
+                    *reinterpret_cast<uint4*>(Y + (size_t)m * N + n) = *reinterpret_cast<const uint4*>(&ys[t * LDY + ch * 8]);
+            }
         }
+        if (r > 0 && threadIdx.x == 0 && !wait_parity_suspend(aux_full, 0u, &never_abort, kWaitNs, kSuspendNs))
+            atomicExch(&g_smallm_status, int(W4A4_ERR_TIMEOUT));  // (the LoRA copies land before the CTA leaves)
+        if (KS > 1) cluster_wait_acquire();  // no rank leaves while a peer may still address its shared memory
     }
-    __syncthreads();
-    // store the columns of the warps this rank owns, 16 bytes at a time
-    if (!*abort) {
-        for (int c = threadIdx.x; c < TOK * (kTileN / 8); c += NT) {
-            const int t = c / (kTileN / 8), ch = c % (kTileN / 8);
-            const int m = tok0 + t, n = nbase + ch * 8;
-            if ((ch >> 1) % KS != kr) continue;  // chunk ch belongs to warp ch / 2
-            if (m < M && n < N)
-                *reinterpret_cast<uint4*>(Y + (size_t)m * N + n) = *reinterpret_cast<const uint4*>(&ys[t * LDY + ch * 8]);
-        }
-    }
-    if (r > 0 && threadIdx.x == 0 && !wait_parity_suspend(aux_full, 0u, &never_abort, kWaitNs, kSuspendNs))
-        atomicExch(&g_smallm_status, int(W4A4_ERR_TIMEOUT));  // (the LoRA copies land before the CTA leaves)
-    if (KS > 1) cluster_wait_acquire();  // no rank leaves while a peer may still address its shared memory
 }
 
 // Split factor: up to two CTAs per SM, so that every SM streams weights with

@@ -62,14 +62,13 @@ constexpr int WARP_MMA = 4, WARP_AUX = 5, WARP_Q0 = 6;
 constexpr int kMaxKS = 8;
 constexpr int kMaxG = 8;     // K groups per CTA
 constexpr int kMaxR = 32;    // LoRA rank
-constexpr int kMaxRing = 8;  // slots of the weight and LoRA-down rings (at most)
 constexpr int kXStride = kMaxG * kGroup + 8;  // halves per staged X row (+8: conflict-free ldmatrix)
 constexpr uint32_t kTmemCols = 256;
 constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr uint32_t kSuspendNs = 20000;
-// named barriers: 1 the quantisation warps; 2 + i the handoff of group i (expansion -> MMA warp);
-// 10 the epilogue warps' staged Y; 11 every thread, once every role is done with tensor memory
-constexpr uint32_t BAR_Q = 1, BAR_G0 = 2, BAR_Y = 2 + kMaxG, BAR_END = 3 + kMaxG;
+// named barriers: 2 + i the handoff of group i (expansion -> MMA warp); 10 the epilogue
+// warps' staged Y; 11 every thread, once every role is done with tensor memory
+constexpr uint32_t BAR_G0 = 2, BAR_Y = 2 + kMaxG, BAR_END = 3 + kMaxG;
 constexpr uint32_t kHandoff = 5 * 32;  // four expansion warps arrive, the MMA warp syncs
 
 __device__ int g_fused_status = 0;
