@@ -281,19 +281,19 @@ def kernel_source_hash(name: str) -> str:
 # counters no longer describe it and traffic is reported as null.
 NCU_TRAFFIC = {
     # the four decoder-layer GEMM launches (qkv, o, gate_up, down) at M = 700, one launch each,
-    # read from HBM (24 input replicas cycled): 3,501,824 + 3,066,112 + 4,747,520 + 4,508,416 bytes read,
-    # 512 written; Y stays in L2 within a launch (profiles/gemm_tc_traffic_decoder_layer_m700.md)
-    (WORKLOAD, "b7ecf7ca82e1c185"): {
-        "bytes_per_pass": 15824384,
-        "per_linear": {"qkv": 3502336, "o": 3066112, "gate_up": 4747520, "down": 4508416},
+    # read from HBM (24 input replicas cycled): 3,501,056 + 3,065,856 + 4,747,520 + 4,507,904 bytes read,
+    # none written; Y stays in L2 within a launch (profiles/gemm_tc_traffic_decoder_layer_m700.md)
+    (WORKLOAD, "958dd4c4b0f2e294"): {
+        "bytes_per_pass": 15822336,
+        "per_linear": {"qkv": 3501056, "o": 3065856, "gate_up": 4747520, "down": 4507904},
         "source": "ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum, one launch per linear "
                   "(profiles/gemm_tc_traffic_decoder_layer_m700.md)"},
     # the M = 8192 GEMMs, two launches per linear (the full rounds, then the last round split over K):
-    # 4096 -> 14336 75.59 + 14.70 MB read, 198.38 MB written; 14336 -> 4096 160.56 + 37.77 MB read,
-    # 51.85 MB written (profiles/gemm_tc_prefill_m8192.md)
-    (PREFILL_WORKLOAD, "b7ecf7ca82e1c185"): {
-        "bytes_per_pass": 288672768 + 250180352,
-        "per_linear": {"gate_up_style": 288672768, "down_style": 250180352},
+    # 4096 -> 14336 71.77 + 14.70 MB read, 208.04 MB written; 14336 -> 4096 160.96 + 37.75 MB read,
+    # 53.07 MB written (profiles/gemm_tc_prefill_m8192.md)
+    (PREFILL_WORKLOAD, "958dd4c4b0f2e294"): {
+        "bytes_per_pass": 294509824 + 251788288,
+        "per_linear": {"gate_up_style": 294509824, "down_style": 251788288},
         "source": "ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum, both launches of each linear "
                   "(profiles/gemm_tc_prefill_m8192.md)"},
 }
