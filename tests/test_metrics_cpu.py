@@ -106,3 +106,17 @@ def test_bench_traffic_is_tied_to_the_kernel_source_it_was_measured_on():
     else:
         assert got["bytes_per_pass"] == sum(rec["per_linear"].values())
     assert bench.ncu_traffic("no such workload") is None
+
+
+def test_gemm_launch_count_per_schedule():
+    """gpu_launches counts two GEMM launches for a call whose last round of tiles runs in a
+    launch of its own, one for every other schedule (the inline split of that round included)."""
+    import bench
+    second = ("gemm_tc tcgen05.f8f6f4 tile=128x128 groups/job=2 stages=4 tiles=2048: 1976 round-robin, last 72 "
+              "split-K=2 (cluster) N-tiles-fastest")
+    inline = ("gemm_tc tcgen05.f8f6f4 tile=128x128 groups/job=2 stages=3 tiles=192: 152 whole, last 40 split-K=2 "
+              "in the same launch (cluster)")
+    plain = "gemm_tc tcgen05.f8f6f4 tile=128x128 groups/job=2 stages=3 split-K=2 (cluster) tiles=48 grid=96"
+    assert bench.gemm_launches(second) == 2
+    assert bench.gemm_launches(inline) == 1
+    assert bench.gemm_launches(plain) == 1
